@@ -1,0 +1,125 @@
+"""Seeded synthetic inputs shared by the tests, the bench and the smoke check.
+
+This module holds none of the attention arithmetic: it only draws random
+tensors. The CUDA path and the CPU oracle both receive exactly the tensors it
+returns, so neither side generates its own inputs.
+
+The pages name no dataset; their long-context workloads (books of 100K+
+tokens, hidden size 4096 in the glossary "sequence parallelism transformers",
+§Sequence Parallelism Fundamentals and §Use Cases) are stood in for by the
+named shapes below, with Gaussian queries/keys/values.
+
+Recipe (every tensor drawn on the CPU with ``torch.Generator().manual_seed``):
+draw q, then k, then v, each float32 N(0, std^2) in [B, S, H, D] order; for
+the GQA workload add +3.0 to every odd sequence row of k (all heads, all
+components) before the cast; cast to the target dtype with round-to-nearest-
+even (``Tensor.to``). Merge partials: n float32 N(0, 1) outputs [B, S, H, D],
+then n lse tensors U(-20, 20) [B, H, S].
+"""
+
+from dataclasses import dataclass, replace
+import math
+
+import torch
+
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    name: str
+    dtype: str          # "bf16" or "f32"
+    B: int
+    H_q: int
+    H_kv: int
+    S: int
+    D: int
+    P: int
+    causal: bool
+    order: str          # "contiguous" or "zigzag"
+    std: float = 1.0
+    k_shift_odd: float = 0.0
+    seed: int = 0
+
+    @property
+    def scale(self):
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def flop(self):
+        """Algorithmic FLOP: 4*B*H_q*S^2*D, halved under the causal mask."""
+        f = 4.0 * self.B * self.H_q * self.S * self.S * self.D
+        return f / 2 if self.causal else f
+
+    def scaled(self, **kw):
+        return replace(self, **kw)
+
+
+@dataclass(frozen=True)
+class MergeWorkload:
+    name: str
+    dtype: str
+    n: int
+    B: int
+    H: int
+    S: int
+    D: int
+    lse_range: float = 20.0
+    seed: int = 0
+
+    @property
+    def bytes(self):
+        """Algorithmic bytes of one N-way merge: read n partials, write one."""
+        esz = 4 if self.dtype == "f32" else 2
+        rows = self.B * self.H * self.S
+        return rows * (self.n + 1) * (self.D * esz + 4)
+
+
+WORKLOADS = {
+    "fp32_s256": AttnWorkload("fp32_s256", "f32", 1, 2, 2, 256, 64, 4, False,
+                              "contiguous", seed=1001),
+    "bf16_s4k_causal": AttnWorkload("bf16_s4k_causal", "bf16", 2, 16, 16, 4096,
+                                    128, 8, True, "contiguous", seed=1002),
+    "bf16_s32k_causal_zigzag": AttnWorkload(
+        "bf16_s32k_causal_zigzag", "bf16", 1, 32, 32, 32768, 128, 8, True,
+        "zigzag", std=0.5, seed=1003),
+    "bf16_s128k_gqa_causal": AttnWorkload(
+        "bf16_s128k_gqa_causal", "bf16", 1, 32, 8, 131072, 128, 16, True,
+        "contiguous", k_shift_odd=3.0, seed=1004),
+    "bf16_s16k_d64": AttnWorkload("bf16_s16k_d64", "bf16", 4, 16, 16, 16384,
+                                  64, 4, False, "contiguous", seed=1006),
+}
+
+MERGE_WORKLOADS = {
+    "merge_p8_s64k": MergeWorkload("merge_p8_s64k", "f32", 8, 1, 32, 65536, 128,
+                                   seed=1005),
+}
+
+HEADLINE = "bf16_s32k_causal_zigzag"
+
+_TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def torch_dtype(name):
+    return _TORCH_DTYPE[name]
+
+
+def make_qkv(w: AttnWorkload):
+    """(q, k, v) CPU tensors of ``w``'s dtype, drawn with ``w.seed``."""
+    g = torch.Generator().manual_seed(w.seed)
+    q = torch.randn(w.B, w.S, w.H_q, w.D, generator=g) * w.std
+    k = torch.randn(w.B, w.S, w.H_kv, w.D, generator=g) * w.std
+    v = torch.randn(w.B, w.S, w.H_kv, w.D, generator=g) * w.std
+    if w.k_shift_odd:
+        k[:, 1::2] += w.k_shift_odd
+    dt = _TORCH_DTYPE[w.dtype]
+    return q.to(dt), k.to(dt), v.to(dt)
+
+
+def make_merge_parts(w: MergeWorkload):
+    """(list of n outputs [B,S,H,D], list of n lse [B,H,S]) CPU tensors."""
+    g = torch.Generator().manual_seed(w.seed)
+    dt = _TORCH_DTYPE[w.dtype]
+    os_ = [torch.randn(w.B, w.S, w.H, w.D, generator=g).to(dt)
+           for _ in range(w.n)]
+    lses = [(torch.rand(w.B, w.H, w.S, generator=g) * 2 - 1) * w.lse_range
+            for _ in range(w.n)]
+    return os_, lses
