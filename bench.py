@@ -1,0 +1,360 @@
+#!/usr/bin/env python
+"""Throughput of exact ring attention on GB300; prints one JSON line.
+
+Default workload: bf16, causal, B=1, H=32, S=32768, D=128, P=8 virtual ranks
+in zig-zag order (the long-context headline shape). One step = one call of
+``ring_attn_fwd_ex`` = all P ring steps of every virtual rank, fused in one
+kernel launch. The metric is algorithmic TFLOP/s (2*B*H*S^2*D for causal).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (the method needs no exchange on one device: "replicas only");
+``value`` is the FLOP of all ranks over the slowest rank's time.
+``--impl reference`` times the float64 CPU oracle on a bounded row sample of
+the same workload (rank 0 only).
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ring-attn fwd TFLOP/s, bf16 S=32K causal, 1 GB300; % of dense BF16 peak"
+UNIT = "TFLOP/s"
+
+# ncu DRAM bytes (read + write) of one launch of the tensor-core kernel on the
+# headline workload, valid only for the kernel source with this digest.
+TRAFFIC = {"attn_tc_sha256_16": None, "bytes_per_launch": None}
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def _kernel_digest():
+    path = os.path.join(ROOT, "sequence_exact_attention_gb300", "csrc", "attn_tc.cu")
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        # under load: samples with power above the midpoint of the range
+        if power:
+            thr = (min(power) + max(power)) / 2
+            loaded = [num(r[1]) for r in rows if num(r[3]) is not None and num(r[3]) >= thr]
+        else:
+            loaded = sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def _dist_setup(n_gpus):
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=None)
+        return world, rank, local, dist
+    return 1, 0, local, None
+
+
+def _oracle_sample_rate(w, q, k, v, n_rows, seed):
+    """float64 oracle on n_rows sampled query rows (all heads); returns
+    (TFLOP/s by the algorithmic count of those rows, seconds, rows)."""
+    import numpy as np
+    import oracle
+    rows = np.sort(np.random.default_rng(seed).choice(w.S, n_rows, replace=False))
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.causal, w.scale, rows)
+    dt = time.perf_counter() - t0
+    pairs = float((rows + 1).sum()) if w.causal else float(n_rows * w.S)
+    flop = 4.0 * w.D * pairs * w.B * w.H_q
+    return flop / dt / 1e12, dt, rows
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def run_reference(args, w):
+    world, rank, _, _ = _dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    from sequence_exact_attention_gb300.workloads import make_qkv
+    q, k, v = make_qkv(w)
+    rows_per_step = args.ref_rows
+    for i in range(args.warmup):
+        _oracle_sample_rate(w, q, k, v, rows_per_step, seed=100 + i)
+    total_flop, total_t = 0.0, 0.0
+    for i in range(args.steps):
+        rate, dt, rows = _oracle_sample_rate(w, q, k, v, rows_per_step, seed=1000 + i)
+        total_flop += rate * dt * 1e12
+        total_t += dt
+    value = total_flop / total_t / 1e12
+    cores = _blas_threads()
+    sample = (f"{rows_per_step} random query rows x all {w.H_q} heads per step "
+              f"(float64 NumPy oracle, full key range per row)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(w):
+    return {"workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "S": w.S,
+            "D": w.D, "P": w.P, "causal": w.causal, "order": w.order,
+            "input_dist": f"N(0,{w.std}^2) bf16" if w.dtype == "bf16" else "N(0,1) f32",
+            "l2": "inputs larger than L2 (q, k, v 256 MiB each vs 126 MiB L2)",
+            "parallelism": "replicas"}
+
+
+def run_ours(args, w):
+    import torch
+    from sequence_exact_attention_gb300 import binding
+    from sequence_exact_attention_gb300.workloads import make_qkv
+
+    world, rank, local, dist = _dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    try:
+        binding.load()
+    except RuntimeError:
+        from sequence_exact_attention_gb300 import build
+        build.build()
+        binding.load()
+
+    q, k, v = make_qkv(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty(w.B, w.S, w.H_q, w.D, dtype=qd.dtype, device=dev)
+    lse = torch.empty(w.B, w.H_q, w.S, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        binding.ring_attn_fwd(qd, kd, vd, w.P, w.causal, w.scale, w.order, out=out,
+                              lse=lse, dev_status=status, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError("device-side wait expired during warm-up")
+
+    # ---- device-timed region: inputs resident in HBM
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if int(status.item()) != 0:
+        raise RuntimeError("device-side wait expired in the timed region")
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flop = w.flop
+    value = world * flop * args.steps / (total_ms / 1e3) / 1e12
+    kernel_ms = statistics.mean(launch_ms)
+
+    # ---- end to end through the public API, host buffers, copies timed
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        step()
+        oh.copy_(out, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_val = world * flop * args.steps / (e2e_ms / 1e3) / 1e12
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = _peaks()
+    peak = float(peaks.get("bf16_tflops"))
+    achieved = flop / (kernel_ms / 1e3) / 1e12
+    digest = _kernel_digest()
+    traffic = (TRAFFIC["bytes_per_launch"]
+               if TRAFFIC["attn_tc_sha256_16"] == digest else None)
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n_rows = args.cpu_rows
+        rate, dt, _ = _oracle_sample_rate(w, q, k, v, n_rows, seed=7)
+        cpu = {"value": rate, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+               "sample": f"{n_rows} random query rows x all {w.H_q} heads of the same "
+                         f"workload, float64 NumPy oracle, {dt:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": _config(w),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "kernel": "attn_tc_kernel<128,false>",
+                     "kernel_ms": kernel_ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "clocks": clk,
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    from sequence_exact_attention_gb300.workloads import WORKLOADS, HEADLINE
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-rows", type=int, default=192)
+    ap.add_argument("--ref-rows", type=int, default=24)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

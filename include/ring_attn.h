@@ -1,0 +1,197 @@
+/*
+ * ring_attn.h - C ABI of the GB300 (sm_103a) exact ring-attention library.
+ *
+ * What it computes. Glossary "sequence parallelism transformers":
+ *  - §Sequence Parallelism Fundamentals ("Sequence Dimension Splitting"): the
+ *    length-S sequence is cut into P chunks, one per rank. Here the ranks are
+ *    virtual: all P live on the one GPU running the call.
+ *  - §Ring Attention: each rank keeps its query block; at step t it attends
+ *    to the key/value block that started on rank (r - t) mod P (blocks move
+ *    from rank i to i+1 each step) and accumulates the outputs; after P
+ *    steps the result equals full softmax attention.
+ *  - §Implementation Considerations ("Numerical Stability", "Load
+ *    Balancing"): partial results are combined with an exact log-sum-exp
+ *    merge; the zig-zag chunk order (2P halves, rank r owns halves r and
+ *    2P-1-r) balances causal work across ranks.
+ * Divisibility follows the nvFuser PR "Transformer sequence parallel
+ * forward" (a sequence-parallel case with s % d != 0 is skipped) and the
+ * mvp-engine "sequence-parallel" skill (seq_len divisible by the split, else
+ * pad explicitly): S % P != 0, or S % 2P != 0 in zig-zag order, is an error.
+ *
+ * For each batch b, query head h and query position i, with key/value head
+ * hk = h / (H_q / H_kv) and allowed keys A(i) = {0..S-1} (non-causal) or
+ * {0..i} (causal, global positions):
+ *     lse[b,h,i] = log sum_{j in A(i)} exp(scale * <q_i, k_j>)      (natural log)
+ *     out[b,i,h] = sum_{j in A(i)} exp(scale * <q_i, k_j> - lse) * v_j
+ *
+ * Layouts (all row-major, contiguous, "BSHD": sequence is dimension 1):
+ *     q, out      [B, S, H_q,  D]
+ *     k, v        [B, S, H_kv, D]
+ *     lse         [B, H_q, S]            float32
+ * Element types: RA_BF16 (bfloat16 in and out, float32 accumulation) or
+ * RA_F32 (float32 throughout).
+ *
+ * Conventions shared by every entry point:
+ *  - Every data pointer is a DEVICE pointer on the current CUDA device, owned
+ *    by the caller. Tensor pointers (q, k, v, out, o_*) are 16-byte aligned;
+ *    lse, visit logs and status words 4-byte aligned (else RA_ERR_ALIGN).
+ *    The library allocates no device memory and keeps no state between calls
+ *    except read-only per-device facts.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Calls enqueue work and return; they never synchronise.
+ *  - Arguments are checked on the host before anything is enqueued; on error
+ *    nothing is launched and the status says why. A failed launch returns
+ *    RA_ERR_LAUNCH. A device-side bounded wait that expired is reported in
+ *    `dev_status` (where the call takes one) as RA_ERR_TIMEOUT, after the
+ *    stream has run the kernel.
+ *  - `scale <= 0` means 1/sqrt(D).
+ *  - Tensors stay in natural token order in every chunk order: the order only
+ *    decides which virtual rank owns which tokens and the sequence of steps.
+ */
+#ifndef RING_ATTN_H
+#define RING_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_NULL = 1,     /* a required pointer is NULL                              */
+  RA_ERR_SHAPE = 2,    /* size <= 0, S % P, S % 2P (zig-zag), H_q % H_kv, n range */
+  RA_ERR_HEADDIM = 3,  /* D is not 64 or 128                                       */
+  RA_ERR_ALIGN = 4,    /* a data pointer is not 16-byte aligned                    */
+  RA_ERR_DTYPE = 5,    /* unknown dtype or order value                             */
+  RA_ERR_DEVICE = 6,   /* current device is not compute capability 10.3            */
+  RA_ERR_LAUNCH = 7,   /* CUDA runtime error while preparing or launching          */
+  RA_ERR_TIMEOUT = 8,  /* a device-side bounded wait expired (dev_status only)     */
+  RA_ERR_BUFFER = 9,   /* a caller buffer is too small                             */
+  RA_ERR_RANGE = 10    /* a size overflows 32-bit indexing, or step out of range   */
+} ra_status;
+
+typedef enum { RA_BF16 = 0, RA_F32 = 1 } ra_dtype;
+typedef enum { RA_ORDER_CONTIGUOUS = 0, RA_ORDER_ZIGZAG = 1 } ra_order;
+
+/* Classes of a (query set, key set) pair under the causal rule j <= i. */
+enum { RA_CLASS_SKIP = 0, RA_CLASS_FULL = 1, RA_CLASS_PARTIAL = 2 };
+
+/* Largest n accepted by attn_lse_merge_n. */
+#define RA_MERGE_MAX_N 16
+
+/*
+ * ring_attn_fwd - exact attention computed as a ring of P virtual ranks,
+ * bfloat16 inputs and output, contiguous chunk order.
+ *
+ * All P ring steps run inside one kernel launch: every query tile keeps its
+ * running (max, sum, unnormalised output) on chip across steps, which is the
+ * log-sum-exp merge of the per-step partials done in registers. Under a
+ * causal mask, key tiles that lie entirely after the query tile are skipped.
+ * `lse` may be NULL (not written). Errors: RA_ERR_NULL (q, k, v or out NULL),
+ * RA_ERR_SHAPE, RA_ERR_HEADDIM, RA_ERR_ALIGN, RA_ERR_RANGE (B*S*H*D beyond
+ * 2^31 elements per tensor), RA_ERR_DEVICE, RA_ERR_LAUNCH.
+ */
+ra_status ring_attn_fwd(const void* q, const void* k, const void* v,
+                        void* out, float* lse,
+                        int B, int H_q, int H_kv, int S, int D, int P,
+                        int causal, float scale, void* stream);
+
+/*
+ * ring_attn_fwd_ex - ring_attn_fwd with every option.
+ *
+ * dtype   RA_BF16 (tensor-core path) or RA_F32 (exact float32 CUDA-core path).
+ * order   RA_ORDER_CONTIGUOUS (rank r owns [rS/P, (r+1)S/P)) or
+ *         RA_ORDER_ZIGZAG (rank r owns halves r and 2P-1-r of length S/2P).
+ * step    -1: all P steps, folded on chip (same result as ring_attn_fwd).
+ *         t in [0, P): ring step t only. Every rank r attends to the chunk of
+ *         rank (r - t) mod P and the call writes that step's PARTIAL result:
+ *         `out` is then float32 [B, S, H_q, D] whatever `dtype` is, and `lse`
+ *         (required) is the partial lse; rows with no allowed key in that
+ *         chunk get out = 0 and lse = -inf. Folding the P partials with
+ *         attn_lse_merge / attn_lse_merge_n gives the full result.
+ * visit_log  NULL, or a device int32 buffer of ring_attn_visit_log_len(...)
+ *         elements: for every (b, h, query tile) the key tiles the kernel
+ *         visited, in visit order (layout at ring_attn_visit_log_len).
+ * dev_status NULL, or a device int the kernel sets to RA_ERR_TIMEOUT if one of
+ *         its bounded waits expired (it is never cleared by the library; the
+ *         caller zeroes it).
+ */
+ra_status ring_attn_fwd_ex(const void* q, const void* k, const void* v,
+                           void* out, float* lse,
+                           int B, int H_q, int H_kv, int S, int D, int P,
+                           int causal, float scale,
+                           int dtype, int order, int step,
+                           int* visit_log, int* dev_status, void* stream);
+
+/*
+ * ring_attn_visit_log_len - size of the visit log of ring_attn_fwd_ex.
+ *
+ * The kernel for `dtype` cuts every chunk (contiguous) or half (zig-zag) of
+ * length L into query and key tiles of `*tile_rows` rows (the last one shorter
+ * when L is not a multiple). Tiles are numbered globally: the segment's index
+ * in position order times `*tiles_per_segment` plus the tile's index in it.
+ * The log holds, for each (b, h, query tile id), `*stride` ints: the number
+ * of visits n, then n entries of 4 ints (step, source rank, key tile id,
+ * class). Total length = B * H_q * n_query_tiles * stride, returned in *len.
+ * Host-only; never touches the GPU.
+ */
+ra_status ring_attn_visit_log_len(int B, int H_q, int S, int D, int P,
+                                  int dtype, int order,
+                                  int* tile_rows, int* tiles_per_segment,
+                                  int* n_query_tiles, int* stride,
+                                  long long* len);
+
+/*
+ * attn_lse_merge - exact merge of two partial attention results over
+ * disjoint key sets (glossary "sequence parallelism transformers",
+ * §Ring Attention and §Implementation Considerations):
+ *     lse = log(exp(lse_a) + exp(lse_b))
+ *     out = exp(lse_a - lse) * o_a + exp(lse_b - lse) * o_b
+ * evaluated with the larger lse factored out. A side with lse = -inf
+ * contributes nothing; both -inf gives out = 0, lse = -inf.
+ * o_a, o_b, out: [B, S, H, D] of `dtype`; lse_a, lse_b, lse: float32
+ * [B, H, S]. `out` may alias o_a or o_b and `lse` may alias lse_a or lse_b
+ * (each element is read before it is written, by the same thread).
+ */
+ra_status attn_lse_merge(const void* o_a, const float* lse_a,
+                         const void* o_b, const float* lse_b,
+                         void* out, float* lse,
+                         int B, int H, int S, int D, int dtype, void* stream);
+
+/*
+ * attn_lse_merge_n - the same merge over n partials in one pass
+ * (1 <= n <= RA_MERGE_MAX_N):
+ *     lse = M + log sum_t exp(lse_t - M),  M = max_t lse_t
+ *     out = sum_t exp(lse_t - lse) * o_t
+ * `o` and `lse` are HOST arrays of n device pointers. Aliasing as for
+ * attn_lse_merge. D is 32, 64, 128 or 256 here.
+ */
+ra_status attn_lse_merge_n(const void* const* o, const float* const* lse,
+                           int n, void* out, float* out_lse,
+                           int B, int H, int S, int D, int dtype, void* stream);
+
+/*
+ * ring_attn_plan - the ring schedule as an int32 table, host only.
+ * One row of RA_PLAN_COLS ints per (rank, step), rank-major then step:
+ *   rank, step, src = (rank - step) mod P, class of the whole (query chunk,
+ *   key chunk) pair, segment length, first and second query segment starts,
+ *   first and second key segment starts (-1 where a rank owns one segment).
+ * `table_len` is the capacity in ints (>= P*P*RA_PLAN_COLS, else
+ * RA_ERR_BUFFER). Never touches the GPU.
+ */
+#define RA_PLAN_COLS 9
+ra_status ring_attn_plan(int S, int P, int causal, int order,
+                         int* table, size_t table_len);
+
+/* Human-readable text of a status; never NULL. */
+const char* ring_attn_strerror(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int ring_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RING_ATTN_H */

@@ -57,6 +57,34 @@ def _rows_softmax(scores):
     return lse, w
 
 
+def _attend(q_rows, k, v, causal, scale, q_pos, kv_pos):
+    """Attention of the query rows ``q_rows`` [B, n, H_q, D] (at global
+    positions ``q_pos``) over the keys at ``kv_pos`` only."""
+    q_rows, k, v = f64(q_rows), f64(k), f64(v)
+    B, n, H_q, D = q_rows.shape
+    H_kv = k.shape[2]
+    g = _group(H_q, H_kv)
+    q_pos = np.asarray(q_pos, dtype=np.int64)
+    kv_pos = np.asarray(kv_pos, dtype=np.int64)
+    out = np.zeros((B, n, H_q, D))
+    lse = np.full((B, H_q, n), -np.inf)
+    if n == 0 or len(kv_pos) == 0:
+        return out, lse
+    allowed = None
+    if causal:
+        allowed = kv_pos[None, :] <= q_pos[:, None]
+    for b in range(B):
+        for h in range(H_q):
+            hk = h // g
+            s = scale * (q_rows[b, :, h, :] @ k[b, kv_pos, hk, :].T)
+            if allowed is not None:
+                s = np.where(allowed, s, -np.inf)
+            l_row, w = _rows_softmax(s)
+            lse[b, h, :] = l_row
+            out[b, :, h, :] = w @ v[b, kv_pos, hk, :]
+    return out, lse
+
+
 def partial_attention(q, k, v, causal, scale, q_pos, kv_pos):
     """Attention of the queries at ``q_pos`` over the keys at ``kv_pos`` only.
 
@@ -67,40 +95,20 @@ def partial_attention(q, k, v, causal, scale, q_pos, kv_pos):
     o [B, len(q_pos), H_q, D] and lse [B, H_q, len(q_pos)], float64; a query
     row with no allowed key in this set gets o = 0 and lse = -inf.
     """
-    q, k, v = f64(q), f64(k), f64(v)
-    B, _, H_q, D = q.shape
-    H_kv = k.shape[2]
-    g = _group(H_q, H_kv)
     q_pos = np.asarray(q_pos, dtype=np.int64)
-    kv_pos = np.asarray(kv_pos, dtype=np.int64)
-    out = np.zeros((B, len(q_pos), H_q, D))
-    lse = np.full((B, H_q, len(q_pos)), -np.inf)
-    if len(q_pos) == 0 or len(kv_pos) == 0:
-        return out, lse
-    allowed = None
-    if causal:
-        allowed = kv_pos[None, :] <= q_pos[:, None]
-    for b in range(B):
-        for h in range(H_q):
-            hk = h // g
-            s = scale * (q[b, q_pos, h, :] @ k[b, kv_pos, hk, :].T)
-            if allowed is not None:
-                s = np.where(allowed, s, -np.inf)
-            l_row, w = _rows_softmax(s)
-            lse[b, h, :] = l_row
-            out[b, :, h, :] = w @ v[b, kv_pos, hk, :]
-    return out, lse
+    return _attend(q[:, q_pos], k, v, causal, scale, q_pos, kv_pos)
 
 
 def attention_rows(q, k, v, causal, scale, rows):
     """Full attention for a subset of query positions ``rows`` (all heads).
 
     Used to check large problems on sampled outputs: each row is computed on
-    its own from the definition, over all S keys.
+    its own from the definition, over all S keys. Only the sampled rows of q
+    are converted to float64.
     """
-    k64 = f64(k)
-    S = k64.shape[1]
-    return partial_attention(q, k64, v, causal, scale, rows, np.arange(S))
+    rows = np.asarray(rows, dtype=np.int64)
+    S = k.shape[1]
+    return _attend(q[:, rows], k, v, causal, scale, rows, np.arange(S))
 
 
 def attention_naive(q, k, v, causal, scale, row_block=1024):

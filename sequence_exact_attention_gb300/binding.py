@@ -1,0 +1,221 @@
+"""ctypes binding of the C-ABI library (``include/ring_attn.h``).
+
+Argument marshalling only: tensors become device pointers and sizes, the
+current torch stream becomes the ``stream`` argument, a non-zero status
+becomes ``RingAttnError``. Every step of the computation runs in the CUDA
+kernels of ``_lib/libringattn.so``; there is no fallback of any kind, and a
+missing library raises at the first call.
+"""
+
+import ctypes
+import math
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libringattn.so")
+
+RA_BF16, RA_F32 = 0, 1
+ORDERS = {"contiguous": 0, "zigzag": 1}
+PLAN_COLS = 9
+MERGE_MAX_N = 16
+
+# every entry point declared in include/ring_attn.h
+EXPORTS = ("ring_attn_fwd", "ring_attn_fwd_ex", "ring_attn_visit_log_len",
+           "attn_lse_merge", "attn_lse_merge_n", "ring_attn_plan",
+           "ring_attn_strerror", "ring_attn_version")
+
+_lib = None
+
+
+class RingAttnError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {strerror(status)} (status {status})")
+
+
+def load():
+    """Load the shared library once; raises if it was not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -m sequence_exact_attention_gb300.build` (no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    c_int, c_float, vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.ring_attn_fwd.restype = c_int
+    lib.ring_attn_fwd.argtypes = [vp, vp, vp, vp, vp] + [c_int] * 7 + [c_float, vp]
+    lib.ring_attn_fwd_ex.restype = c_int
+    lib.ring_attn_fwd_ex.argtypes = ([vp, vp, vp, vp, vp] + [c_int] * 7 + [c_float]
+                                     + [c_int] * 3 + [vp, vp, vp])
+    lib.ring_attn_visit_log_len.restype = c_int
+    lib.ring_attn_visit_log_len.argtypes = [c_int] * 7 + [ip, ip, ip, ip,
+                                                          ctypes.POINTER(ctypes.c_longlong)]
+    lib.attn_lse_merge.restype = c_int
+    lib.attn_lse_merge.argtypes = [vp] * 6 + [c_int] * 5 + [vp]
+    lib.attn_lse_merge_n.restype = c_int
+    lib.attn_lse_merge_n.argtypes = [vp, vp, c_int, vp, vp] + [c_int] * 5 + [vp]
+    lib.ring_attn_plan.restype = c_int
+    lib.ring_attn_plan.argtypes = [c_int, c_int, c_int, c_int, ip, ctypes.c_size_t]
+    lib.ring_attn_strerror.restype = ctypes.c_char_p
+    lib.ring_attn_strerror.argtypes = [c_int]
+    lib.ring_attn_version.restype = c_int
+    lib.ring_attn_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def strerror(status):
+    return load().ring_attn_strerror(int(status)).decode()
+
+
+def _check(status, where):
+    if status != 0:
+        raise RingAttnError(status, where)
+
+
+# ------------------------------------------------------------------ host-only
+
+def ring_attn_plan(S, P, causal, order="contiguous"):
+    """The ring schedule table, int32 [P*P, 9] (see ring_attn_plan in the header)."""
+    lib = load()
+    n = P * P * PLAN_COLS
+    buf = (ctypes.c_int * n)()
+    _check(lib.ring_attn_plan(S, P, int(bool(causal)), ORDERS[order], buf, n),
+           "ring_attn_plan")
+    return np.frombuffer(buf, dtype=np.int32).reshape(P * P, PLAN_COLS).copy()
+
+
+def visit_log_layout(B, H_q, S, D, P, dtype, order="contiguous"):
+    """dict(tile_rows, tiles_per_segment, n_query_tiles, stride, len)."""
+    lib = load()
+    vals = [ctypes.c_int() for _ in range(4)]
+    ln = ctypes.c_longlong()
+    _check(lib.ring_attn_visit_log_len(B, H_q, S, D, P, _dtype_code(dtype),
+                                       ORDERS[order], *[ctypes.byref(x) for x in vals],
+                                       ctypes.byref(ln)), "ring_attn_visit_log_len")
+    keys = ("tile_rows", "tiles_per_segment", "n_query_tiles", "stride")
+    out = {k: v.value for k, v in zip(keys, vals)}
+    out["len"] = ln.value
+    return out
+
+
+# ------------------------------------------------------------------ tensors
+
+def _dtype_code(dt):
+    import torch
+    if dt in (torch.bfloat16, "bf16"):
+        return RA_BF16
+    if dt in (torch.float32, "f32"):
+        return RA_F32
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def ring_attn_fwd(q, k, v, P, causal, scale=None, order="contiguous", step=-1,
+                  out=None, lse=None, want_lse=True, visit_log=None,
+                  dev_status=None, stream=None):
+    """Ring attention of q [B,S,H_q,D], k/v [B,S,H_kv,D] (CUDA tensors).
+
+    Returns (out, lse). bf16 inputs run on the tensor-core kernel, float32 on
+    the exact CUDA-core kernel. With ``step`` = t >= 0 only ring step t runs
+    and (out, lse) are that step's float32 partial result.
+    """
+    import torch
+    lib = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dev(t, n)
+    B, S, H_q, D = q.shape
+    H_kv = k.shape[2]
+    if k.shape != (B, S, H_kv, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, S, H_kv, D] matching q")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share a dtype")
+    code = _dtype_code(q.dtype)
+    out_dtype = torch.float32 if step >= 0 else q.dtype
+    if out is None:
+        out = torch.empty(B, S, H_q, D, device=q.device, dtype=out_dtype)
+    if lse is None and (want_lse or step >= 0):
+        lse = torch.empty(B, H_q, S, device=q.device, dtype=torch.float32)
+    for t, n in ((out, "out"), (lse, "lse"), (visit_log, "visit_log"),
+                 (dev_status, "dev_status")):
+        if t is not None:
+            _dev(t, n)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    st = lib.ring_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                              B, H_q, H_kv, S, D, P, int(bool(causal)), sc,
+                              code, ORDERS[order], int(step), _ptr(visit_log),
+                              _ptr(dev_status), _stream(stream))
+    _check(st, "ring_attn_fwd_ex")
+    return out, lse
+
+
+def ring_attn_fwd_plain(q, k, v, out, lse, P, causal, scale=None, stream=None):
+    """The plain ``ring_attn_fwd`` entry point (bf16, contiguous order)."""
+    lib = load()
+    B, S, H_q, D = q.shape
+    H_kv = k.shape[2]
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    st = lib.ring_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                           B, H_q, H_kv, S, D, P, int(bool(causal)), sc,
+                           _stream(stream))
+    _check(st, "ring_attn_fwd")
+    return out, lse
+
+
+def attn_lse_merge(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
+    """Pairwise merge; o_* [B,S,H,D], lse_* [B,H,S] float32."""
+    import torch
+    lib = load()
+    for t, n in ((o_a, "o_a"), (o_b, "o_b"), (lse_a, "lse_a"), (lse_b, "lse_b")):
+        _dev(t, n)
+    B, S, H, D = o_a.shape
+    if out is None:
+        out = torch.empty_like(o_a)
+    if lse is None:
+        lse = torch.empty_like(lse_a)
+    st = lib.attn_lse_merge(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b),
+                            _ptr(out), _ptr(lse), B, H, S, D,
+                            _dtype_code(o_a.dtype), _stream(stream))
+    _check(st, "attn_lse_merge")
+    return out, lse
+
+
+def attn_lse_merge_n(os_, lses, out=None, lse=None, stream=None):
+    """N-way merge of lists of partials (one pass)."""
+    import torch
+    lib = load()
+    n = len(os_)
+    for t in list(os_) + list(lses):
+        _dev(t, "partial")
+    B, S, H, D = os_[0].shape
+    if out is None:
+        out = torch.empty_like(os_[0])
+    if lse is None:
+        lse = torch.empty_like(lses[0])
+    o_arr = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in os_])
+    l_arr = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in lses])
+    st = lib.attn_lse_merge_n(o_arr, l_arr, n, _ptr(out), _ptr(lse), B, H, S, D,
+                              _dtype_code(os_[0].dtype), _stream(stream))
+    _check(st, "attn_lse_merge_n")
+    return out, lse

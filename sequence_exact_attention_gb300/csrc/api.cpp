@@ -1,0 +1,119 @@
+// extern "C" entry points: argument checks, then dispatch to one kernel.
+//
+// Every check runs on the host before anything touches the GPU, so a bad
+// call returns its status without launching work.
+#include <cstdint>
+
+#include "ra_internal.h"
+
+using namespace ra;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+constexpr long long kMaxElems = 0x7fffffffLL;   // 32-bit element indexing
+
+ra_status check_attn_args(const void* q, const void* k, const void* v,
+                          const void* out, const float* lse, int B, int H_q,
+                          int H_kv, int S, int D, int dtype, int step,
+                          const int* visit_log, const int* dev_status) {
+  if (!q || !k || !v || !out) return RA_ERR_NULL;
+  if (step >= 0 && !lse) return RA_ERR_NULL;
+  if (dtype != RA_BF16 && dtype != RA_F32) return RA_ERR_DTYPE;
+  if (B <= 0 || H_q <= 0 || H_kv <= 0 || S <= 0) return RA_ERR_SHAPE;
+  if (D != 64 && D != 128) return RA_ERR_HEADDIM;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return RA_ERR_ALIGN;
+  if ((lse && !aligned(lse, 4)) || (visit_log && !aligned(visit_log, 4)) ||
+      (dev_status && !aligned(dev_status, 4)))
+    return RA_ERR_ALIGN;
+  const long long nq = (long long)B * S * H_q * D;
+  const long long nk = (long long)B * S * H_kv * D;
+  if (nq > kMaxElems || nk > kMaxElems) return RA_ERR_RANGE;
+  return RA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ra_status ring_attn_fwd_ex(const void* q, const void* k, const void* v,
+                           void* out, float* lse, int B, int H_q, int H_kv,
+                           int S, int D, int P, int causal, float scale,
+                           int dtype, int order, int step, int* visit_log,
+                           int* dev_status, void* stream) {
+  ra_status st = check_attn_args(q, k, v, out, lse, B, H_q, H_kv, S, D, dtype,
+                                 step, visit_log, dev_status);
+  if (st != RA_OK) return st;
+  Geometry g;
+  st = make_geometry(B, H_q, H_kv, S, D, P, causal, scale, order, step,
+                     tile_rows_for(dtype, D), &g);
+  if (st != RA_OK) return st;
+  int log_stride = 0;
+  if (visit_log) {
+    long long len = 0;
+    st = ring_attn_visit_log_len(B, H_q, S, D, P, dtype, order, nullptr,
+                                 nullptr, nullptr, &log_stride, &len);
+    if (st != RA_OK) return st;
+    if (len > kMaxElems) return RA_ERR_RANGE;
+  }
+  int sms = 0;
+  st = check_device(&sms);
+  if (st != RA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == RA_F32)
+    return launch_attn_simt(g, static_cast<const float*>(q),
+                            static_cast<const float*>(k),
+                            static_cast<const float*>(v), out, lse, visit_log,
+                            log_stride, dev_status, s);
+  return launch_attn_tc(g, q, k, v, out, lse, visit_log, log_stride,
+                        dev_status, sms, s);
+}
+
+ra_status ring_attn_fwd(const void* q, const void* k, const void* v,
+                        void* out, float* lse, int B, int H_q, int H_kv, int S,
+                        int D, int P, int causal, float scale, void* stream) {
+  return ring_attn_fwd_ex(q, k, v, out, lse, B, H_q, H_kv, S, D, P, causal,
+                          scale, RA_BF16, RA_ORDER_CONTIGUOUS, -1, nullptr,
+                          nullptr, stream);
+}
+
+ra_status attn_lse_merge_n(const void* const* o, const float* const* lse,
+                           int n, void* out, float* out_lse, int B, int H,
+                           int S, int D, int dtype, void* stream) {
+  if (!o || !lse || !out || !out_lse) return RA_ERR_NULL;
+  if (n < 1 || n > RA_MERGE_MAX_N) return RA_ERR_SHAPE;
+  if (dtype != RA_BF16 && dtype != RA_F32) return RA_ERR_DTYPE;
+  if (B <= 0 || H <= 0 || S <= 0) return RA_ERR_SHAPE;
+  if (D != 32 && D != 64 && D != 128 && D != 256) return RA_ERR_HEADDIM;
+  MergeArgs a = {};
+  for (int i = 0; i < n; ++i) {
+    if (!o[i] || !lse[i]) return RA_ERR_NULL;
+    if (!aligned(o[i], 16) || !aligned(lse[i], 4)) return RA_ERR_ALIGN;
+    a.o[i] = o[i];
+    a.lse[i] = lse[i];
+  }
+  if (!aligned(out, 16) || !aligned(out_lse, 4)) return RA_ERR_ALIGN;
+  if ((long long)B * S * H * D > kMaxElems) return RA_ERR_RANGE;
+  a.n = n;
+  a.out = out;
+  a.out_lse = out_lse;
+  a.B = B; a.H = H; a.S = S; a.D = D;
+  int sms = 0;
+  ra_status st = check_device(&sms);
+  if (st != RA_OK) return st;
+  return launch_merge(a, dtype, sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ra_status attn_lse_merge(const void* o_a, const float* lse_a, const void* o_b,
+                         const float* lse_b, void* out, float* lse, int B,
+                         int H, int S, int D, int dtype, void* stream) {
+  const void* o[2] = {o_a, o_b};
+  const float* l[2] = {lse_a, lse_b};
+  return attn_lse_merge_n(o, l, 2, out, lse, B, H, S, D, dtype, stream);
+}
+
+}  // extern "C"

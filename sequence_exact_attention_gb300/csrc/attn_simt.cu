@@ -1,0 +1,187 @@
+// Exact float32 ring attention on the CUDA cores (FMA pipe).
+//
+// The float32 workload is held to 1e-4 against the float64 definition, which
+// rules out TF32 tensor-core products; this kernel keeps every product and
+// sum in IEEE float32 and uses the accurate exp2f/log2f.
+//
+// Ring structure (glossary "sequence parallelism transformers", §Ring
+// Attention): a block owns one query tile of 64 rows of one (batch, head)
+// inside the segment of virtual rank r, and walks the key tiles of steps
+// t = 0..P-1 in ring order (source rank (r - t) mod P). Per key tile it
+// computes the 64 scores of each row, folds them into the running row state
+// (max m, sum l, unnormalised output acc) -- the log-sum-exp merge of the
+// per-tile partial results, done in registers -- and at the end writes
+// out = acc / l and lse = ln(2) * (m + log2 l).
+//
+// Mapping: 256 threads = 64 rows x 4 threads. The 4 threads of a row split D
+// in interleaved 16-byte vectors (thread p owns vectors p, p+4, ...), so a
+// key row read from shared memory is one contiguous 64-byte broadcast per
+// row group; partial dot products are combined with two xor-shuffles.
+#include <cmath>
+#include <cstdint>
+
+#include "ra_internal.h"
+#include "ring_iter.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kRows = 64;        // query / key tile rows
+constexpr int kThreads = 256;    // 4 threads per query row
+
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+  acc = fmaf(a.x, b.x, acc);
+  acc = fmaf(a.y, b.y, acc);
+  acc = fmaf(a.z, b.z, acc);
+  return fmaf(a.w, b.w, acc);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+attn_simt_kernel(const Geometry g, const float* __restrict__ q,
+                 const float* __restrict__ k, const float* __restrict__ v,
+                 float* __restrict__ out, float* __restrict__ lse,
+                 int* __restrict__ vlog, int log_stride) {
+  constexpr int V4 = D / 4;          // float4 per row
+  constexpr int NV = V4 / 4;         // float4 per thread
+  extern __shared__ float4 smem[];
+  float4* Ks = smem;                 // [kRows][V4]
+  float4* Vs = smem + kRows * V4;    // [kRows][V4]
+
+  const int BH = g.B * g.H_q;
+  const int bh = blockIdx.x % BH;
+  const int n_qt = g.n_seg * g.nt;
+  const int qid = n_qt - 1 - blockIdx.x / BH;    // later positions first
+  const int seg = qid / g.nt, ti = qid % g.nt;
+  const int q_lo = seg * g.seg_len + ti * kRows;
+  const int q_valid = min(kRows, g.seg_len - ti * kRows);
+  const int r = seg_owner(g, seg);
+  const int b = bh / g.H_q, h = bh % g.H_q;
+  const int hk = h / (g.H_q / g.H_kv);
+
+  const int row = threadIdx.x >> 2, part = threadIdx.x & 3;
+  const int q_pos = q_lo + row;
+  const bool row_valid = row < q_valid;
+
+  float4 qv[NV], acc[NV];
+  const float4* qrow = reinterpret_cast<const float4*>(
+      q + (((size_t)b * g.S + (row_valid ? q_pos : q_lo)) * g.H_q + h) * D);
+#pragma unroll
+  for (int e = 0; e < NV; ++e) {
+    qv[e] = row_valid ? qrow[part + 4 * e] : make_float4(0.f, 0.f, 0.f, 0.f);
+    acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float m = -INFINITY, l = 0.f;
+
+  int* log_base = vlog ? vlog + ((size_t)bh * n_qt + qid) * log_stride : nullptr;
+  int n_vis = 0;
+
+  KvIter it;
+  it.init(g);
+  KvTile kv;
+  while (it.next(g, r, kv)) {
+    const int work = tile_work(g, q_lo, q_valid, kv);
+    if (work == kSkip) continue;
+    if (log_base && threadIdx.x == 0) log_visit(log_base, n_vis, kv, tile_class(g, q_lo, kv));
+    ++n_vis;
+
+    __syncthreads();    // the previous tile is no longer read
+    for (int idx = threadIdx.x; idx < kRows * V4; idx += kThreads) {
+      const int kr = idx / V4, c = idx % V4;
+      float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
+      if (kr < kv.valid) {
+        const size_t off = (((size_t)b * g.S + kv.lo + kr) * g.H_kv + hk) * V4 + c;
+        kk = reinterpret_cast<const float4*>(k)[off];
+        vv = reinterpret_cast<const float4*>(v)[off];
+      }
+      Ks[idx] = kk;
+      Vs[idx] = vv;
+    }
+    __syncthreads();
+
+    float s[kRows];
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+      float p = 0.f;
+#pragma unroll
+      for (int e = 0; e < NV; ++e) p = dot4(qv[e], Ks[j * V4 + part + 4 * e], p);
+      p += __shfl_xor_sync(0xffffffffu, p, 1);
+      p += __shfl_xor_sync(0xffffffffu, p, 2);
+      s[j] = p;
+    }
+    if (work == kMask) {
+#pragma unroll
+      for (int j = 0; j < kRows; ++j)
+        if (j >= kv.valid || (g.causal && kv.lo + j > q_pos)) s[j] = -INFINITY;
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) mx = fmaxf(mx, s[j]);
+    const float m_new = fmaxf(m, mx * g.scale_log2);
+    const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
+    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+    l *= alpha;
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      acc[e].x *= alpha; acc[e].y *= alpha; acc[e].z *= alpha; acc[e].w *= alpha;
+    }
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+      const float p = exp2f(fmaf(s[j], g.scale_log2, -m_use));
+      l += p;
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        const float4 vv = Vs[j * V4 + part + 4 * e];
+        acc[e].x = fmaf(p, vv.x, acc[e].x);
+        acc[e].y = fmaf(p, vv.y, acc[e].y);
+        acc[e].z = fmaf(p, vv.z, acc[e].z);
+        acc[e].w = fmaf(p, vv.w, acc[e].w);
+      }
+    }
+    m = m_new;
+  }
+
+  if (row_valid) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    float4* orow = reinterpret_cast<float4*>(
+        out + (((size_t)b * g.S + q_pos) * g.H_q + h) * D);
+#pragma unroll
+    for (int e = 0; e < NV; ++e)
+      orow[part + 4 * e] = make_float4(acc[e].x * inv, acc[e].y * inv,
+                                       acc[e].z * inv, acc[e].w * inv);
+    if (part == 0 && lse)
+      lse[(size_t)bh * g.S + q_pos] =
+          l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+  }
+  if (log_base && threadIdx.x == 0) log_base[0] = n_vis;
+}
+
+template <int D>
+ra_status launch_d(const Geometry& g, const float* q, const float* k,
+                   const float* v, float* out, float* lse, int* vlog,
+                   int log_stride, cudaStream_t stream) {
+  const int smem = 2 * kRows * D * (int)sizeof(float);
+  if (cudaFuncSetAttribute(attn_simt_kernel<D>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return RA_ERR_LAUNCH;
+  const long long grid = (long long)g.n_seg * g.nt * g.B * g.H_q;
+  if (grid > 0x7fffffffLL) return RA_ERR_RANGE;
+  attn_simt_kernel<D><<<(unsigned)grid, kThreads, smem, stream>>>(
+      g, q, k, v, out, lse, vlog, log_stride);
+  return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+ra_status launch_attn_simt(const Geometry& g, const float* q, const float* k,
+                           const float* v, void* out, float* lse,
+                           int* visit_log, int log_stride, int* dev_status,
+                           cudaStream_t stream) {
+  (void)dev_status;   // this kernel has no waits that could expire
+  float* o = static_cast<float*>(out);
+  if (g.D == 64) return launch_d<64>(g, q, k, v, o, lse, visit_log, log_stride, stream);
+  return launch_d<128>(g, q, k, v, o, lse, visit_log, log_stride, stream);
+}
+
+}  // namespace ra

@@ -1,0 +1,502 @@
+// Exact ring attention on the tcgen05 tensor cores (bf16 in, f32 accumulate).
+//
+// Glossary "sequence parallelism transformers":
+//  - §Ring Attention: each virtual rank keeps its query block; at step t it
+//    attends to the key/value block of rank (r - t) mod P ("receive from
+//    i-1"), and accumulates outputs; only the local block and the received
+//    block need to be resident ("Memory Efficiency").
+//  - §Flash Attention with Sequence Parallelism: attention is computed tile
+//    by tile (prior art; the tiling below is laid out for sm_103a).
+//  - §Implementation Considerations: the softmax normalisation across blocks
+//    is kept exact with a running maximum and sum (log-sum-exp merge).
+//
+// One CTA owns a pair of 128-row query tiles of one (batch, head) inside one
+// segment of virtual rank r, and walks the key tiles of the ring in order.
+// "Receiving" a block is a TMA load of its tile from this GPU's HBM/L2 into a
+// shared-memory ring of stages. Warp roles (320 threads):
+//   warps 0-3  softmax for query tile 0 (one thread per row = TMEM lane)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    TMA producer: Q once, then K/V tiles into the stage ring
+//   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
+// Tensor memory (512 columns): tile k uses columns [256k, 256k+128) for the
+// f32 scores S = Q K^T, reused in place for P (bf16, packed two per column,
+// 64 columns) and [256k+128, 256k+128+D) for the f32 output accumulator O.
+// Per key tile j: S_k = Q_k K_j^T (SS MMA) -> softmax reads S_k, writes P_k,
+// rescales O_k if its running max moved by more than 2^8 -> O_k += P_k V_j
+// (TS MMA, P from TMEM). The running (max, sum, O) carried across ring steps
+// is the in-register form of the log-sum-exp merge of per-step partials.
+//
+// Every wait is bounded: after kTimeoutNs a thread raises a CTA-wide abort
+// flag, every role falls through to the common teardown (which still waits,
+// bounded, for the tensor-core work it issued, then frees TMEM), and the
+// kernel reports RA_ERR_TIMEOUT through the status word.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "ra_internal.h"
+#include "ring_iter.cuh"
+#include "sm100.cuh"
+
+namespace ra {
+namespace {
+
+using namespace sm100;
+
+constexpr int kTile = 128;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;          // lazy rescale threshold (x256)
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr int kBoxBytes = kTile * 64 * 2;      // one TMA box: 128 rows x 64 bf16
+
+template <int D>
+struct Cfg {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;   // + alignment slack
+  // barrier indices (8 bytes each)
+  static constexpr int bQFull = 0;
+  static constexpr int bKFull = 1;
+  static constexpr int bKEmpty = bKFull + kStages;
+  static constexpr int bVFull = bKEmpty + kStages;
+  static constexpr int bVEmpty = bVFull + kStages;
+  static constexpr int bSFull = bVEmpty + kStages;     // [2]
+  static constexpr int bPFull = bSFull + 2;            // [2]
+  static constexpr int bODone = bPFull + 2;            // [2]
+  static constexpr int bFinal = bODone + 2;
+  static constexpr int kNumBars = bFinal + 1;
+  static constexpr int kHolderOff = kBarBytes - 16;    // TMEM base address
+  static constexpr int kAbortOff = kBarBytes - 8;      // abort flag
+  static_assert(kNumBars * 8 <= kHolderOff, "barrier area overflow");
+  // one CTA per SM: the kernel owns all 512 TMEM columns
+  static_assert(kSmemBytes > 116 * 1024, "must not fit two CTAs per SM");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ uint32_t s_col(int k) { return (uint32_t)(k * 256); }
+__device__ __forceinline__ uint32_t o_col(int k) { return (uint32_t)(k * 256 + 128); }
+
+template <int D, bool kOutF32>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+               const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const Geometry g,
+               void* __restrict__ out, float* __restrict__ lse,
+               int* __restrict__ vlog, int log_stride, int* __restrict__ status) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  auto bar = [&](int i) -> uint32_t { return base + C::kBarOff + 8u * (uint32_t)i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kBarOff + C::kAbortOff);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + C::kBarOff + C::kHolderOff);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work item: pair of query tiles, later positions launched first
+  const int BH = g.B * g.H_q;
+  const int bh = blockIdx.x % BH;
+  const int pairs_per_seg = (g.nt + 1) / 2;
+  const int n_pairs = g.n_seg * pairs_per_seg;
+  const int pair = n_pairs - 1 - (int)(blockIdx.x / BH);
+  const int seg = pair / pairs_per_seg;
+  const int ti0 = (pair % pairs_per_seg) * 2;
+  const int r = seg_owner(g, seg);
+  const int b = bh / g.H_q, h = bh % g.H_q;
+  const int hk = h / (g.H_q / g.H_kv);
+  int q_lo[2], q_valid[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int ti = ti0 + k;
+    q_lo[k] = seg * g.seg_len + ti * kTile;
+    q_valid[k] = ti < g.nt ? min(kTile, g.seg_len - ti * kTile) : 0;
+  }
+
+  // ---- set-up: barriers, abort flag, TMEM
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::bQFull), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::bKFull + s), 1);
+      mbar_init(bar(C::bKEmpty + s), 1);
+      mbar_init(bar(C::bVFull + s), 1);
+      mbar_init(bar(C::bVEmpty + s), 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar(C::bSFull + k), 1);
+      mbar_init(bar(C::bPFull + k), 128);
+      mbar_init(bar(C::bODone + k), 1);
+    }
+    mbar_init(bar(C::bFinal), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == kProducerWarp) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      const uint32_t q_smem = base + C::kQOff;
+      mbar_arrive_expect_tx(bar(C::bQFull), 2 * C::kTileBytes);
+      for (int k = 0; k < 2; ++k)
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_4d(q_smem + k * C::kTileBytes + bx * kBoxBytes, &tm_q, bar(C::bQFull),
+                      bx * 64, h, q_lo[k], b);
+      KvIter it;
+      it.init(g);
+      KvTile kv;
+      int j = 0;
+      while (it.next(g, r, kv)) {
+        if (tile_work(g, q_lo[0], q_valid[0], kv) == kSkip &&
+            tile_work(g, q_lo[1], q_valid[1], kv) == kSkip)
+          continue;
+        const int s = j % C::kStages;
+        const uint32_t use = (uint32_t)(j / C::kStages);
+        if (j >= C::kStages &&
+            !mbar_wait(bar(C::bKEmpty + s), (use - 1) & 1, abort_flag, kTimeoutNs))
+          break;
+        mbar_arrive_expect_tx(bar(C::bKFull + s), C::kTileBytes);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_4d(base + C::kKOff + s * C::kTileBytes + bx * kBoxBytes, &tm_k,
+                      bar(C::bKFull + s), bx * 64, hk, kv.lo, b);
+        if (j >= C::kStages &&
+            !mbar_wait(bar(C::bVEmpty + s), (use - 1) & 1, abort_flag, kTimeoutNs))
+          break;
+        mbar_arrive_expect_tx(bar(C::bVFull + s), C::kTileBytes);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_4d(base + C::kVOff + s * C::kTileBytes + bx * kBoxBytes, &tm_v,
+                      bar(C::bVFull + s), bx * 64, hk, kv.lo, b);
+        ++j;
+      }
+      // Every issued load lands before the CTA leaves (already true unless
+      // the CTA aborted): wait, bounded, on the last use of each stage.
+      for (int jj = (j > C::kStages ? j - C::kStages : 0); jj < j; ++jj) {
+        const int s = jj % C::kStages;
+        const uint32_t ph = (uint32_t)(jj / C::kStages) & 1;
+        volatile int never = 0;
+        mbar_wait(bar(C::bKFull + s), ph, &never, kTimeoutNs);
+        mbar_wait(bar(C::bVFull + s), ph, &never, kTimeoutNs);
+      }
+      volatile int never = 0;
+      mbar_wait(bar(C::bQFull), 0, &never, kTimeoutNs);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTile, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
+      uint32_t n_pv[2] = {0, 0}, n_p[2] = {0, 0};
+      bool ok = mbar_wait(bar(C::bQFull), 0, abort_flag, kTimeoutNs);
+      tc_fence_after();
+      KvIter it;
+      it.init(g);
+      KvTile kv;
+      int j = 0;
+      while (ok && it.next(g, r, kv)) {
+        bool act[2];
+        act[0] = tile_work(g, q_lo[0], q_valid[0], kv) != kSkip;
+        act[1] = tile_work(g, q_lo[1], q_valid[1], kv) != kSkip;
+        if (!act[0] && !act[1]) continue;
+        const int s = j % C::kStages;
+        const uint32_t ph = (uint32_t)(j / C::kStages) & 1;
+        const uint32_t k_smem = base + C::kKOff + s * C::kTileBytes;
+        const uint32_t v_smem = base + C::kVOff + s * C::kTileBytes;
+        if (!mbar_wait(bar(C::bKFull + s), ph, abort_flag, kTimeoutNs)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (!ok || !act[k]) continue;
+          // P_k of the previous tile aliases S_k: its PV must be done
+          if (n_pv[k] > 0) {
+            ok = mbar_wait(bar(C::bODone + k), (n_pv[k] - 1) & 1, abort_flag, kTimeoutNs);
+            tc_fence_after();
+          }
+          if (!ok) continue;
+          const uint32_t q_smem = base + C::kQOff + k * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
+            umma_ss(tmem + s_col(k), sw128_desc(q_smem + off, 16, 1024),
+                    sw128_desc(k_smem + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(C::bSFull + k));
+        }
+        if (!ok) break;
+        umma_commit(bar(C::bKEmpty + s));
+        if (!mbar_wait(bar(C::bVFull + s), ph, abort_flag, kTimeoutNs)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (!ok || !act[k]) continue;
+          ok = mbar_wait(bar(C::bPFull + k), n_p[k] & 1, abort_flag, kTimeoutNs);
+          if (!ok) continue;
+          ++n_p[k];
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            umma_ts(tmem + o_col(k), tmem + s_col(k) + kk * 8,
+                    sw128_desc(v_smem + kk * 2048, kBoxBytes, 1024), idesc_o,
+                    (n_pv[k] > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(bar(C::bODone + k));
+          ++n_pv[k];
+        }
+        if (!ok) break;
+        umma_commit(bar(C::bVEmpty + s));
+        ++j;
+      }
+      // all tensor-core work of this CTA has completed before teardown
+      umma_commit(bar(C::bFinal));
+      volatile int never = 0;
+      mbar_wait(bar(C::bFinal), 0, &never, kTimeoutNs);
+    }
+    __syncwarp();
+  } else {
+    // ======================= softmax, one thread per row =======================
+    const int k = warp >> 2;                 // query tile of this warpgroup
+    const int wq = warp & 3;                 // TMEM lane quarter
+    const int row = wq * 32 + lane;
+    const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + t_lane + s_col(k);
+    const uint32_t tO = tmem + t_lane + o_col(k);
+    // (selects, not indexing: a runtime index would put the arrays in local memory)
+    const int my_q_lo = k ? q_lo[1] : q_lo[0];
+    const int my_q_valid = k ? q_valid[1] : q_valid[0];
+    const int q_pos = my_q_lo + row;
+    const bool row_valid = row < my_q_valid;
+    const float sl2 = g.scale_log2;
+
+    const int n_qt = g.n_seg * g.nt;
+    int* log_base = (vlog && my_q_valid > 0 && (threadIdx.x & 127) == 0)
+                        ? vlog + ((size_t)bh * n_qt + seg * g.nt + ti0 + k) * log_stride
+                        : nullptr;
+    int n_vis = 0;
+
+    float m_run = -INFINITY, l_run = 0.f;
+    uint32_t n_s = 0, n_pv = 0;
+    bool ok = true;
+    KvIter it;
+    it.init(g);
+    KvTile kv;
+    while (it.next(g, r, kv)) {
+      const int work = tile_work(g, my_q_lo, my_q_valid, kv);
+      if (work == kSkip) continue;
+      if (log_base) log_visit(log_base, n_vis, kv, tile_class(g, my_q_lo, kv));
+      ++n_vis;
+      ok = mbar_wait(bar(C::bSFull + k), n_s & 1, abort_flag, kTimeoutNs);
+      if (!ok) break;
+      ++n_s;
+      tc_fence_after();
+
+      float s[kTile];
+#pragma unroll
+      for (int c = 0; c < kTile / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tS + c * 32, u);
+        tmem_ld_wait(u);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(u[i]);
+      }
+      if (work == kMask) {
+        const int lim = g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid;
+#pragma unroll
+        for (int c = 0; c < kTile; ++c)
+          if (c >= lim) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < kTile; ++c) mx = fmaxf(mx, s[c]);
+      const float m_new = fmaxf(m_run, mx * sl2);
+      const bool resc = m_new > m_run + kRescaleLog2;
+      float alpha = 1.f;
+      if (resc) {
+        alpha = ex2_approx(m_run - m_new);     // 0 when m_run = -inf
+        m_run = m_new;
+        l_run *= alpha;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      float sum = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2_approx(fmaf(s[half * 64 + 2 * i], sl2, -m_use));
+          const float p1 = ex2_approx(fmaf(s[half * 64 + 2 * i + 1], sl2, -m_use));
+          sum += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tS + half * 32, pk);
+      }
+      l_run += sum;
+      // O_k must be scaled by alpha before P_k V_j is added to it
+      if (__any_sync(0xffffffffu, resc) && n_pv > 0) {
+        ok = mbar_wait(bar(C::bODone + k), (n_pv - 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tO + c * 32, u);
+          tmem_ld_wait(u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          tmem_st32(tO + c * 32, u);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::bPFull + k));
+      ++n_pv;
+    }
+    if (log_base) log_base[0] = n_vis;
+
+    // ---- epilogue: out = O / l, lse = ln2 * (m + log2 l)
+    if (ok && n_pv > 0) {
+      ok = mbar_wait(bar(C::bODone + k), (n_pv - 1) & 1, abort_flag, kTimeoutNs);
+      tc_fence_after();
+    }
+    if (ok) {
+      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      const size_t row_off = (((size_t)b * g.S + q_pos) * g.H_q + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        if (n_pv > 0) {
+          tmem_ld32(tO + c * 32, u);
+          tmem_ld_wait(u);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = 0u;
+        }
+        if (row_valid) {
+          if (kOutF32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + row_off + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(u[4 * i]) * inv_l,
+                                   __uint_as_float(u[4 * i + 1]) * inv_l,
+                                   __uint_as_float(u[4 * i + 2]) * inv_l,
+                                   __uint_as_float(u[4 * i + 3]) * inv_l);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + row_off + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(u[8 * i + 0]) * inv_l, __uint_as_float(u[8 * i + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(u[8 * i + 2]) * inv_l, __uint_as_float(u[8 * i + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(u[8 * i + 4]) * inv_l, __uint_as_float(u[8 * i + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(u[8 * i + 6]) * inv_l, __uint_as_float(u[8 * i + 7]) * inv_l);
+              dst[i] = w;
+            }
+          }
+        }
+      }
+      if (row_valid && lse)
+        lse[(size_t)bh * g.S + q_pos] =
+            l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag && status) atomicExch(status, (int)RA_ERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ host
+using EncodeTiledFn = decltype(&cuTensorMapEncodeTiled);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// [B, S, H, D] bf16 tensor; box = 64 columns x 1 head x 128 rows x 1 batch,
+// 128-byte swizzle (the layout tcgen05 reads with sw128 descriptors).
+bool make_bshd_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2,
+                           (cuuint64_t)S * H * D * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool kOutF32>
+ra_status launch_typed(const Geometry& g, const CUtensorMap& mq, const CUtensorMap& mk,
+                       const CUtensorMap& mv, void* out, float* lse, int* vlog,
+                       int log_stride, int* status, cudaStream_t stream) {
+  using C = Cfg<D>;
+  auto kern = attn_tc_kernel<D, kOutF32>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes) != cudaSuccess)
+    return RA_ERR_LAUNCH;
+  const long long pairs = (long long)g.n_seg * ((g.nt + 1) / 2);
+  const long long grid = pairs * g.B * g.H_q;
+  if (grid > 0x7fffffffLL) return RA_ERR_RANGE;
+  kern<<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, g, out, lse, vlog,
+                                                            log_stride, status);
+  return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+ra_status launch_attn_tc(const Geometry& g, const void* q, const void* k, const void* v,
+                         void* out, float* lse, int* visit_log, int log_stride,
+                         int* dev_status, int sm_count, cudaStream_t stream) {
+  (void)sm_count;
+  CUtensorMap mq, mk, mv;
+  if (!make_bshd_map(&mq, q, g.B, g.S, g.H_q, g.D) ||
+      !make_bshd_map(&mk, k, g.B, g.S, g.H_kv, g.D) ||
+      !make_bshd_map(&mv, v, g.B, g.S, g.H_kv, g.D))
+    return RA_ERR_LAUNCH;
+  const bool f32_out = g.step >= 0;
+  if (g.D == 64)
+    return f32_out ? launch_typed<64, true>(g, mq, mk, mv, out, lse, visit_log, log_stride, dev_status, stream)
+                   : launch_typed<64, false>(g, mq, mk, mv, out, lse, visit_log, log_stride, dev_status, stream);
+  return f32_out ? launch_typed<128, true>(g, mq, mk, mv, out, lse, visit_log, log_stride, dev_status, stream)
+                 : launch_typed<128, false>(g, mq, mk, mv, out, lse, visit_log, log_stride, dev_status, stream);
+}
+
+}  // namespace ra

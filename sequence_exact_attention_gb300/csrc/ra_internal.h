@@ -1,0 +1,60 @@
+// Internal declarations shared by the host entry points and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/ring_attn.h"
+
+namespace ra {
+
+// Geometry of one ring-attention call, as every kernel role sees it.
+// Segments are the contiguous token ranges a virtual rank owns: one chunk of
+// S/P tokens (contiguous order) or two halves of S/(2P) tokens (zig-zag).
+// Segment g (in position order) starts at g * seg_len. Each segment is cut
+// into `nt` tiles of `tile` rows; the last may be shorter.
+struct Geometry {
+  int B, H_q, H_kv, S, D, P;
+  int causal;
+  int order;       // RA_ORDER_*
+  int step;        // -1: all steps; else the single ring step to run
+  int seg_len;     // tokens per segment
+  int n_seg;       // P or 2P
+  int segs_per_rank;
+  int tile;        // tile rows of the kernel
+  int nt;          // tiles per segment
+  float scale;     // softmax scale
+  float scale_log2;  // scale * log2(e)
+};
+
+// Host-side planning helpers (plan.cpp).
+ra_status make_geometry(int B, int H_q, int H_kv, int S, int D, int P,
+                        int causal, float scale, int order, int step, int tile,
+                        Geometry* g);
+int tile_rows_for(int dtype, int D);
+
+// Per-device facts, cached (plan.cpp).
+ra_status check_device(int* sm_count);
+
+// Launchers (one per kernel family). They assume validated arguments.
+ra_status launch_attn_simt(const Geometry& g, const float* q, const float* k,
+                           const float* v, void* out, float* lse,
+                           int* visit_log, int log_stride, int* dev_status,
+                           cudaStream_t stream);
+ra_status launch_attn_tc(const Geometry& g, const void* q, const void* k,
+                         const void* v, void* out, float* lse, int* visit_log,
+                         int log_stride, int* dev_status, int sm_count,
+                         cudaStream_t stream);
+
+struct MergeArgs {
+  const void* o[RA_MERGE_MAX_N];
+  const float* lse[RA_MERGE_MAX_N];
+  int n;
+  void* out;
+  float* out_lse;
+  int B, H, S, D;
+};
+ra_status launch_merge(const MergeArgs& a, int dtype, int sm_count,
+                       cudaStream_t stream);
+
+}  // namespace ra

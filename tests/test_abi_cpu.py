@@ -1,0 +1,151 @@
+"""Host-side checks of the C-ABI library; no GPU work is launched.
+
+The library must load and export every entry point of include/ring_attn.h,
+its host-only planner must equal the oracle's schedule bit for bit, and every
+invalid argument must be rejected before the library touches the GPU.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from sequence_exact_attention_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ring_attn.h")
+
+RA_OK, RA_ERR_NULL, RA_ERR_SHAPE, RA_ERR_HEADDIM, RA_ERR_ALIGN = 0, 1, 2, 3, 4
+RA_ERR_DTYPE, RA_ERR_DEVICE, RA_ERR_BUFFER, RA_ERR_RANGE = 5, 6, 9, 10
+
+
+def _header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:ra_status|const char\*|int)\s+(\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _header_functions()
+    assert len(names) >= 8
+    assert set(names) == set(binding.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+    assert lib.ring_attn_version() >= 100
+
+
+def test_strerror_covers_every_status(lib):
+    seen = set()
+    for st in range(0, 11):
+        msg = binding.strerror(st)
+        assert msg and msg != "unknown status"
+        seen.add(msg)
+    assert len(seen) == 11
+    assert binding.strerror(99) == "unknown status"
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("order", ["contiguous", "zigzag"])
+@pytest.mark.parametrize("S,P", [(8, 2), (256, 4), (4096, 8), (32768, 8),
+                                 (131072, 16), (96, 3), (16, 16), (7, 7)])
+def test_plan_matches_oracle_schedule(S, P, causal, order):
+    o = oracle.ORDER_ZIGZAG if order == "zigzag" else oracle.ORDER_CONTIGUOUS
+    if order == "zigzag" and S % (2 * P):
+        with pytest.raises(binding.RingAttnError) as e:
+            binding.ring_attn_plan(S, P, causal, order)
+        assert e.value.status == RA_ERR_SHAPE
+        return
+    got = binding.ring_attn_plan(S, P, causal, order)
+    want = oracle.schedule_table(S, P, causal, o)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_plan_rejects_small_buffer_and_bad_args(lib):
+    buf = (ctypes.c_int * 10)()
+    assert lib.ring_attn_plan(8, 2, 1, 0, buf, 10) == RA_ERR_BUFFER
+    assert lib.ring_attn_plan(8, 2, 1, 0, None, 100) == RA_ERR_NULL
+    assert lib.ring_attn_plan(9, 2, 1, 0, buf, 10) == RA_ERR_SHAPE
+    assert lib.ring_attn_plan(8, 0, 1, 0, buf, 10) == RA_ERR_SHAPE
+    assert lib.ring_attn_plan(8, 2, 1, 7, buf, 10) == RA_ERR_DTYPE
+
+
+@pytest.mark.parametrize("dtype,tile", [("bf16", 128), ("f32", 64)])
+def test_visit_log_layout(dtype, tile):
+    lay = binding.visit_log_layout(2, 4, 4096, 128, 8, dtype, "zigzag")
+    seg = 4096 // 16
+    nt = -(-seg // tile)
+    assert lay["tile_rows"] == tile
+    assert lay["tiles_per_segment"] == nt
+    assert lay["n_query_tiles"] == 16 * nt
+    assert lay["stride"] == 1 + 4 * 16 * nt
+    assert lay["len"] == 2 * 4 * 16 * nt * lay["stride"]
+
+
+# ---- argument checks: every call below fails before the GPU is touched.
+# Pointer values are never dereferenced; the checks are on the host.
+A = 0x10000          # a 16-byte aligned fake address
+
+
+def _fwd(lib, q=A, k=A, v=A, out=A, lse=A, B=1, Hq=2, Hkv=2, S=256, D=64, P=4,
+         causal=1, scale=0.0, dtype=0, order=0, step=-1, log=None, status=None):
+    vp = ctypes.c_void_p
+    return lib.ring_attn_fwd_ex(vp(q), vp(k), vp(v), vp(out), vp(lse), B, Hq, Hkv,
+                                S, D, P, causal, scale, dtype, order, step,
+                                vp(log), vp(status), None)
+
+
+def test_fwd_argument_errors(lib):
+    assert _fwd(lib, q=0) == RA_ERR_NULL
+    assert _fwd(lib, out=0) == RA_ERR_NULL
+    assert _fwd(lib, lse=0, step=1) == RA_ERR_NULL        # partials need lse
+    assert _fwd(lib, B=0) == RA_ERR_SHAPE
+    assert _fwd(lib, S=0) == RA_ERR_SHAPE
+    assert _fwd(lib, S=-5) == RA_ERR_SHAPE
+    assert _fwd(lib, S=250) == RA_ERR_SHAPE               # S % P
+    assert _fwd(lib, S=260, order=1) == RA_ERR_SHAPE      # S % 2P
+    assert _fwd(lib, Hq=3, Hkv=2) == RA_ERR_SHAPE
+    assert _fwd(lib, P=0) == RA_ERR_SHAPE
+    assert _fwd(lib, D=96) == RA_ERR_HEADDIM
+    assert _fwd(lib, D=256) == RA_ERR_HEADDIM
+    assert _fwd(lib, q=A + 8) == RA_ERR_ALIGN
+    assert _fwd(lib, out=A + 4) == RA_ERR_ALIGN
+    assert _fwd(lib, lse=A + 2) == RA_ERR_ALIGN
+    assert _fwd(lib, dtype=2) == RA_ERR_DTYPE
+    assert _fwd(lib, order=2) == RA_ERR_DTYPE
+    assert _fwd(lib, step=4) == RA_ERR_RANGE
+    assert _fwd(lib, step=-2) == RA_ERR_RANGE
+    assert _fwd(lib, B=1, Hq=64, Hkv=64, S=1 << 20, D=128, P=8) == RA_ERR_RANGE
+    vp = ctypes.c_void_p
+    assert lib.ring_attn_fwd(vp(0), vp(A), vp(A), vp(A), vp(A), 1, 2, 2, 256, 64,
+                             4, 1, 0.0, None) == RA_ERR_NULL
+
+
+def test_merge_argument_errors(lib):
+    vp = ctypes.c_void_p
+    assert lib.attn_lse_merge(vp(0), vp(A), vp(A), vp(A), vp(A), vp(A), 1, 2, 8, 64,
+                              1, None) == RA_ERR_NULL
+    assert lib.attn_lse_merge(vp(A), vp(A), vp(A), vp(A), vp(A), vp(A), 1, 2, 8, 48,
+                              1, None) == RA_ERR_HEADDIM
+    assert lib.attn_lse_merge(vp(A + 4), vp(A), vp(A), vp(A), vp(A), vp(A), 1, 2, 8,
+                              64, 1, None) == RA_ERR_ALIGN
+    assert lib.attn_lse_merge(vp(A), vp(A), vp(A), vp(A), vp(A), vp(A), 1, 2, 0, 64,
+                              1, None) == RA_ERR_SHAPE
+    assert lib.attn_lse_merge(vp(A), vp(A), vp(A), vp(A), vp(A), vp(A), 1, 2, 8, 64,
+                              3, None) == RA_ERR_DTYPE
+    arr = (ctypes.c_void_p * 17)(*([A] * 17))
+    assert lib.attn_lse_merge_n(arr, arr, 17, vp(A), vp(A), 1, 2, 8, 64, 1,
+                                None) == RA_ERR_SHAPE
+    assert lib.attn_lse_merge_n(arr, arr, 0, vp(A), vp(A), 1, 2, 8, 64, 1,
+                                None) == RA_ERR_SHAPE
+
+
+def test_valid_call_without_gpu_reports_device_error(lib):
+    """With every argument valid the only thing missing here is the GPU."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: this case would launch on fake pointers")
+    assert _fwd(lib) == RA_ERR_DEVICE
