@@ -78,7 +78,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -201,6 +201,47 @@ def _config(w):
             "parallelism": "replicas"}
 
 
+def _e2e(args, w, q, k, v, qd, kd, vd, out, lse, step, dev, stream, dist, world):
+    """Same metric through the public API with pinned host buffers: every
+    step copies q, k, v host->device, runs the call, copies out and lse back."""
+    import torch
+    flop = w.flop
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        step()
+        oh.copy_(out, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_val = world * flop * args.steps / (e2e_ms / 1e3) / 1e12
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    return {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
 def run_ours(args, w):
     import torch
     from sequence_exact_attention_gb300 import binding
@@ -266,38 +307,9 @@ def run_ours(args, w):
     kernel_ms = statistics.mean(launch_ms)
 
     # ---- end to end through the public API, host buffers, copies timed
-    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-
-    def e2e_step():
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        step()
-        oh.copy_(out, non_blocking=True)
-        lh.copy_(lse, non_blocking=True)
-
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    if dist:
-        dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = world * flop * args.steps / (e2e_ms / 1e3) / 1e12
-    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
-    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(args, w, q, k, v, qd, kd, vd, out, lse, step, dev, stream, dist, world)
 
     if rank != 0:
         return 0
@@ -329,8 +341,7 @@ def run_ours(args, w):
                      "kernel": "attn_tc_kernel<128,false>",
                      "kernel_ms": kernel_ms},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "clocks": clk,
         "gpu_launches": args.steps,
     }
@@ -342,15 +353,20 @@ def main():
     from sequence_exact_attention_gb300.workloads import WORKLOADS, HEADLINE
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
-    ap.add_argument("--cpu-rows", type=int, default=192)
+    ap.add_argument("--cpu-rows", type=int, default=768)
     ap.add_argument("--ref-rows", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="override S (smaller profiling cases of the same shape)")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
+    if args.seq_len:
+        w = w.scaled(S=args.seq_len, name=f"{w.name}@S={args.seq_len}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -106,17 +106,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work item: pair of query tiles, later positions launched first
-  const int BH = g.B * g.H_q;
-  const int bh = blockIdx.x % BH;
+  // ---- work item: a pair of query tiles. Block order: (batch, kv head)
+  // outermost, so the CTAs resident at one time read the keys/values of one
+  // or two kv heads and find them in L2; then pairs by decreasing position
+  // (decreasing causal work, longest first); the query heads sharing the kv
+  // head innermost, so they read the same key tiles at the same time.
+  const int grp = g.H_q / g.H_kv;
   const int pairs_per_seg = (g.nt + 1) / 2;
   const int n_pairs = g.n_seg * pairs_per_seg;
-  const int pair = n_pairs - 1 - (int)(blockIdx.x / BH);
+  const int hg = (int)(blockIdx.x % grp);
+  const int rest = (int)(blockIdx.x / grp);
+  const int pair = n_pairs - 1 - rest % n_pairs;
+  const int bhk = rest / n_pairs;
+  const int b = bhk / g.H_kv, hk = bhk % g.H_kv;
+  const int h = hk * grp + hg;
+  const int bh = b * g.H_q + h;
   const int seg = pair / pairs_per_seg;
   const int ti0 = (pair % pairs_per_seg) * 2;
   const int r = seg_owner(g, seg);
-  const int b = bh / g.H_q, h = bh % g.H_q;
-  const int hk = h / (g.H_q / g.H_kv);
   int q_lo[2], q_valid[2];
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
@@ -309,13 +316,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       tc_fence_after();
 
       float s[kTile];
+      {
+        uint32_t u0[32], u1[32], u2[32], u3[32];
+        tmem_ld32(tS + 0, u0);
+        tmem_ld32(tS + 32, u1);
+        tmem_ld32(tS + 64, u2);
+        tmem_ld32(tS + 96, u3);
+        tmem_ld_wait();
+        reg_fence(u0); reg_fence(u1); reg_fence(u2); reg_fence(u3);
 #pragma unroll
-      for (int c = 0; c < kTile / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tS + c * 32, u);
-        tmem_ld_wait(u);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(u[i]);
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(u0[i]);
+          s[32 + i] = __uint_as_float(u1[i]);
+          s[64 + i] = __uint_as_float(u2[i]);
+          s[96 + i] = __uint_as_float(u3[i]);
+        }
       }
       if (work == kMask) {
         const int lim = g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid;
