@@ -78,6 +78,7 @@ struct Cfg {
   static constexpr int bFinal = bODone + 2;
   static constexpr int kNumBars = bFinal + 1;
   static constexpr int kHolderOff = kBarBytes - 16;    // TMEM base address
+  static constexpr int kNeverOff = kBarBytes - 12;     // stays 0: waits that ignore aborts
   static constexpr int kAbortOff = kBarBytes - 8;      // abort flag
   static_assert(kNumBars * 8 <= kHolderOff, "barrier area overflow");
   // one CTA per SM: the kernel owns all 512 TMEM columns
@@ -103,6 +104,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   auto bar = [&](int i) -> uint32_t { return base + C::kBarOff + 8u * (uint32_t)i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kBarOff + C::kAbortOff);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + C::kBarOff + C::kHolderOff);
+  volatile int* never = reinterpret_cast<volatile int*>(base_ptr + C::kBarOff + C::kNeverOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -124,13 +126,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int seg = pair / pairs_per_seg;
   const int ti0 = (pair % pairs_per_seg) * 2;
   const int r = seg_owner(g, seg);
-  int q_lo[2], q_valid[2];
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int ti = ti0 + k;
-    q_lo[k] = seg * g.seg_len + ti * kTile;
-    q_valid[k] = ti < g.nt ? min(kTile, g.seg_len - ti * kTile) : 0;
-  }
+  // the two query tiles (scalars: runtime-indexed arrays go to local memory)
+  const int q_lo0 = seg * g.seg_len + ti0 * kTile;
+  const int q_lo1 = q_lo0 + kTile;
+  const int q_valid0 = min(kTile, g.seg_len - ti0 * kTile);
+  const int q_valid1 = ti0 + 1 < g.nt ? min(kTile, g.seg_len - (ti0 + 1) * kTile) : 0;
 
   // ---- set-up: barriers, abort flag, TMEM
   if (threadIdx.x == 0) {
@@ -148,6 +148,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     mbar_init(bar(C::bFinal), 1);
     *abort_flag = 0;
+    *never = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -164,17 +165,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (lane == 0) {
       const uint32_t q_smem = base + C::kQOff;
       mbar_arrive_expect_tx(bar(C::bQFull), 2 * C::kTileBytes);
-      for (int k = 0; k < 2; ++k)
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_load_4d(q_smem + k * C::kTileBytes + bx * kBoxBytes, &tm_q, bar(C::bQFull),
-                      bx * 64, h, q_lo[k], b);
+      for (int bx = 0; bx < C::kBoxes; ++bx) {
+        tma_load_4d(q_smem + bx * kBoxBytes, &tm_q, bar(C::bQFull), bx * 64, h, q_lo0, b);
+        tma_load_4d(q_smem + C::kTileBytes + bx * kBoxBytes, &tm_q, bar(C::bQFull), bx * 64,
+                    h, q_lo1, b);
+      }
       KvIter it;
       it.init(g);
       KvTile kv;
       int j = 0;
       while (it.next(g, r, kv)) {
-        if (tile_work(g, q_lo[0], q_valid[0], kv) == kSkip &&
-            tile_work(g, q_lo[1], q_valid[1], kv) == kSkip)
+        if (tile_work(g, q_lo0, q_valid0, kv) == kSkip &&
+            tile_work(g, q_lo1, q_valid1, kv) == kSkip)
           continue;
         const int s = j % C::kStages;
         const uint32_t use = (uint32_t)(j / C::kStages);
@@ -199,12 +201,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int jj = (j > C::kStages ? j - C::kStages : 0); jj < j; ++jj) {
         const int s = jj % C::kStages;
         const uint32_t ph = (uint32_t)(jj / C::kStages) & 1;
-        volatile int never = 0;
-        mbar_wait(bar(C::bKFull + s), ph, &never, kTimeoutNs);
-        mbar_wait(bar(C::bVFull + s), ph, &never, kTimeoutNs);
+        mbar_wait(bar(C::bKFull + s), ph, never, kTimeoutNs);
+        mbar_wait(bar(C::bVFull + s), ph, never, kTimeoutNs);
       }
-      volatile int never = 0;
-      mbar_wait(bar(C::bQFull), 0, &never, kTimeoutNs);
+      mbar_wait(bar(C::bQFull), 0, never, kTimeoutNs);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -212,70 +212,107 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTile, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
-      uint32_t n_pv[2] = {0, 0}, n_p[2] = {0, 0};
+      // per query tile: PV groups issued, P tiles consumed (scalars, not
+      // arrays: a runtime-indexed array would live in local memory)
+      uint32_t npv0 = 0, npv1 = 0, np0 = 0, np1 = 0;
       bool ok = mbar_wait(bar(C::bQFull), 0, abort_flag, kTimeoutNs);
       tc_fence_after();
       KvIter it;
       it.init(g);
-      KvTile kv;
-      int j = 0;
-      while (ok && it.next(g, r, kv)) {
-        bool act[2];
-        act[0] = tile_work(g, q_lo[0], q_valid[0], kv) != kSkip;
-        act[1] = tile_work(g, q_lo[1], q_valid[1], kv) != kSkip;
-        if (!act[0] && !act[1]) continue;
-        const int s = j % C::kStages;
-        const uint32_t ph = (uint32_t)(j / C::kStages) & 1;
-        const uint32_t k_smem = base + C::kKOff + s * C::kTileBytes;
-        const uint32_t v_smem = base + C::kVOff + s * C::kTileBytes;
-        if (!mbar_wait(bar(C::bKFull + s), ph, abort_flag, kTimeoutNs)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          if (!ok || !act[k]) continue;
-          // P_k of the previous tile aliases S_k: its PV must be done
-          if (n_pv[k] > 0) {
-            ok = mbar_wait(bar(C::bODone + k), (n_pv[k] - 1) & 1, abort_flag, kTimeoutNs);
-            tc_fence_after();
-          }
-          if (!ok) continue;
-          const uint32_t q_smem = base + C::kQOff + k * C::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
-            umma_ss(tmem + s_col(k), sw128_desc(q_smem + off, 16, 1024),
-                    sw128_desc(k_smem + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(bar(C::bSFull + k));
+
+      auto next_active = [&](KvTile& t, bool& a0, bool& a1) -> bool {
+        while (it.next(g, r, t)) {
+          a0 = tile_work(g, q_lo0, q_valid0, t) != kSkip;
+          a1 = tile_work(g, q_lo1, q_valid1, t) != kSkip;
+          if (a0 || a1) return true;
         }
-        if (!ok) break;
-        umma_commit(bar(C::bKEmpty + s));
-        if (!mbar_wait(bar(C::bVFull + s), ph, abort_flag, kTimeoutNs)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          if (!ok || !act[k]) continue;
-          ok = mbar_wait(bar(C::bPFull + k), n_p[k] & 1, abort_flag, kTimeoutNs);
-          if (!ok) continue;
-          ++n_p[k];
+        return false;
+      };
+      // S_k = Q_k K^T for the key tile in stage s. P_k of the previous key
+      // tile aliases S_k, so the previous PV of tile k must have completed.
+      auto issue_s = [&](int k, uint32_t npv, int s) {
+        if (npv > 0) {
+          ok = ok && mbar_wait(bar(C::bODone + k), (npv - 1) & 1, abort_flag, kTimeoutNs);
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            umma_ts(tmem + o_col(k), tmem + s_col(k) + kk * 8,
-                    sw128_desc(v_smem + kk * 2048, kBoxBytes, 1024), idesc_o,
-                    (n_pv[k] > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(bar(C::bODone + k));
-          ++n_pv[k];
         }
-        if (!ok) break;
-        umma_commit(bar(C::bVEmpty + s));
+        if (!ok) return;
+        const uint32_t q_smem = base + C::kQOff + k * C::kTileBytes;
+        const uint32_t k_smem = base + C::kKOff + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
+          umma_ss(tmem + s_col(k), sw128_desc(q_smem + off, 16, 1024),
+                  sw128_desc(k_smem + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(C::bSFull + k));
+      };
+      // O_k += P_k V for the value tile in stage s, once softmax published P_k.
+      auto issue_pv = [&](int k, uint32_t np, uint32_t npv, int s) {
+        ok = ok && mbar_wait(bar(C::bPFull + k), np & 1, abort_flag, kTimeoutNs);
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t v_smem = base + C::kVOff + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          umma_ts(tmem + o_col(k), tmem + s_col(k) + kk * 8,
+                  sw128_desc(v_smem + kk * 2048, kBoxBytes, 1024), idesc_o,
+                  (npv > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(C::bODone + k));
+      };
+      auto wait_full = [&](int which, int j) {
+        ok = ok && mbar_wait(bar(which + j % C::kStages), (uint32_t)(j / C::kStages) & 1,
+                             abort_flag, kTimeoutNs);
+        tc_fence_after();
+      };
+
+      // Software pipeline over the active key tiles j = 0, 1, ...:
+      //   prologue  S_0(0) S_1(0)
+      //   round j   PV_0(j) S_0(j+1) PV_1(j) S_1(j+1)
+      // S_k(j+1) goes right after PV_k(j) so that softmax k can start on the
+      // next tile while the tensor core works on the other query tile.
+      KvTile cur, nxt;
+      bool a0c = false, a1c = false, a0n = false, a1n = false;
+      bool have = ok && next_active(cur, a0c, a1c);
+      int j = 0;
+      if (have) {
+        wait_full(C::bKFull, 0);
+        if (a0c) issue_s(0, npv0, 0);
+        if (a1c) issue_s(1, npv1, 0);
+        if (ok) umma_commit(bar(C::bKEmpty + 0));
+      }
+      while (have && ok) {
+        const bool have_n = next_active(nxt, a0n, a1n);
+        const int s = j % C::kStages, sn = (j + 1) % C::kStages;
+        wait_full(C::bVFull, j);
+        if (a0c) {
+          issue_pv(0, np0, npv0, s);
+          ++np0;
+          ++npv0;
+        }
+        if (have_n) {
+          wait_full(C::bKFull, j + 1);
+          if (a0n) issue_s(0, npv0, sn);
+        }
+        if (a1c) {
+          issue_pv(1, np1, npv1, s);
+          ++np1;
+          ++npv1;
+        }
+        if (ok) umma_commit(bar(C::bVEmpty + s));
+        if (have_n) {
+          if (a1n) issue_s(1, npv1, sn);
+          if (ok) umma_commit(bar(C::bKEmpty + sn));
+        }
+        cur = nxt;
+        a0c = a0n;
+        a1c = a1n;
+        have = have_n;
         ++j;
       }
       // all tensor-core work of this CTA has completed before teardown
       umma_commit(bar(C::bFinal));
-      volatile int never = 0;
-      mbar_wait(bar(C::bFinal), 0, &never, kTimeoutNs);
+      mbar_wait(bar(C::bFinal), 0, never, kTimeoutNs);
     }
     __syncwarp();
   } else {
@@ -287,8 +324,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t tS = tmem + t_lane + s_col(k);
     const uint32_t tO = tmem + t_lane + o_col(k);
     // (selects, not indexing: a runtime index would put the arrays in local memory)
-    const int my_q_lo = k ? q_lo[1] : q_lo[0];
-    const int my_q_valid = k ? q_valid[1] : q_valid[0];
+    const int my_q_lo = k ? q_lo1 : q_lo0;
+    const int my_q_valid = k ? q_valid1 : q_valid0;
     const int q_pos = my_q_lo + row;
     const bool row_valid = row < my_q_valid;
     const float sl2 = g.scale_log2;
@@ -338,9 +375,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int c = 0; c < kTile; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // row max: 8 independent chains, then a tree (max is exact in any order)
+      float m8[8];
 #pragma unroll
-      for (int c = 1; c < kTile; ++c) mx = fmaxf(mx, s[c]);
+      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(s[i], s[8 + i]);
+#pragma unroll
+      for (int c = 16; c < kTile; c += 8)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[c + i]);
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const float m_new = fmaxf(m_run, mx * sl2);
       const bool resc = m_new > m_run + kRescaleLog2;
       float alpha = 1.f;
@@ -350,7 +394,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         l_run *= alpha;
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float sum = 0.f;
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
@@ -358,12 +402,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int i = 0; i < 32; ++i) {
           const float p0 = ex2_approx(fmaf(s[half * 64 + 2 * i], sl2, -m_use));
           const float p1 = ex2_approx(fmaf(s[half * 64 + 2 * i + 1], sl2, -m_use));
-          sum += p0 + p1;
+          sum4[(2 * i) & 3] += p0;
+          sum4[(2 * i + 1) & 3] += p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tS + half * 32, pk);
       }
-      l_run += sum;
+      l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       // O_k must be scaled by alpha before P_k V_j is added to it
       if (__any_sync(0xffffffffu, resc) && n_pv > 0) {
         ok = mbar_wait(bar(C::bODone + k), (n_pv - 1) & 1, abort_flag, kTimeoutNs);
