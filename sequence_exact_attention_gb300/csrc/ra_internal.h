@@ -4,7 +4,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/ring_attn.h"
+#include "ring_attn.h"
 
 namespace ra {
 
