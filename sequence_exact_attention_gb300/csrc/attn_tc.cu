@@ -13,11 +13,20 @@
 // One CTA owns a pair of 128-row query tiles of one (batch, head) inside one
 // segment of virtual rank r, and walks the key tiles of the ring in order.
 // "Receiving" a block is a TMA load of its tile from this GPU's HBM/L2 into a
-// shared-memory ring of stages. Warp roles (320 threads):
+// shared-memory ring of slots (K_0, V_0, K_1, V_1, ... in load order, so a
+// load can start as soon as the slot of the load kSlots earlier is free).
+// Warp roles (352 threads):
 //   warps 0-3  softmax for query tile 0 (one thread per row = TMEM lane)
 //   warps 4-7  softmax for query tile 1
-//   warp  8    TMA producer: Q once, then K/V tiles into the stage ring
-//   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
+//   warp  8    TMA producer: Q once, then K/V tiles into the slot ring
+//   warp  9    TMEM allocator; one thread issues tcgen05.mma for query tile 0
+//   warp 10    one thread issues tcgen05.mma for query tile 1
+//   warp 11    spare (completes the third warpgroup for register re-allocation)
+// The third warpgroup gives registers to the softmax warpgroups
+// (setmaxnreg: 168 at launch; 56 for warps 8-11, 224 for warps 0-7;
+// 128*56 + 256*224 = 384*168, the block's launch allocation).
+// Each query tile has its own issuing thread, so neither tile's chain
+// (S -> softmax -> PV -> next S) waits behind the other's.
 // Tensor memory (512 columns): tile k uses columns [256k, 256k+128) for the
 // f32 scores S = Q K^T, reused in place for P (bf16, packed two per column,
 // 64 columns) and [256k+128, 256k+128+D) for the f32 output accumulator O.
@@ -47,9 +56,10 @@ namespace {
 using namespace sm100;
 
 constexpr int kTile = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;         // 3 warpgroups; warp 11 only takes part in set-up
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp0 = 9;          // also allocates / frees TMEM
+constexpr int kMmaWarp1 = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;          // lazy rescale threshold (x256)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -59,24 +69,21 @@ template <int D>
 struct Cfg {
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kBoxes = D / 64;
-  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kSlots = D == 128 ? 5 : 8;     // K/V slot ring
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kSlotOff = kQOff + 2 * kTileBytes;
+  static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;   // + alignment slack
   // barrier indices (8 bytes each)
   static constexpr int bQFull = 0;
-  static constexpr int bKFull = 1;
-  static constexpr int bKEmpty = bKFull + kStages;
-  static constexpr int bVFull = bKEmpty + kStages;
-  static constexpr int bVEmpty = bVFull + kStages;
-  static constexpr int bSFull = bVEmpty + kStages;     // [2]
+  static constexpr int bFull = 1;                      // [kSlots]
+  static constexpr int bEmpty = bFull + kSlots;        // [kSlots], one arrival per issuer
+  static constexpr int bSFull = bEmpty + kSlots;       // [2]
   static constexpr int bPFull = bSFull + 2;            // [2]
   static constexpr int bODone = bPFull + 2;            // [2]
-  static constexpr int bFinal = bODone + 2;
-  static constexpr int kNumBars = bFinal + 1;
+  static constexpr int bFinal = bODone + 2;            // [2]
+  static constexpr int kNumBars = bFinal + 2;
   static constexpr int kHolderOff = kBarBytes - 16;    // TMEM base address
   static constexpr int kNeverOff = kBarBytes - 12;     // stays 0: waits that ignore aborts
   static constexpr int kAbortOff = kBarBytes - 8;      // abort flag
@@ -88,6 +95,43 @@ struct Cfg {
 
 __device__ __forceinline__ uint32_t s_col(int k) { return (uint32_t)(k * 256); }
 __device__ __forceinline__ uint32_t o_col(int k) { return (uint32_t)(k * 256 + 128); }
+
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+static_assert(128 * 56 + 256 * 224 <= 384 * 168, "register split exceeds the launch allocation");
+
+// Three-input maximum (sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two float32 lanes packed in one 64-bit register: d = a * b + c, d = a + b.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 template <int D, bool kOutF32>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -135,23 +179,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   // ---- set-up: barriers, abort flag, TMEM
   if (threadIdx.x == 0) {
     mbar_init(bar(C::bQFull), 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(C::bKFull + s), 1);
-      mbar_init(bar(C::bKEmpty + s), 1);
-      mbar_init(bar(C::bVFull + s), 1);
-      mbar_init(bar(C::bVEmpty + s), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(bar(C::bFull + s), 1);
+      mbar_init(bar(C::bEmpty + s), 2);
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(bar(C::bSFull + k), 1);
       mbar_init(bar(C::bPFull + k), 128);
       mbar_init(bar(C::bODone + k), 1);
+      mbar_init(bar(C::bFinal + k), 1);
     }
-    mbar_init(bar(C::bFinal), 1);
     *abort_flag = 0;
     *never = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp0) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
   }
@@ -160,6 +202,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
+  if (warp >= 8) {
+  setmaxnreg_dec<56>();
   if (warp == kProducerWarp) {
     // ======================= TMA producer =======================
     if (lane == 0) {
@@ -173,150 +217,107 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       KvIter it;
       it.init(g);
       KvTile kv;
-      int j = 0;
-      while (it.next(g, r, kv)) {
+      int n = 0;            // loads issued: K_j is load 2j, V_j is load 2j+1
+      bool ok = true;
+      while (ok && it.next(g, r, kv)) {
         if (tile_work(g, q_lo0, q_valid0, kv) == kSkip &&
             tile_work(g, q_lo1, q_valid1, kv) == kSkip)
           continue;
-        const int s = j % C::kStages;
-        const uint32_t use = (uint32_t)(j / C::kStages);
-        if (j >= C::kStages &&
-            !mbar_wait(bar(C::bKEmpty + s), (use - 1) & 1, abort_flag, kTimeoutNs))
-          break;
-        mbar_arrive_expect_tx(bar(C::bKFull + s), C::kTileBytes);
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_load_4d(base + C::kKOff + s * C::kTileBytes + bx * kBoxBytes, &tm_k,
-                      bar(C::bKFull + s), bx * 64, hk, kv.lo, b);
-        if (j >= C::kStages &&
-            !mbar_wait(bar(C::bVEmpty + s), (use - 1) & 1, abort_flag, kTimeoutNs))
-          break;
-        mbar_arrive_expect_tx(bar(C::bVFull + s), C::kTileBytes);
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_load_4d(base + C::kVOff + s * C::kTileBytes + bx * kBoxBytes, &tm_v,
-                      bar(C::bVFull + s), bx * 64, hk, kv.lo, b);
-        ++j;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {      // 0: K, 1: V
+          const int slot = n % C::kSlots;
+          const uint32_t use = (uint32_t)(n / C::kSlots);
+          if (n >= C::kSlots &&
+              !mbar_wait(bar(C::bEmpty + slot), (use - 1) & 1, abort_flag, kTimeoutNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(C::bFull + slot), C::kTileBytes);
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_4d(base + C::kSlotOff + slot * C::kTileBytes + bx * kBoxBytes,
+                        which ? (const void*)&tm_v : (const void*)&tm_k, bar(C::bFull + slot),
+                        bx * 64, hk, kv.lo, b);
+          ++n;
+        }
       }
       // Every issued load lands before the CTA leaves (already true unless
-      // the CTA aborted): wait, bounded, on the last use of each stage.
-      for (int jj = (j > C::kStages ? j - C::kStages : 0); jj < j; ++jj) {
-        const int s = jj % C::kStages;
-        const uint32_t ph = (uint32_t)(jj / C::kStages) & 1;
-        mbar_wait(bar(C::bKFull + s), ph, never, kTimeoutNs);
-        mbar_wait(bar(C::bVFull + s), ph, never, kTimeoutNs);
-      }
+      // the CTA aborted): wait, bounded, on the last use of each slot.
+      for (int nn = (n > C::kSlots ? n - C::kSlots : 0); nn < n; ++nn)
+        mbar_wait(bar(C::bFull + nn % C::kSlots), (uint32_t)(nn / C::kSlots) & 1, never,
+                  kTimeoutNs);
       mbar_wait(bar(C::bQFull), 0, never, kTimeoutNs);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ======================= MMA issuer =======================
+  } else if (warp == kMmaWarp0 || warp == kMmaWarp1) {
+    // ======================= MMA issuer of query tile k =======================
     if (lane == 0) {
+      const int k = warp - kMmaWarp0;
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTile, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
-      // per query tile: PV groups issued, P tiles consumed (scalars, not
-      // arrays: a runtime-indexed array would live in local memory)
-      uint32_t npv0 = 0, npv1 = 0, np0 = 0, np1 = 0;
+      const int my_q_lo = k ? q_lo1 : q_lo0;
+      const int my_q_valid = k ? q_valid1 : q_valid0;
+      const uint32_t q_smem = base + C::kQOff + k * C::kTileBytes;
+      const uint32_t d_s = tmem + s_col(k), d_o = tmem + o_col(k);
+      uint32_t npv = 0;     // PV groups issued for this tile (= P tiles consumed)
       bool ok = mbar_wait(bar(C::bQFull), 0, abort_flag, kTimeoutNs);
       tc_fence_after();
       KvIter it;
       it.init(g);
-
-      auto next_active = [&](KvTile& t, bool& a0, bool& a1) -> bool {
-        while (it.next(g, r, t)) {
-          a0 = tile_work(g, q_lo0, q_valid0, t) != kSkip;
-          a1 = tile_work(g, q_lo1, q_valid1, t) != kSkip;
-          if (a0 || a1) return true;
-        }
-        return false;
-      };
-      // S_k = Q_k K^T for the key tile in stage s. P_k of the previous key
-      // tile aliases S_k, so the previous PV of tile k must have completed.
-      auto issue_s = [&](int k, uint32_t npv, int s) {
-        if (npv > 0) {
-          ok = ok && mbar_wait(bar(C::bODone + k), (npv - 1) & 1, abort_flag, kTimeoutNs);
+      KvTile kv;
+      int j = 0;            // key tiles consumed (active for either query tile)
+      while (ok && it.next(g, r, kv)) {
+        const bool act = tile_work(g, my_q_lo, my_q_valid, kv) != kSkip;
+        if (!act && tile_work(g, k ? q_lo0 : q_lo1, k ? q_valid0 : q_valid1, kv) == kSkip)
+          continue;
+        const int nk = 2 * j, nv = 2 * j + 1;
+        const int sk = nk % C::kSlots, sv = nv % C::kSlots;
+        if (act) {
+          // S = Q K^T. P of the previous key tile aliases S: its PV must be done.
+          ok = mbar_wait(bar(C::bFull + sk), (uint32_t)(nk / C::kSlots) & 1, abort_flag,
+                         kTimeoutNs);
+          if (ok && npv > 0)
+            ok = mbar_wait(bar(C::bODone + k), (npv - 1) & 1, abort_flag, kTimeoutNs);
+          if (!ok) break;
           tc_fence_after();
-        }
-        if (!ok) return;
-        const uint32_t q_smem = base + C::kQOff + k * C::kTileBytes;
-        const uint32_t k_smem = base + C::kKOff + s * C::kTileBytes;
+          const uint32_t k_smem = base + C::kSlotOff + sk * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
-          umma_ss(tmem + s_col(k), sw128_desc(q_smem + off, 16, 1024),
-                  sw128_desc(k_smem + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(bar(C::bSFull + k));
-      };
-      // O_k += P_k V for the value tile in stage s, once softmax published P_k.
-      auto issue_pv = [&](int k, uint32_t np, uint32_t npv, int s) {
-        ok = ok && mbar_wait(bar(C::bPFull + k), np & 1, abort_flag, kTimeoutNs);
-        if (!ok) return;
-        tc_fence_after();
-        const uint32_t v_smem = base + C::kVOff + s * C::kTileBytes;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
+            umma_ss(d_s, sw128_desc(q_smem + off, 16, 1024), sw128_desc(k_smem + off, 16, 1024),
+                    idesc_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(C::bSFull + k));
+          umma_commit(bar(C::bEmpty + sk));
+          // O += P V once softmax has published P (and rescaled O).
+          ok = mbar_wait(bar(C::bFull + sv), (uint32_t)(nv / C::kSlots) & 1, abort_flag,
+                         kTimeoutNs) &&
+               mbar_wait(bar(C::bPFull + k), npv & 1, abort_flag, kTimeoutNs);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t v_smem = base + C::kSlotOff + sv * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          umma_ts(tmem + o_col(k), tmem + s_col(k) + kk * 8,
-                  sw128_desc(v_smem + kk * 2048, kBoxBytes, 1024), idesc_o,
-                  (npv > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_ts(d_o, d_s + kk * 8, sw128_desc(v_smem + kk * 2048, kBoxBytes, 1024), idesc_o,
+                    (npv > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar(C::bODone + k));
+          umma_commit(bar(C::bEmpty + sv));
+          ++npv;
+        } else {
+          // this tile does not use key tile j: release both slots for it
+          mbar_arrive(bar(C::bEmpty + sk));
+          mbar_arrive(bar(C::bEmpty + sv));
         }
-        umma_commit(bar(C::bODone + k));
-      };
-      auto wait_full = [&](int which, int j) {
-        ok = ok && mbar_wait(bar(which + j % C::kStages), (uint32_t)(j / C::kStages) & 1,
-                             abort_flag, kTimeoutNs);
-        tc_fence_after();
-      };
-
-      // Software pipeline over the active key tiles j = 0, 1, ...:
-      //   prologue  S_0(0) S_1(0)
-      //   round j   PV_0(j) S_0(j+1) PV_1(j) S_1(j+1)
-      // S_k(j+1) goes right after PV_k(j) so that softmax k can start on the
-      // next tile while the tensor core works on the other query tile.
-      KvTile cur, nxt;
-      bool a0c = false, a1c = false, a0n = false, a1n = false;
-      bool have = ok && next_active(cur, a0c, a1c);
-      int j = 0;
-      if (have) {
-        wait_full(C::bKFull, 0);
-        if (a0c) issue_s(0, npv0, 0);
-        if (a1c) issue_s(1, npv1, 0);
-        if (ok) umma_commit(bar(C::bKEmpty + 0));
-      }
-      while (have && ok) {
-        const bool have_n = next_active(nxt, a0n, a1n);
-        const int s = j % C::kStages, sn = (j + 1) % C::kStages;
-        wait_full(C::bVFull, j);
-        if (a0c) {
-          issue_pv(0, np0, npv0, s);
-          ++np0;
-          ++npv0;
-        }
-        if (have_n) {
-          wait_full(C::bKFull, j + 1);
-          if (a0n) issue_s(0, npv0, sn);
-        }
-        if (a1c) {
-          issue_pv(1, np1, npv1, s);
-          ++np1;
-          ++npv1;
-        }
-        if (ok) umma_commit(bar(C::bVEmpty + s));
-        if (have_n) {
-          if (a1n) issue_s(1, npv1, sn);
-          if (ok) umma_commit(bar(C::bKEmpty + sn));
-        }
-        cur = nxt;
-        a0c = a0n;
-        a1c = a1n;
-        have = have_n;
         ++j;
       }
-      // all tensor-core work of this CTA has completed before teardown
-      umma_commit(bar(C::bFinal));
-      mbar_wait(bar(C::bFinal), 0, never, kTimeoutNs);
+      // all tensor-core work this thread issued has completed before teardown
+      umma_commit(bar(C::bFinal + k));
+      mbar_wait(bar(C::bFinal + k), 0, never, kTimeoutNs);
     }
     __syncwarp();
+  }
   } else {
     // ======================= softmax, one thread per row =======================
+    setmaxnreg_inc<224>();
     const int k = warp >> 2;                 // query tile of this warpgroup
     const int wq = warp & 3;                 // TMEM lane quarter
     const int row = wq * 32 + lane;
@@ -329,6 +330,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int q_pos = my_q_lo + row;
     const bool row_valid = row < my_q_valid;
     const float sl2 = g.scale_log2;
+    const uint64_t sl2x2 = pack2(sl2, sl2);
 
     const int n_qt = g.n_seg * g.nt;
     int* log_base = (vlog && my_q_valid > 0 && (threadIdx.x & 127) == 0)
@@ -337,7 +339,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     int n_vis = 0;
 
     float m_run = -INFINITY, l_run = 0.f;
-    uint32_t n_s = 0, n_pv = 0;
+    uint32_t n_pv = 0;       // P tiles published (= S tiles consumed)
     bool ok = true;
     KvIter it;
     it.init(g);
@@ -347,9 +349,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (work == kSkip) continue;
       if (log_base) log_visit(log_base, n_vis, kv, tile_class(g, my_q_lo, kv));
       ++n_vis;
-      ok = mbar_wait(bar(C::bSFull + k), n_s & 1, abort_flag, kTimeoutNs);
+      ok = mbar_wait(bar(C::bSFull + k), n_pv & 1, abort_flag, kTimeoutNs);
       if (!ok) break;
-      ++n_s;
       tc_fence_after();
 
       float s[kTile];
@@ -375,16 +376,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int c = 0; c < kTile; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      // row max: 8 independent chains, then a tree (max is exact in any order)
+      // row max: 8 independent chains of 3-input maxima, then a tree
       float m8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(s[i], s[8 + i]);
+      for (int i = 0; i < 8; ++i) m8[i] = fmax3(s[i], s[8 + i], s[16 + i]);
 #pragma unroll
-      for (int c = 16; c < kTile; c += 8)
+      for (int c = 24; c < kTile - 8; c += 16)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[c + i]);
-      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[c + i], s[c + 8 + i]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[kTile - 8 + i]);
+      const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                             fmaxf(m8[6], m8[7]));
       const float m_new = fmaxf(m_run, mx * sl2);
       const bool resc = m_new > m_run + kRescaleLog2;
       float alpha = 1.f;
@@ -394,21 +397,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         l_run *= alpha;
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t neg_m2 = pack2(-m_use, -m_use);
+      uint64_t sum2a = pack2(0.f, 0.f), sum2b = sum2a;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2_approx(fmaf(s[half * 64 + 2 * i], sl2, -m_use));
-          const float p1 = ex2_approx(fmaf(s[half * 64 + 2 * i + 1], sl2, -m_use));
-          sum4[(2 * i) & 3] += p0;
-          sum4[(2 * i + 1) & 3] += p1;
+          // (s0, s1) * scale*log2(e) - m in one packed FMA, then two exp2
+          const uint64_t x2 = ffma2(pack2(s[half * 64 + 2 * i], s[half * 64 + 2 * i + 1]),
+                                    sl2x2, neg_m2);
+          float x0, x1;
+          unpack2(x2, x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          if (i & 1) sum2b = fadd2(sum2b, pack2(p0, p1));
+          else sum2a = fadd2(sum2a, pack2(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tS + half * 32, pk);
       }
-      l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      {
+        float a0, a1;
+        unpack2(fadd2(sum2a, sum2b), a0, a1);
+        l_run += a0 + a1;
+      }
       // O_k must be scaled by alpha before P_k V_j is added to it
       if (__any_sync(0xffffffffu, resc) && n_pv > 0) {
         ok = mbar_wait(bar(C::bODone + k), (n_pv - 1) & 1, abort_flag, kTimeoutNs);
@@ -481,7 +494,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   // ---- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
