@@ -303,8 +303,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           umma_commit(bar(C::bEmpty + sv));
           ++npv;
         } else {
-          // this tile does not use key tile j: release both slots for it
-          mbar_arrive(bar(C::bEmpty + sk));
+          // This tile does not use key tile j; it still owes one release per
+          // slot. Waiting for each load first keeps the release in step with
+          // the slot's use: an early arrive would count toward the slot's
+          // NEXT use and free it while the other tile still reads it.
+          ok = mbar_wait(bar(C::bFull + sk), (uint32_t)(nk / C::kSlots) & 1, abort_flag,
+                         kTimeoutNs);
+          if (ok) mbar_arrive(bar(C::bEmpty + sk));
+          ok = ok && mbar_wait(bar(C::bFull + sv), (uint32_t)(nv / C::kSlots) & 1, abort_flag,
+                               kTimeoutNs);
+          if (!ok) break;
           mbar_arrive(bar(C::bEmpty + sv));
         }
         ++j;
