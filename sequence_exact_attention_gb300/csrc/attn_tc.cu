@@ -19,14 +19,11 @@
 //   warps 0-3  softmax for query tile 0 (one thread per row = TMEM lane)
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer: Q once, then K/V tiles into the slot ring
-//   warp  9    TMEM allocator; one thread issues tcgen05.mma for query tile 0
-//   warp 10    one thread issues tcgen05.mma for query tile 1
-//   warp 11    spare (completes the third warpgroup for register re-allocation)
+//   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
+//   warps 10-11 spare (complete the third warpgroup for register re-allocation)
 // The third warpgroup gives registers to the softmax warpgroups
 // (setmaxnreg: 168 at launch; 56 for warps 8-11, 224 for warps 0-7;
 // 128*56 + 256*224 = 384*168, the block's launch allocation).
-// Each query tile has its own issuing thread, so neither tile's chain
-// (S -> softmax -> PV -> next S) waits behind the other's.
 // Tensor memory (512 columns): tile k uses columns [256k, 256k+128) for the
 // f32 scores S = Q K^T, reused in place for P (bf16, packed two per column,
 // 64 columns) and [256k+128, 256k+128+D) for the f32 output accumulator O.
@@ -56,10 +53,9 @@ namespace {
 using namespace sm100;
 
 constexpr int kTile = 128;
-constexpr int kThreads = 384;         // 3 warpgroups; warp 11 only takes part in set-up
+constexpr int kThreads = 384;         // 3 warpgroups; warps 10-11 only take part in set-up
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp0 = 9;          // also allocates / frees TMEM
-constexpr int kMmaWarp1 = 10;
+constexpr int kMmaWarp = 9;           // also allocates / frees TMEM
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;          // lazy rescale threshold (x256)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -78,12 +74,12 @@ struct Cfg {
   // barrier indices (8 bytes each)
   static constexpr int bQFull = 0;
   static constexpr int bFull = 1;                      // [kSlots]
-  static constexpr int bEmpty = bFull + kSlots;        // [kSlots], one arrival per issuer
+  static constexpr int bEmpty = bFull + kSlots;        // [kSlots]
   static constexpr int bSFull = bEmpty + kSlots;       // [2]
   static constexpr int bPFull = bSFull + 2;            // [2]
   static constexpr int bODone = bPFull + 2;            // [2]
-  static constexpr int bFinal = bODone + 2;            // [2]
-  static constexpr int kNumBars = bFinal + 2;
+  static constexpr int bFinal = bODone + 2;
+  static constexpr int kNumBars = bFinal + 1;
   static constexpr int kHolderOff = kBarBytes - 16;    // TMEM base address
   static constexpr int kNeverOff = kBarBytes - 12;     // stays 0: waits that ignore aborts
   static constexpr int kAbortOff = kBarBytes - 8;      // abort flag
@@ -104,7 +100,7 @@ template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
-static_assert(128 * 56 + 256 * 224 <= 384 * 168, "register split exceeds the launch allocation");
+static_assert(128 * 64 + 256 * 216 <= 384 * 168, "register split exceeds the launch allocation");
 
 // Three-input maximum (sm_100 family).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -181,19 +177,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(bar(C::bQFull), 1);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(bar(C::bFull + s), 1);
-      mbar_init(bar(C::bEmpty + s), 2);
+      mbar_init(bar(C::bEmpty + s), 1);
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(bar(C::bSFull + k), 1);
       mbar_init(bar(C::bPFull + k), 128);
       mbar_init(bar(C::bODone + k), 1);
-      mbar_init(bar(C::bFinal + k), 1);
     }
+    mbar_init(bar(C::bFinal), 1);
     *abort_flag = 0;
     *never = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp0) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
   }
@@ -203,7 +199,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   const uint32_t tmem = *tmem_holder;
 
   if (warp >= 8) {
-  setmaxnreg_dec<56>();
+  setmaxnreg_dec<64>();
   if (warp == kProducerWarp) {
     // ======================= TMA producer =======================
     if (lane == 0) {
@@ -248,84 +244,116 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_wait(bar(C::bQFull), 0, never, kTimeoutNs);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp0 || warp == kMmaWarp1) {
-    // ======================= MMA issuer of query tile k =======================
+  } else if (warp == kMmaWarp) {
+    // ======================= MMA issuer (one thread) =======================
     if (lane == 0) {
-      const int k = warp - kMmaWarp0;
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTile, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
-      const int my_q_lo = k ? q_lo1 : q_lo0;
-      const int my_q_valid = k ? q_valid1 : q_valid0;
-      const uint32_t q_smem = base + C::kQOff + k * C::kTileBytes;
-      const uint32_t d_s = tmem + s_col(k), d_o = tmem + o_col(k);
-      uint32_t npv = 0;     // PV groups issued for this tile (= P tiles consumed)
+      // PV groups issued per query tile (scalars, not an array: a
+      // runtime-indexed array would live in local memory)
+      uint32_t npv0 = 0, npv1 = 0;
       bool ok = mbar_wait(bar(C::bQFull), 0, abort_flag, kTimeoutNs);
       tc_fence_after();
       KvIter it;
       it.init(g);
-      KvTile kv;
-      int j = 0;            // key tiles consumed (active for either query tile)
-      while (ok && it.next(g, r, kv)) {
-        const bool act = tile_work(g, my_q_lo, my_q_valid, kv) != kSkip;
-        if (!act && tile_work(g, k ? q_lo0 : q_lo1, k ? q_valid0 : q_valid1, kv) == kSkip)
-          continue;
-        const int nk = 2 * j, nv = 2 * j + 1;
-        const int sk = nk % C::kSlots, sv = nv % C::kSlots;
-        if (act) {
-          // S = Q K^T. P of the previous key tile aliases S: its PV must be done.
-          ok = mbar_wait(bar(C::bFull + sk), (uint32_t)(nk / C::kSlots) & 1, abort_flag,
-                         kTimeoutNs);
-          if (ok && npv > 0)
-            ok = mbar_wait(bar(C::bODone + k), (npv - 1) & 1, abort_flag, kTimeoutNs);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t k_smem = base + C::kSlotOff + sk * C::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
-            umma_ss(d_s, sw128_desc(q_smem + off, 16, 1024), sw128_desc(k_smem + off, 16, 1024),
-                    idesc_s, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(bar(C::bSFull + k));
-          umma_commit(bar(C::bEmpty + sk));
-          // O += P V once softmax has published P (and rescaled O).
-          ok = mbar_wait(bar(C::bFull + sv), (uint32_t)(nv / C::kSlots) & 1, abort_flag,
-                         kTimeoutNs) &&
-               mbar_wait(bar(C::bPFull + k), npv & 1, abort_flag, kTimeoutNs);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t v_smem = base + C::kSlotOff + sv * C::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ts(d_o, d_s + kk * 8, sw128_desc(v_smem + kk * 2048, kBoxBytes, 1024), idesc_o,
-                    (npv > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar(C::bODone + k));
-          umma_commit(bar(C::bEmpty + sv));
-          ++npv;
-        } else {
-          // This tile does not use key tile j; it still owes one release per
-          // slot. Waiting for each load first keeps the release in step with
-          // the slot's use: an early arrive would count toward the slot's
-          // NEXT use and free it while the other tile still reads it.
-          ok = mbar_wait(bar(C::bFull + sk), (uint32_t)(nk / C::kSlots) & 1, abort_flag,
-                         kTimeoutNs);
-          if (ok) mbar_arrive(bar(C::bEmpty + sk));
-          ok = ok && mbar_wait(bar(C::bFull + sv), (uint32_t)(nv / C::kSlots) & 1, abort_flag,
-                               kTimeoutNs);
-          if (!ok) break;
-          mbar_arrive(bar(C::bEmpty + sv));
+
+      auto next_active = [&](KvTile& t, bool& a0, bool& a1) -> bool {
+        while (it.next(g, r, t)) {
+          a0 = tile_work(g, q_lo0, q_valid0, t) != kSkip;
+          a1 = tile_work(g, q_lo1, q_valid1, t) != kSkip;
+          if (a0 || a1) return true;
         }
+        return false;
+      };
+      // load n of the slot ring: K_j is load 2j, V_j is load 2j+1
+      auto wait_load = [&](int n) {
+        ok = ok && mbar_wait(bar(C::bFull + n % C::kSlots), (uint32_t)(n / C::kSlots) & 1,
+                             abort_flag, kTimeoutNs);
+        tc_fence_after();
+      };
+      // S_k = Q_k K_j^T. P_k of the previous key tile aliases S_k, so the
+      // previous PV of tile k must have completed first.
+      auto issue_s = [&](int k, uint32_t npv, int j) {
+        if (ok && npv > 0) {
+          ok = mbar_wait(bar(C::bODone + k), (npv - 1) & 1, abort_flag, kTimeoutNs);
+          tc_fence_after();
+        }
+        if (!ok) return;
+        const uint32_t q_smem = base + C::kQOff + k * C::kTileBytes;
+        const uint32_t k_smem = base + C::kSlotOff + ((2 * j) % C::kSlots) * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
+          umma_ss(tmem + s_col(k), sw128_desc(q_smem + off, 16, 1024),
+                  sw128_desc(k_smem + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(C::bSFull + k));
+      };
+      // O_k += P_k V_j once softmax k has published P_k (and rescaled O_k).
+      auto issue_pv = [&](int k, uint32_t npv, int j) {
+        ok = ok && mbar_wait(bar(C::bPFull + k), npv & 1, abort_flag, kTimeoutNs);
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t v_smem = base + C::kSlotOff + ((2 * j + 1) % C::kSlots) * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ts(tmem + o_col(k), tmem + s_col(k) + kk * 8,
+                  sw128_desc(v_smem + kk * 2048, kBoxBytes, 1024), idesc_o,
+                  (npv > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(C::bODone + k));
+      };
+
+      // Software pipeline over the active key tiles j = 0, 1, ...:
+      //   prologue  S_0(0) S_1(0)
+      //   round j   PV_0(j) S_0(j+1) PV_1(j) S_1(j+1)
+      // S_k(j+1) follows PV_k(j) so that softmax 0 works while the tensor
+      // core runs tile 1's pair of MMAs and the other way round (the two
+      // softmax warpgroups stay half a round apart).
+      KvTile cur, nxt;
+      bool a0c = false, a1c = false, a0n = false, a1n = false;
+      bool have = ok && next_active(cur, a0c, a1c);
+      int j = 0;
+      if (have) {
+        wait_load(0);
+        if (a0c) issue_s(0, npv0, 0);
+        if (a1c) issue_s(1, npv1, 0);
+        if (ok) umma_commit(bar(C::bEmpty + 0));
+      }
+      while (have && ok) {
+        const bool have_n = next_active(nxt, a0n, a1n);
+        wait_load(2 * j + 1);
+        if (a0c) {
+          issue_pv(0, npv0, j);
+          ++npv0;
+        }
+        if (have_n) {
+          wait_load(2 * j + 2);
+          if (a0n) issue_s(0, npv0, j + 1);
+        }
+        if (a1c) {
+          issue_pv(1, npv1, j);
+          ++npv1;
+        }
+        if (ok) umma_commit(bar(C::bEmpty + (2 * j + 1) % C::kSlots));   // V_j
+        if (have_n) {
+          if (a1n) issue_s(1, npv1, j + 1);
+          if (ok) umma_commit(bar(C::bEmpty + (2 * j + 2) % C::kSlots));   // K_{j+1}
+        }
+        cur = nxt;
+        a0c = a0n;
+        a1c = a1n;
+        have = have_n;
         ++j;
       }
-      // all tensor-core work this thread issued has completed before teardown
-      umma_commit(bar(C::bFinal + k));
-      mbar_wait(bar(C::bFinal + k), 0, never, kTimeoutNs);
+      // all tensor-core work of this CTA has completed before teardown
+      umma_commit(bar(C::bFinal));
+      mbar_wait(bar(C::bFinal), 0, never, kTimeoutNs);
     }
     __syncwarp();
   }
   } else {
     // ======================= softmax, one thread per row =======================
-    setmaxnreg_inc<224>();
+    setmaxnreg_inc<216>();
     const int k = warp >> 2;                 // query tile of this warpgroup
     const int wq = warp & 3;                 // TMEM lane quarter
     const int row = wq * 32 + lane;
@@ -502,7 +530,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   // ---- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp0) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
