@@ -70,7 +70,9 @@ struct Cfg {
   static constexpr int kSlotOff = kQOff + 2 * kTileBytes;
   static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;   // + alignment slack
+  static constexpr int kFlagsOff = kBarBytes;          // 16 x u32: key-tile flags ring
+  static constexpr int kFlagsBytes = 64;
+  static constexpr int kSmemBytes = kBarOff + kBarBytes + kFlagsBytes + 1024;   // + alignment slack
   // barrier indices (8 bytes each)
   static constexpr int bQFull = 0;
   static constexpr int bFull = 1;                      // [kSlots]
@@ -145,6 +147,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kBarOff + C::kAbortOff);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + C::kBarOff + C::kHolderOff);
   volatile int* never = reinterpret_cast<volatile int*>(base_ptr + C::kBarOff + C::kNeverOff);
+  // Key-tile flags, written by the producer before it arms K_j's slot and
+  // read by the MMA thread after that slot's load completed: bit 0/1 = query
+  // tile 0/1 uses key tile j, bit 2 = no key tile j (end of the sequence).
+  volatile uint32_t* tile_flags =
+      reinterpret_cast<volatile uint32_t*>(base_ptr + C::kBarOff + C::kFlagsOff);
+  constexpr uint32_t kFlagEnd = 4u;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -216,9 +224,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       int n = 0;            // loads issued: K_j is load 2j, V_j is load 2j+1
       bool ok = true;
       while (ok && it.next(g, r, kv)) {
-        if (tile_work(g, q_lo0, q_valid0, kv) == kSkip &&
-            tile_work(g, q_lo1, q_valid1, kv) == kSkip)
-          continue;
+        const bool act0 = tile_work(g, q_lo0, q_valid0, kv) != kSkip;
+        const bool act1 = tile_work(g, q_lo1, q_valid1, kv) != kSkip;
+        if (!act0 && !act1) continue;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {      // 0: K, 1: V
           const int slot = n % C::kSlots;
@@ -228,12 +236,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             ok = false;
             break;
           }
+          if (which == 0) tile_flags[(n >> 1) & 15] = (act0 ? 1u : 0u) | (act1 ? 2u : 0u);
           mbar_arrive_expect_tx(bar(C::bFull + slot), C::kTileBytes);
           for (int bx = 0; bx < C::kBoxes; ++bx)
             tma_load_4d(base + C::kSlotOff + slot * C::kTileBytes + bx * kBoxBytes,
                         which ? (const void*)&tm_v : (const void*)&tm_k, bar(C::bFull + slot),
                         bx * 64, hk, kv.lo, b);
           ++n;
+        }
+      }
+      // End marker: K's slot of the key tile after the last one completes
+      // with no load and the flag kFlagEnd.
+      if (ok) {
+        const int slot = n % C::kSlots;
+        const uint32_t use = (uint32_t)(n / C::kSlots);
+        if (n < C::kSlots ||
+            mbar_wait(bar(C::bEmpty + slot), (use - 1) & 1, abort_flag, kTimeoutNs)) {
+          tile_flags[(n >> 1) & 15] = kFlagEnd;
+          mbar_arrive(bar(C::bFull + slot));
         }
       }
       // Every issued load lands before the CTA leaves (already true unless
@@ -254,17 +274,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       uint32_t npv0 = 0, npv1 = 0;
       bool ok = mbar_wait(bar(C::bQFull), 0, abort_flag, kTimeoutNs);
       tc_fence_after();
-      KvIter it;
-      it.init(g);
-
-      auto next_active = [&](KvTile& t, bool& a0, bool& a1) -> bool {
-        while (it.next(g, r, t)) {
-          a0 = tile_work(g, q_lo0, q_valid0, t) != kSkip;
-          a1 = tile_work(g, q_lo1, q_valid1, t) != kSkip;
-          if (a0 || a1) return true;
-        }
-        return false;
-      };
       // load n of the slot ring: K_j is load 2j, V_j is load 2j+1
       auto wait_load = [&](int n) {
         ok = ok && mbar_wait(bar(C::bFull + n % C::kSlots), (uint32_t)(n / C::kSlots) & 1,
@@ -309,27 +318,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       // S_k(j+1) follows PV_k(j) so that softmax 0 works while the tensor
       // core runs tile 1's pair of MMAs and the other way round (the two
       // softmax warpgroups stay half a round apart).
-      KvTile cur, nxt;
-      bool a0c = false, a1c = false, a0n = false, a1n = false;
-      bool have = ok && next_active(cur, a0c, a1c);
+      // The key-tile sequence comes from the producer's flags (read after
+      // the K load of that tile completed), so this thread does no index
+      // arithmetic between the MMAs it issues.
+      wait_load(0);
+      uint32_t f = ok ? tile_flags[0] : kFlagEnd;
+      bool have = !(f & kFlagEnd);
+      bool a0c = f & 1u, a1c = f & 2u;
       int j = 0;
       if (have) {
-        wait_load(0);
         if (a0c) issue_s(0, npv0, 0);
         if (a1c) issue_s(1, npv1, 0);
         if (ok) umma_commit(bar(C::bEmpty + 0));
       }
       while (have && ok) {
-        const bool have_n = next_active(nxt, a0n, a1n);
         wait_load(2 * j + 1);
         if (a0c) {
           issue_pv(0, npv0, j);
           ++npv0;
         }
-        if (have_n) {
-          wait_load(2 * j + 2);
-          if (a0n) issue_s(0, npv0, j + 1);
-        }
+        wait_load(2 * j + 2);
+        f = ok ? tile_flags[(j + 1) & 15] : kFlagEnd;
+        const bool have_n = !(f & kFlagEnd);
+        const bool a0n = have_n && (f & 1u), a1n = have_n && (f & 2u);
+        if (a0n) issue_s(0, npv0, j + 1);
         if (a1c) {
           issue_pv(1, npv1, j);
           ++npv1;
@@ -339,7 +351,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           if (a1n) issue_s(1, npv1, j + 1);
           if (ok) umma_commit(bar(C::bEmpty + (2 * j + 2) % C::kSlots));   // K_{j+1}
         }
-        cur = nxt;
         a0c = a0n;
         a1c = a1n;
         have = have_n;
