@@ -245,6 +245,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           ++n;
         }
       }
+      // Every issued load lands before the CTA leaves (already true unless
+      // the CTA aborted): wait, bounded, on the last use of each slot. This
+      // comes before the end marker, which completes one more phase of a slot.
+      for (int nn = (n > C::kSlots ? n - C::kSlots : 0); nn < n; ++nn)
+        mbar_wait(bar(C::bFull + nn % C::kSlots), (uint32_t)(nn / C::kSlots) & 1, never,
+                  kTimeoutNs);
+      mbar_wait(bar(C::bQFull), 0, never, kTimeoutNs);
       // End marker: K's slot of the key tile after the last one completes
       // with no load and the flag kFlagEnd.
       if (ok) {
@@ -256,12 +263,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           mbar_arrive(bar(C::bFull + slot));
         }
       }
-      // Every issued load lands before the CTA leaves (already true unless
-      // the CTA aborted): wait, bounded, on the last use of each slot.
-      for (int nn = (n > C::kSlots ? n - C::kSlots : 0); nn < n; ++nn)
-        mbar_wait(bar(C::bFull + nn % C::kSlots), (uint32_t)(nn / C::kSlots) & 1, never,
-                  kTimeoutNs);
-      mbar_wait(bar(C::bQFull), 0, never, kTimeoutNs);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -545,7 +546,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (threadIdx.x == 0 && *abort_flag && status) atomicExch(status, (int)RA_ERR_TIMEOUT);
+  // a wait that expired anywhere, including the teardown drains, is reported
+  if (threadIdx.x == 0 && (*abort_flag || *never) && status)
+    atomicExch(status, (int)RA_ERR_TIMEOUT);
 }
 
 // ------------------------------------------------------------------ host
