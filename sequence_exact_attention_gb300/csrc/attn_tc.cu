@@ -322,6 +322,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       // The key-tile sequence comes from the producer's flags (read after
       // the K load of that tile completed), so this thread does no index
       // arithmetic between the MMAs it issues.
+      // Waits and slot releases sit where the tensor core still has queued
+      // work: V_j is waited for before S_1 is issued (not before PV_0), and
+      // the release of K_j's slot is committed after PV_0(j).
       wait_load(0);
       uint32_t f = ok ? tile_flags[0] : kFlagEnd;
       bool have = !(f & kFlagEnd);
@@ -329,15 +332,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       int j = 0;
       if (have) {
         if (a0c) issue_s(0, npv0, 0);
+        wait_load(1);
         if (a1c) issue_s(1, npv1, 0);
-        if (ok) umma_commit(bar(C::bEmpty + 0));
       }
       while (have && ok) {
-        wait_load(2 * j + 1);
         if (a0c) {
           issue_pv(0, npv0, j);
           ++npv0;
         }
+        if (ok) umma_commit(bar(C::bEmpty + (2 * j) % C::kSlots));         // K_j
         wait_load(2 * j + 2);
         f = ok ? tile_flags[(j + 1) & 15] : kFlagEnd;
         const bool have_n = !(f & kFlagEnd);
@@ -347,10 +350,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           issue_pv(1, npv1, j);
           ++npv1;
         }
-        if (ok) umma_commit(bar(C::bEmpty + (2 * j + 1) % C::kSlots));   // V_j
+        if (ok) umma_commit(bar(C::bEmpty + (2 * j + 1) % C::kSlots));     // V_j
         if (have_n) {
+          wait_load(2 * j + 3);
           if (a1n) issue_s(1, npv1, j + 1);
-          if (ok) umma_commit(bar(C::bEmpty + (2 * j + 2) % C::kSlots));   // K_{j+1}
         }
         a0c = a0n;
         a1c = a1n;
