@@ -34,7 +34,7 @@ UNIT = "TFLOP/s"
 
 # ncu DRAM bytes (read + write) of one launch of the tensor-core kernel on the
 # headline workload, valid only for the kernel source with this digest.
-TRAFFIC = {"attn_tc_sha256_16": None, "bytes_per_launch": None}
+TRAFFIC = {"attn_tc_sha256_16": None, "workload": None, "bytes_per_launch": None}
 
 
 def _env_int(name, default):
@@ -194,10 +194,13 @@ def run_reference(args, w):
 
 
 def _config(w):
+    esz = 2 if w.dtype == "bf16" else 4
+    in_mib = w.B * w.S * (w.H_q + 2 * w.H_kv) * w.D * esz / 2**20
+    l2 = (f"inputs larger than L2 (q+k+v {in_mib:.0f} MiB vs 126 MiB L2)" if in_mib > 126
+          else f"inputs fit in L2 (q+k+v {in_mib:.1f} MiB); no flush")
     return {"workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "S": w.S,
             "D": w.D, "P": w.P, "causal": w.causal, "order": w.order,
-            "input_dist": f"N(0,{w.std}^2) bf16" if w.dtype == "bf16" else "N(0,1) f32",
-            "l2": "inputs larger than L2 (q, k, v 256 MiB each vs 126 MiB L2)",
+            "input_dist": f"N(0,{w.std}^2) {w.dtype}", "l2": l2,
             "parallelism": "replicas"}
 
 
@@ -315,11 +318,21 @@ def run_ours(args, w):
         return 0
 
     peaks, peak_src = _peaks()
-    peak = float(peaks.get("bf16_tflops"))
     achieved = flop / (kernel_ms / 1e3) / 1e12
-    digest = _kernel_digest()
-    traffic = (TRAFFIC["bytes_per_launch"]
-               if TRAFFIC["attn_tc_sha256_16"] == digest else None)
+    if w.dtype == "bf16":
+        bound, peak = "tensor", float(peaks.get("bf16_tflops"))
+        peak_note = f"{peak_src} bf16 dense (burst)"
+        kname = f"attn_tc_kernel<{w.D},false>"
+        digest = _kernel_digest()
+        traffic = (TRAFFIC["bytes_per_launch"]
+                   if TRAFFIC["attn_tc_sha256_16"] == digest and w.name == TRAFFIC.get("workload")
+                   else None)
+    else:
+        # exact fp32 FMA path: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz
+        bound, peak = "alu", 152 * 128 * 2 * 2.07e9 / 1e12
+        peak_note = "fp32 FMA: SM count x lanes x 2 x max SM clock"
+        kname = f"attn_simt_kernel<{w.D}>"
+        traffic = None
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -333,13 +346,11 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": _config(w),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16 dense (burst)",
-                     "kernel": "attn_tc_kernel<128,false>",
-                     "kernel_ms": kernel_ms},
+                     "peak_source": peak_note, "kernel": kname, "kernel_ms": kernel_ms},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clk,
@@ -349,14 +360,82 @@ def run_ours(args, w):
     return 0
 
 
+def run_merge(args, w):
+    """The standalone n-way LSE merge on its workload; HBM-bound, GB/s."""
+    import torch
+    from sequence_exact_attention_gb300 import binding
+    from sequence_exact_attention_gb300.workloads import make_merge_parts
+
+    world, rank, local, dist = _dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load()
+    os_, ls = make_merge_parts(w)
+    od = [o.to(dev) for o in os_]
+    ld = [l.to(dev) for l in ls]
+    out = torch.empty_like(od[0])
+    lse = torch.empty_like(ld[0])
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        binding.attn_lse_merge_n(od, ld, out=out, lse=lse, stream=stream)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        binding.attn_lse_merge_n(od, ld, out=out, lse=lse, stream=stream)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if rank != 0:
+        return 0
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    peaks, src = _peaks()
+    gbs = w.bytes / (kernel_ms / 1e3) / 1e9
+    line = {
+        "metric": "LSE merge GB/s (algorithmic bytes)", "value":
+            world * w.bytes * args.steps / (total_ms / 1e3) / 1e9,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32" if w.dtype == "f32" else "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "n": w.n, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
+                   "l2": "inputs larger than L2 (8 GiB of partials)"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]),
+                     "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                     "peak_source": f"{src} HBM copy", "kernel": "lse_merge_kernel",
+                     "kernel_ms": kernel_ms},
+        "clocks": clk, "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
-    from sequence_exact_attention_gb300.workloads import WORKLOADS, HEADLINE
+    from sequence_exact_attention_gb300.workloads import WORKLOADS, HEADLINE, MERGE_WORKLOADS
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE,
+                    choices=sorted(WORKLOADS) + sorted(MERGE_WORKLOADS))
     ap.add_argument("--cpu-rows", type=int, default=768)
     ap.add_argument("--ref-rows", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -364,6 +443,8 @@ def main():
     ap.add_argument("--seq-len", type=int, default=0,
                     help="override S (smaller profiling cases of the same shape)")
     args = ap.parse_args()
+    if args.workload in MERGE_WORKLOADS:
+        return run_merge(args, MERGE_WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
     if args.seq_len:
         w = w.scaled(S=args.seq_len, name=f"{w.name}@S={args.seq_len}")
