@@ -77,11 +77,10 @@ attn_simt_kernel(const Geometry g, const float* __restrict__ q,
   int n_vis = 0;
 
   KvIter it;
-  it.init(g);
+  it.init(g, r, q_lo, q_valid);
   KvTile kv;
-  while (it.next(g, r, kv)) {
-    const int work = tile_work(g, q_lo, q_valid, kv);
-    if (work == kSkip) continue;
+  while (it.next(g, kv)) {
+    const int work = kv.work;
     if (log_base && threadIdx.x == 0) log_visit(log_base, n_vis, kv, tile_class(g, q_lo, kv));
     ++n_vis;
 

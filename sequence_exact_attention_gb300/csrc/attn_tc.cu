@@ -212,12 +212,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int bx = 0; bx < C::kBoxes; ++bx)
         tma_load_4d(q_smem + bx * kBoxBytes, &tm_q, bar(C::bQFull), bx * 64, h, q_lo, b);
       KvIter it;
-      it.init(g);
+      it.init(g, r, q_lo, q_valid);
       KvTile kv;
       int j = 0;
       bool ok = true;
-      while (ok && it.next(g, r, kv)) {
-        if (tile_work(g, q_lo, q_valid, kv) == kSkip) continue;
+      while (ok && it.next(g, kv)) {
         const int bb = j % kBuf;
         const uint32_t u = (uint32_t)(j / kBuf);
         const uint32_t k_smem = base + C::kSlotOff + (2 * bb) * C::kTileBytes;
@@ -290,12 +289,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (lane == 0) {
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
       KvIter it;
-      it.init(g);
+      it.init(g, r, q_lo, q_valid);
       KvTile kv;
       bool ok = true;
       int j = 0;
-      while (ok && it.next(g, r, kv)) {
-        if (tile_work(g, q_lo, q_valid, kv) == kSkip) continue;
+      while (ok && it.next(g, kv)) {
         const int bb = j % kBuf;
         const uint32_t u = (uint32_t)(j / kBuf);
         ok = mbar_wait(bar(C::bVFull + bb), u & 1, abort_flag, kTimeoutNs) &&
@@ -333,11 +331,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     int j = 0;               // key tiles done (= P tiles published)
     bool ok = true;
     KvIter it;
-    it.init(g);
+    it.init(g, r, q_lo, q_valid);
     KvTile kv;
-    while (it.next(g, r, kv)) {
-      const int work = tile_work(g, q_lo, q_valid, kv);
-      if (work == kSkip) continue;
+    while (it.next(g, kv)) {
+      const int work = kv.work;
       if (log_base) log_visit(log_base, j, kv, tile_class(g, q_lo, kv));
       const int bb = j % kBuf;
       const uint32_t u = (uint32_t)(j / kBuf);

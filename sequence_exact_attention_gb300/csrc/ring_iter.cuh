@@ -32,52 +32,74 @@ struct KvTile {
   int id;       // global tile id = segment * nt + index in segment
   int lo;       // first token position
   int valid;    // rows in this tile (< tile only at a ragged segment end)
-};
-
-// Walks, for query rank r, the key tiles of steps [t_begin, t_end) in ring
-// order: step by step, the source rank's segments in ascending position,
-// each segment's tiles in order.
-struct KvIter {
-  int t, t_end, which, i;
-
-  __device__ __forceinline__ void init(const Geometry& g) {
-    if (g.step >= 0) { t = g.step; t_end = g.step + 1; }
-    else { t = 0; t_end = g.P; }
-    which = 0;
-    i = 0;
-  }
-
-  __device__ __forceinline__ bool next(const Geometry& g, int r, KvTile& kv) {
-    while (t < t_end) {
-      if (i < g.nt) {
-        const int src = ((r - t) % g.P + g.P) % g.P;
-        const int seg = rank_seg(g, src, which);
-        kv.step = t;
-        kv.src = src;
-        kv.id = seg * g.nt + i;
-        kv.lo = seg * g.seg_len + i * g.tile;
-        kv.valid = min(g.tile, g.seg_len - i * g.tile);
-        ++i;
-        return true;
-      }
-      i = 0;
-      if (++which >= g.segs_per_rank) { which = 0; ++t; }
-    }
-    return false;
-  }
+  int work;     // kNoMask or kMask (SKIP tiles are never returned)
 };
 
 // What a (query tile, key tile) pair needs.
 enum TileWork { kSkip = 0, kNoMask = 1, kMask = 2 };
 
-// q_lo/q_valid: the query tile's first position and valid rows.
-__device__ __forceinline__ int tile_work(const Geometry& g, int q_lo, int q_valid,
-                                         const KvTile& kv) {
-  if (q_valid <= 0) return kSkip;
-  if (g.causal && kv.lo > q_lo + q_valid - 1) return kSkip;   // all keys after all queries
-  const bool all_allowed = !g.causal || (kv.lo + kv.valid - 1 <= q_lo);
-  return (all_allowed && kv.valid == g.tile) ? kNoMask : kMask;
-}
+// Walks, for one query tile of rank r, the key tiles of steps
+// [t_begin, t_end) in ring order: step by step, the source rank's segments in
+// ascending position, each segment's tiles in order. Tiles that the causal
+// rule masks out entirely are left out; since positions grow along a
+// segment, the rest of a segment is dropped at its first such tile.
+// Everything is updated incrementally (no division in the loop): every role
+// of a kernel walks this sequence once per key tile.
+struct KvIter {
+  int t, t_end;    // current step, end step
+  int src;         // source rank of step t
+  int which;       // segment of src being walked (0 or 1)
+  int lo;          // first position of the next tile
+  int id;          // id of the next tile
+  int rem;         // rows of the current segment from `lo` on
+  int q_lo, q_hi;  // the query tile's first and last valid position
+
+  __device__ __forceinline__ void start_segment(const Geometry& g) {
+    const int seg = rank_seg(g, src, which);
+    lo = seg * g.seg_len;
+    id = seg * g.nt;
+    rem = g.seg_len;
+  }
+
+  __device__ __forceinline__ void init(const Geometry& g, int r, int q_first, int q_valid) {
+    if (g.step >= 0) { t = g.step; t_end = g.step + 1; }
+    else { t = 0; t_end = g.P; }
+    src = r - t;
+    if (src < 0) src += g.P;
+    which = 0;
+    q_lo = q_first;
+    q_hi = q_first + q_valid - 1;
+    if (q_valid <= 0) t = t_end;       // nothing to attend to
+    start_segment(g);
+  }
+
+  __device__ __forceinline__ bool next(const Geometry& g, KvTile& kv) {
+    while (t < t_end) {
+      if (rem > 0 && !(g.causal && lo > q_hi)) {
+        const int valid = min(g.tile, rem);
+        kv.step = t;
+        kv.src = src;
+        kv.id = id;
+        kv.lo = lo;
+        kv.valid = valid;
+        const bool all_allowed = !g.causal || (lo + valid - 1 <= q_lo);
+        kv.work = (all_allowed && valid == g.tile) ? kNoMask : kMask;
+        lo += g.tile;
+        rem -= g.tile;
+        ++id;
+        return true;
+      }
+      // next segment of this source rank, or the next ring step
+      if (++which >= g.segs_per_rank) {
+        which = 0;
+        ++t;
+        if (--src < 0) src += g.P;
+      }
+      start_segment(g);
+    }
+    return false;
+  }
+};
 
 // Pair class for the visit log: FULL iff every (valid query, valid key) pair
 // is allowed, PARTIAL otherwise (SKIP tiles are never visited).
