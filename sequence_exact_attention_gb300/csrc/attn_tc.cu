@@ -15,10 +15,11 @@
 // j = 0, 1, ... (tiles wholly after the query tile under a causal mask are
 // left out). "Receiving" a block is a TMA load of its tiles from this GPU's
 // HBM/L2 into shared memory. Warp roles (224 threads):
-//   warps 0-3  softmax: one thread per query row = one TMEM lane
-//   warp  4    TMA producer: Q once, then K_j and V_j into three slot pairs
-//   warp  5    TMEM allocator; one thread issues the S = Q K^T MMAs
-//   warp  6    one thread issues the O += P V MMAs
+//   warps 0-7  softmax: two threads per query row (row = TMEM lane), each
+//              taking 64 of the 128 key columns and half of O's columns
+//   warp  8    TMA producer: Q once, then K_j (3 slots) and V_j (2 slots)
+//   warp  9    TMEM allocator; one thread issues the S = Q K^T MMAs
+//   warp 10    one thread issues the O += P V MMAs
 // Tensor memory (512 columns): three S buffers of 128 f32 columns at 0, 128,
 // 256 (key tile j uses buffer j mod 3; softmax writes P as bf16 over the
 // first 64 columns of that buffer) and the O accumulator at 384.
@@ -28,12 +29,14 @@
 // core always has the next S or PV queued.
 //
 // Synchronisation (b = j mod 3, u = j / 3 is the use count of buffer b):
-//   kfull[b], vfull[b]  TMA of K_j / V_j landed           (phase u)
+//   kfull[b]            TMA of K_j landed                  (phase u)
+//   vfull[j mod 2]      TMA of V_j landed                  (phase j / 2)
 //   sfull[b]            S(j) done (S issuer's commit)      (phase u)
-//   pfull[b]            P(j) written, O rescaled (128 arrivals)
+//   pfull[b]            P(j) written, O rescaled (256 arrivals)
 //   odone[b]            PV(j) done (PV issuer's commit)    (phase u)
 // The producer reuses K_j's slot when sfull[b] completes phase u-1 and V_j's
-// when odone[b] does: the completion barriers double as "slot free". Every
+// (two V slots) once PV(j-2) is done: the completion barriers double as
+// "slot free". Every
 // barrier's next phase depends on the waiter's own progress, so no waiter can
 // fall two phases behind (parity waits are unambiguous).
 //
@@ -62,11 +65,12 @@ namespace {
 using namespace sm100;
 
 constexpr int kTile = 128;
-constexpr int kThreads = 224;
-constexpr int kProducerWarp = 4;
-constexpr int kSIssuerWarp = 5;       // also allocates / frees TMEM
-constexpr int kPVIssuerWarp = 6;
-constexpr int kBuf = 3;               // S/P buffers in TMEM, K/V slot pairs in smem
+constexpr int kThreads = 352;
+constexpr int kProducerWarp = 8;
+constexpr int kSIssuerWarp = 9;       // also allocates / frees TMEM
+constexpr int kPVIssuerWarp = 10;
+constexpr int kBuf = 3;               // S/P buffers in TMEM = K slots in smem
+constexpr int kVBuf = 2;              // V slots in smem
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 384;
 constexpr float kRescaleLog2 = 8.0f;          // lazy rescale threshold (x256)
@@ -78,20 +82,23 @@ struct Cfg {
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kBoxes = D / 64;
   static constexpr int kQOff = 0;
-  static constexpr int kSlotOff = kQOff + kTileBytes;        // K_b at 2b, V_b at 2b+1
-  static constexpr int kBarOff = kSlotOff + 2 * kBuf * kTileBytes;
+  static constexpr int kKOff = kQOff + kTileBytes;           // K_j in slot j mod 3
+  static constexpr int kVOff = kKOff + kBuf * kTileBytes;    // V_j in slot j mod 2
+  static constexpr int kBarOff = kVOff + kVBuf * kTileBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kFlagsOff = kBarBytes;          // 16 x u32: key-tile flags ring
   static constexpr int kFlagsBytes = 64;
-  static constexpr int kUsed = kBarOff + kBarBytes + kFlagsBytes + 1024;   // + alignment slack
+  static constexpr int kRedOff = kBarOff + kBarBytes + kFlagsBytes;   // softmax exchange
+  static constexpr int kRedBytes = 768 * 4;   // maxima [2][2][128], sums [2][128]
+  static constexpr int kUsed = kRedOff + kRedBytes + 1024;   // + alignment slack
   // Request more than half an SM's shared memory so that one CTA owns the SM
   // and its 512 TMEM columns (the D=64 layout alone would fit two).
   static constexpr int kSmemBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
   // barrier indices (8 bytes each)
   static constexpr int bQFull = 0;
   static constexpr int bKFull = 1;                     // [3]
-  static constexpr int bVFull = bKFull + kBuf;         // [3]
-  static constexpr int bSFull = bVFull + kBuf;         // [3]
+  static constexpr int bVFull = bKFull + kBuf;         // [2]
+  static constexpr int bSFull = bVFull + kVBuf;        // [3]
   static constexpr int bPFull = bSFull + kBuf;         // [3], 128 arrivals
   static constexpr int bODone = bPFull + kBuf;         // [3]
   static constexpr int bFinalS = bODone + kBuf;
@@ -106,6 +113,11 @@ struct Cfg {
 };
 
 __device__ __forceinline__ uint32_t s_col(int b) { return (uint32_t)(b * 128); }
+
+// Barrier among `count` threads of the CTA (ids 1-15; 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 // Three-input maximum (sm_100 family).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -182,11 +194,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   // ---- set-up: barriers, abort flag, TMEM
   if (threadIdx.x == 0) {
     mbar_init(bar(C::bQFull), 1);
+    for (int i = 0; i < kVBuf; ++i) mbar_init(bar(C::bVFull + i), 1);
     for (int i = 0; i < kBuf; ++i) {
       mbar_init(bar(C::bKFull + i), 1);
-      mbar_init(bar(C::bVFull + i), 1);
       mbar_init(bar(C::bSFull + i), 1);
-      mbar_init(bar(C::bPFull + i), 128);
+      mbar_init(bar(C::bPFull + i), 256);
       mbar_init(bar(C::bODone + i), 1);
     }
     mbar_init(bar(C::bFinalS), 1);
@@ -219,7 +231,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       while (ok && it.next(g, kv)) {
         const int bb = j % kBuf;
         const uint32_t u = (uint32_t)(j / kBuf);
-        const uint32_t k_smem = base + C::kSlotOff + (2 * bb) * C::kTileBytes;
+        const uint32_t k_smem = base + C::kKOff + bb * C::kTileBytes;
         // K_j reuses the slot of K_{j-3}: free once S(j-3) is done
         if (j >= kBuf && !mbar_wait(bar(C::bSFull + bb), (u - 1) & 1, abort_flag, kTimeoutNs)) {
           ok = false;
@@ -229,24 +241,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         mbar_arrive_expect_tx(bar(C::bKFull + bb), C::kTileBytes);
         for (int bx = 0; bx < C::kBoxes; ++bx)
           tma_load_4d(k_smem + bx * kBoxBytes, &tm_k, bar(C::bKFull + bb), bx * 64, hk, kv.lo, b);
-        // V_j reuses the slot of V_{j-3}: free once PV(j-3) is done
-        if (j >= kBuf && !mbar_wait(bar(C::bODone + bb), (u - 1) & 1, abort_flag, kTimeoutNs)) {
+        // V_j reuses the slot of V_{j-2}: free once PV(j-2) is done
+        // (odone of buffer (j-2) mod 3, phase (j-2) / 3)
+        const int vb = j % kVBuf;
+        if (j >= kVBuf &&
+            !mbar_wait(bar(C::bODone + (j - 2) % kBuf), (uint32_t)((j - 2) / kBuf) & 1,
+                       abort_flag, kTimeoutNs)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar(C::bVFull + bb), C::kTileBytes);
+        mbar_arrive_expect_tx(bar(C::bVFull + vb), C::kTileBytes);
         for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_load_4d(k_smem + C::kTileBytes + bx * kBoxBytes, &tm_v, bar(C::bVFull + bb),
-                      bx * 64, hk, kv.lo, b);
+          tma_load_4d(base + C::kVOff + vb * C::kTileBytes + bx * kBoxBytes, &tm_v,
+                      bar(C::bVFull + vb), bx * 64, hk, kv.lo, b);
         ++j;
       }
       // Every issued load lands before the CTA leaves (already true unless
       // the CTA aborted). This comes before the end marker, which completes
       // one more phase of a K barrier.
-      for (int jj = (j > kBuf ? j - kBuf : 0); jj < j; ++jj) {
+      for (int jj = (j > kBuf ? j - kBuf : 0); jj < j; ++jj)
         mbar_wait(bar(C::bKFull + jj % kBuf), (uint32_t)(jj / kBuf) & 1, never, kTimeoutNs);
-        mbar_wait(bar(C::bVFull + jj % kBuf), (uint32_t)(jj / kBuf) & 1, never, kTimeoutNs);
-      }
+      for (int jj = (j > kVBuf ? j - kVBuf : 0); jj < j; ++jj)
+        mbar_wait(bar(C::bVFull + jj % kVBuf), (uint32_t)(jj / kVBuf) & 1, never, kTimeoutNs);
       mbar_wait(bar(C::bQFull), 0, never, kTimeoutNs);
       // End marker: K barrier of tile j completes with no load, flag kFlagEnd.
       if (ok) {
@@ -270,7 +286,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (j >= kBuf) ok = mbar_wait(bar(C::bODone + bb), (u - 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t k_smem = base + C::kSlotOff + (2 * bb) * C::kTileBytes;
+        const uint32_t k_smem = base + C::kKOff + bb * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
@@ -296,11 +312,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       while (ok && it.next(g, kv)) {
         const int bb = j % kBuf;
         const uint32_t u = (uint32_t)(j / kBuf);
-        ok = mbar_wait(bar(C::bVFull + bb), u & 1, abort_flag, kTimeoutNs) &&
+        const int vb = j % kVBuf;
+        ok = mbar_wait(bar(C::bVFull + vb), (uint32_t)(j / kVBuf) & 1, abort_flag, kTimeoutNs) &&
              mbar_wait(bar(C::bPFull + bb), u & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t v_smem = base + C::kSlotOff + (2 * bb + 1) * C::kTileBytes;
+        const uint32_t v_smem = base + C::kVOff + vb * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           umma_ts(tmem + kOCol, tmem + s_col(bb) + kk * 8,
@@ -314,70 +331,93 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     __syncwarp();
   } else {
-    // ======================= softmax, one thread per row =======================
-    const int row = warp * 32 + lane;
-    const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
-    const uint32_t tO = tmem + t_lane + kOCol;
+    // ================= softmax: two threads per row, 64 columns each =================
+    // Warps w and w+4 share TMEM lane quarter w % 4 (the same 32 rows); warp
+    // w < 4 handles key columns 0-63 and O columns [0, D/2), warp w+4 the
+    // other halves. The partial row maxima meet in shared memory (one named
+    // barrier per warp pair and key tile); each half keeps its own partial sum.
+    const int wq = warp & 3;                 // TMEM lane quarter
+    const int half = warp >> 2;              // column half
+    const int row = wq * 32 + lane;
+    const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
+    const uint32_t tO = tmem + t_lane + kOCol + half * (D / 2);
     const int q_pos = q_lo + row;
     const bool row_valid = row < q_valid;
     const float sl2 = g.scale_log2;
     const uint64_t sl2x2 = pack2(sl2, sl2);
+    const uint32_t pair_bar = 1 + wq;        // named barrier of the warp pair
+    // [2 tile parities][2 halves][128 rows] partial maxima, then partial sums
+    float* red = reinterpret_cast<float*>(base_ptr + C::kRedOff);
 
     int* log_base = (vlog && threadIdx.x == 0)
                         ? vlog + ((size_t)bh * n_qt + qt) * log_stride
                         : nullptr;
 
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;    // l_run: this half's partial sum
     int j = 0;               // key tiles done (= P tiles published)
     bool ok = true;
     KvIter it;
     it.init(g, r, q_lo, q_valid);
     KvTile kv;
+    // Both warps of a pair pass exactly one named barrier per key tile (and
+    // one after the loop), also after an abort: a warp that gave up keeps
+    // walking the tiles and only meets the barriers, so its partner is never
+    // left waiting at a barrier that would not complete.
     while (it.next(g, kv)) {
       const int work = kv.work;
       if (log_base) log_visit(log_base, j, kv, tile_class(g, q_lo, kv));
       const int bb = j % kBuf;
       const uint32_t u = (uint32_t)(j / kBuf);
-      const uint32_t tS = tmem + t_lane + s_col(bb);
-      ok = mbar_wait(bar(C::bSFull + bb), u & 1, abort_flag, kTimeoutNs);
-      if (!ok) break;
+      const uint32_t tS = tmem + t_lane + s_col(bb) + half * 64;
+      if (ok) ok = mbar_wait(bar(C::bSFull + bb), u & 1, abort_flag, kTimeoutNs);
+      if (!ok) {
+        named_bar_sync(pair_bar, 64);
+        ++j;
+        continue;
+      }
       tc_fence_after();
 
-      float s[kTile];
+      float s[64];
       {
-        uint32_t u0[32], u1[32], u2[32], u3[32];
+        uint32_t u0[32], u1[32];
         tmem_ld32(tS + 0, u0);
         tmem_ld32(tS + 32, u1);
-        tmem_ld32(tS + 64, u2);
-        tmem_ld32(tS + 96, u3);
         tmem_ld_wait();
-        reg_fence(u0); reg_fence(u1); reg_fence(u2); reg_fence(u3);
+        reg_fence(u0); reg_fence(u1);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           s[i] = __uint_as_float(u0[i]);
           s[32 + i] = __uint_as_float(u1[i]);
-          s[64 + i] = __uint_as_float(u2[i]);
-          s[96 + i] = __uint_as_float(u3[i]);
         }
       }
       if (work == kMask) {
-        const int lim = g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid;
+        const int lim = (g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid) - half * 64;
 #pragma unroll
-        for (int c = 0; c < kTile; ++c)
+        for (int c = 0; c < 64; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      // row max: 8 independent chains of 3-input maxima, then a tree
+      // partial row max over 64 columns: 8 chains of 3-input maxima
       float m8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) m8[i] = fmax3(s[i], s[8 + i], s[16 + i]);
 #pragma unroll
-      for (int c = 24; c < kTile - 8; c += 16)
+      for (int c = 24; c < 56; c += 16)
 #pragma unroll
         for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[c + i], s[c + 8 + i]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[kTile - 8 + i]);
-      const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
-                             fmaxf(m8[6], m8[7]));
+      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[56 + i]);
+      const float mx_half = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                                  fmaxf(m8[6], m8[7]));
+      // combine with the partner half of the row
+      // (the barrier also orders both halves' S loads before either half
+      // writes P over the S columns)
+      float* red_j = red + (j & 1) * 256;
+      red_j[half * 128 + row] = mx_half;
+      tc_fence_before();
+      named_bar_sync(pair_bar, 64);
+      tc_fence_after();
+      const float mx = fmaxf(mx_half, red_j[(half ^ 1) * 128 + row]);
+
       const float m_new = fmaxf(m_run, mx * sl2);
       const bool resc = m_new > m_run + kRescaleLog2;
       float alpha = 1.f;
@@ -389,39 +429,38 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       const uint64_t neg_m2 = pack2(-m_use, -m_use);
       uint64_t sum2a = pack2(0.f, 0.f), sum2b = sum2a;
+      uint32_t pk[32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          // (s0, s1) * scale*log2(e) - m in one packed FMA, then two exp2
-          const uint64_t x2 = ffma2(pack2(s[half * 64 + 2 * i], s[half * 64 + 2 * i + 1]),
-                                    sl2x2, neg_m2);
-          float x0, x1;
-          unpack2(x2, x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          if (i & 1) sum2b = fadd2(sum2b, pack2(p0, p1));
-          else sum2a = fadd2(sum2a, pack2(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(tS + half * 32, pk);
+      for (int i = 0; i < 32; ++i) {
+        // (s0, s1) * scale*log2(e) - m in one packed FMA, then two exp2
+        const uint64_t x2 = ffma2(pack2(s[2 * i], s[2 * i + 1]), sl2x2, neg_m2);
+        float x0, x1;
+        unpack2(x2, x0, x1);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        if (i & 1) sum2b = fadd2(sum2b, pack2(p0, p1));
+        else sum2a = fadd2(sum2a, pack2(p0, p1));
+        pk[i] = pack_bf16x2(p0, p1);
       }
+      tmem_st32(tmem + t_lane + s_col(bb) + half * 32, pk);   // P columns of this half
       {
         float a0, a1;
         unpack2(fadd2(sum2a, sum2b), a0, a1);
         l_run += a0 + a1;
       }
       // O must be scaled by alpha before P(j) V_j is added to it, i.e. after
-      // PV(j-1) is done
+      // PV(j-1) is done (both halves take the same decision)
       if (__any_sync(0xffffffffu, resc) && j > 0) {
         const int pb = (j - 1) % kBuf;
         ok = mbar_wait(bar(C::bODone + pb), (uint32_t)((j - 1) / kBuf) & 1, abort_flag,
                        kTimeoutNs);
-        if (!ok) break;
+        if (!ok) {
+          ++j;
+          continue;
+        }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t uo[32];
           tmem_ld32(tO + c * 32, uo);
           tmem_ld_wait(uo);
@@ -437,17 +476,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     if (log_base) log_base[0] = j;
 
-    // ---- epilogue: out = O / l, lse = ln2 * (m + log2 l)
+    // ---- epilogue: out = O / l, lse = ln2 * (m + log2 l), l = sum of both halves
+    red[512 + half * 128 + row] = l_run;
+    named_bar_sync(pair_bar, 64);
+    const float l_tot = l_run + red[512 + (half ^ 1) * 128 + row];
     if (ok && j > 0) {
       ok = mbar_wait(bar(C::bODone + (j - 1) % kBuf), (uint32_t)((j - 1) / kBuf) & 1,
                      abort_flag, kTimeoutNs);
       tc_fence_after();
     }
     if (ok) {
-      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-      const size_t row_off = (((size_t)b * g.S + q_pos) * g.H_q + h) * D;
+      const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+      const size_t row_off = (((size_t)b * g.S + q_pos) * g.H_q + h) * D + half * (D / 2);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t uo[32];
         if (j > 0) {
           tmem_ld32(tO + c * 32, uo);
@@ -479,9 +521,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
         }
       }
-      if (row_valid && lse)
+      if (row_valid && lse && half == 0)
         lse[(size_t)bh * g.S + q_pos] =
-            l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+            l_tot > 0.f ? (m_run + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
