@@ -76,7 +76,10 @@ constexpr uint32_t kOCol = 384;
 constexpr float kRescaleLog2 = 8.0f;          // lazy rescale threshold (x256)
 // Of every 8 column pairs of a softmax row half, this many get their
 // exponentials from exp2_poly2 on the FMA pipe, the rest from ex2.approx.
-constexpr int kPolyPairsPer8 = 3;
+// Measured on GB300 (headline workload): 0 -> 1493, 2 -> 1416, 3 -> 1384,
+// 4 -> 1334 TFLOP/s; the softmax is issue-bound, not bound by the special
+// function unit, so every exponential stays on ex2.approx.
+constexpr int kPolyPairsPer8 = 0;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kBoxBytes = kTile * 64 * 2;      // one TMA box: 128 rows x 64 bf16
 
