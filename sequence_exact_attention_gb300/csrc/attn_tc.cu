@@ -396,12 +396,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     bool ok = true;
     KvIter it;
     it.init(g, r, q_lo, q_valid);
-    KvTile kv;
+    KvTile kv, nxt;
     // Both warps of a pair pass exactly one named barrier per key tile (and
     // one after the loop), also after an abort: a warp that gave up keeps
     // walking the tiles and only meets the barriers, so its partner is never
     // left waiting at a barrier that would not complete.
-    while (it.next(g, kv)) {
+    // The next key tile is looked up while this tile's scores load.
+    bool have = it.next(g, kv);
+    while (have) {
       const int work = kv.work;
       if (log_base) log_visit(log_base, j, kv, tile_class(g, q_lo, kv));
       const int bb = j % kBuf;
@@ -411,15 +413,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (!ok) {
         named_bar_sync(pair_bar, 64);
         ++j;
+        have = it.next(g, kv);
         continue;
       }
       tc_fence_after();
 
       float s[64];
+      bool have_next;
       {
         uint32_t u0[32], u1[32];
         tmem_ld32(tS + 0, u0);
         tmem_ld32(tS + 32, u1);
+        have_next = it.next(g, nxt);
         tmem_ld_wait();
         reg_fence(u0); reg_fence(u1);
 #pragma unroll
@@ -499,6 +504,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        kTimeoutNs);
         if (!ok) {
           ++j;
+          kv = nxt;
+          have = have_next;
           continue;
         }
         tc_fence_after();
@@ -516,6 +523,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       tc_fence_before();
       mbar_arrive(bar(C::bPFull + bb));
       ++j;
+      kv = nxt;
+      have = have_next;
     }
     if (log_base) log_base[0] = j;
 
