@@ -184,6 +184,23 @@ ra_status attn_lse_merge_n(const void* const* o, const float* const* lse,
 ra_status ring_attn_plan(int S, int P, int causal, int order,
                          int* table, size_t table_len);
 
+/*
+ * ring_attn_expiry_test - exercises the failure path of the tensor-core
+ * kernel's bounded waits; for tests, never needed in normal use.
+ * Runs the bf16 kernel on B = H_q = H_kv = 1, D = 128, P = 1, non-causal,
+ * 1 <= S <= 4096 (q, k, v, out [1, S, 1, 128] bf16; lse [1, 1, S]) with the
+ * load of the first value tile withheld, so the wait for it expires after
+ * about two seconds. The kernel then gives up in every role, waits (bounded)
+ * for the copies and tensor-core work it issued, frees its tensor memory,
+ * returns, and sets *dev_status (device int, required) to RA_ERR_TIMEOUT.
+ * `out` and `lse` are left partly unwritten. The CUDA context stays usable.
+ * Returns RA_OK when the kernel was launched (the expiry shows in dev_status
+ * after the stream has run it), else an argument or launch error.
+ */
+ra_status ring_attn_expiry_test(const void* q, const void* k, const void* v,
+                                void* out, float* lse, int S, int* dev_status,
+                                void* stream);
+
 /* Human-readable text of a status; never NULL. */
 const char* ring_attn_strerror(int status);
 

@@ -24,7 +24,7 @@ MERGE_MAX_N = 16
 # every entry point declared in include/ring_attn.h
 EXPORTS = ("ring_attn_fwd", "ring_attn_fwd_ex", "ring_attn_visit_log_len",
            "attn_lse_merge", "attn_lse_merge_n", "ring_attn_plan",
-           "ring_attn_strerror", "ring_attn_version")
+           "ring_attn_expiry_test", "ring_attn_strerror", "ring_attn_version")
 
 _lib = None
 
@@ -61,6 +61,8 @@ def load():
     lib.attn_lse_merge_n.argtypes = [vp, vp, c_int, vp, vp] + [c_int] * 5 + [vp]
     lib.ring_attn_plan.restype = c_int
     lib.ring_attn_plan.argtypes = [c_int, c_int, c_int, c_int, ip, ctypes.c_size_t]
+    lib.ring_attn_expiry_test.restype = c_int
+    lib.ring_attn_expiry_test.argtypes = [vp, vp, vp, vp, vp, c_int, vp, vp]
     lib.ring_attn_strerror.restype = ctypes.c_char_p
     lib.ring_attn_strerror.argtypes = [c_int]
     lib.ring_attn_version.restype = c_int
@@ -219,3 +221,12 @@ def attn_lse_merge_n(os_, lses, out=None, lse=None, stream=None):
                               _dtype_code(os_[0].dtype), _stream(stream))
     _check(st, "attn_lse_merge_n")
     return out, lse
+
+
+def expiry_test(q, k, v, out, lse, dev_status, stream=None):
+    """Launch the kernel with one load withheld (see ring_attn_expiry_test)."""
+    lib = load()
+    S = q.shape[1]
+    st = lib.ring_attn_expiry_test(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), S,
+                                   _ptr(dev_status), _stream(stream))
+    _check(st, "ring_attn_expiry_test")

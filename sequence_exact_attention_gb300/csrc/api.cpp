@@ -81,6 +81,24 @@ ra_status ring_attn_fwd(const void* q, const void* k, const void* v,
                           nullptr, stream);
 }
 
+ra_status ring_attn_expiry_test(const void* q, const void* k, const void* v, void* out,
+                                float* lse, int S, int* dev_status, void* stream) {
+  if (!dev_status) return RA_ERR_NULL;
+  ra_status st = check_attn_args(q, k, v, out, lse, 1, 1, 1, S, 128, RA_BF16, -1, nullptr,
+                                 dev_status);
+  if (st != RA_OK) return st;
+  if (S > 4096) return RA_ERR_RANGE;
+  Geometry g;
+  st = make_geometry(1, 1, 1, S, 128, 1, 0, 0.f, RA_ORDER_CONTIGUOUS, -1,
+                     tile_rows_for(RA_BF16, 128), &g);
+  if (st != RA_OK) return st;
+  int sms = 0;
+  st = check_device(&sms);
+  if (st != RA_OK) return st;
+  return launch_attn_tc_withheld(g, q, k, v, out, lse, dev_status, sms,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
 ra_status attn_lse_merge_n(const void* const* o, const float* const* lse,
                            int n, void* out, float* out_lse, int B, int H,
                            int S, int D, int dtype, void* stream) {

@@ -265,6 +265,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       it.init(g, r, q_lo, q_valid);
       KvTile kv;
       int j = 0;
+      int nk = 0, nv = 0;   // key tiles whose K / V slot use has been armed
       bool ok = true;
       while (ok && it.next(g, kv)) {
         const int bb = j % kBuf;
@@ -279,6 +280,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         mbar_arrive_expect_tx(bar(C::bKFull + bb), C::kTileBytes);
         for (int bx = 0; bx < C::kBoxes; ++bx)
           tma_load_4d(k_smem + bx * kBoxBytes, &tm_k, bar(C::bKFull + bb), bx * 64, hk, kv.lo, b);
+        nk = j + 1;
         // V_j reuses the slot of V_{j-2}: free once PV(j-2) is done
         // (odone of buffer (j-2) mod 3, phase (j-2) / 3)
         const int vb = j % kVBuf;
@@ -288,19 +290,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar(C::bVFull + vb), C::kTileBytes);
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_load_4d(base + C::kVOff + vb * C::kTileBytes + bx * kBoxBytes, &tm_v,
-                      bar(C::bVFull + vb), bx * 64, hk, kv.lo, b);
+        if (!(g.withhold_v0 && j == 0)) {      // test of the expiry path only
+          mbar_arrive_expect_tx(bar(C::bVFull + vb), C::kTileBytes);
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_4d(base + C::kVOff + vb * C::kTileBytes + bx * kBoxBytes, &tm_v,
+                        bar(C::bVFull + vb), bx * 64, hk, kv.lo, b);
+        }
+        nv = j + 1;
         ++j;
       }
       // Every issued load lands before the CTA leaves (already true unless
       // the CTA aborted). This comes before the end marker, which completes
       // one more phase of a K barrier.
-      for (int jj = (j > kBuf ? j - kBuf : 0); jj < j; ++jj)
+      for (int jj = (nk > kBuf ? nk - kBuf : 0); jj < nk; ++jj)
         mbar_wait(bar(C::bKFull + jj % kBuf), (uint32_t)(jj / kBuf) & 1, never, kTimeoutNs);
-      for (int jj = (j > kVBuf ? j - kVBuf : 0); jj < j; ++jj)
-        mbar_wait(bar(C::bVFull + jj % kVBuf), (uint32_t)(jj / kVBuf) & 1, never, kTimeoutNs);
+      for (int jj = (nv > kVBuf ? nv - kVBuf : 0); jj < nv; ++jj)
+        if (!(g.withhold_v0 && jj == 0))
+          mbar_wait(bar(C::bVFull + jj % kVBuf), (uint32_t)(jj / kVBuf) & 1, never, kTimeoutNs);
       mbar_wait(bar(C::bQFull), 0, never, kTimeoutNs);
       // End marker: K barrier of tile j completes with no load, flag kFlagEnd.
       if (ok) {
@@ -643,6 +649,14 @@ ra_status launch_typed(const Geometry& g, const CUtensorMap& mq, const CUtensorM
 }
 
 }  // namespace
+
+ra_status launch_attn_tc_withheld(const Geometry& g0, const void* q, const void* k,
+                                  const void* v, void* out, float* lse, int* dev_status,
+                                  int sm_count, cudaStream_t stream) {
+  Geometry g = g0;
+  g.withhold_v0 = 1;
+  return launch_attn_tc(g, q, k, v, out, lse, nullptr, 0, dev_status, sm_count, stream);
+}
 
 ra_status launch_attn_tc(const Geometry& g, const void* q, const void* k, const void* v,
                          void* out, float* lse, int* visit_log, int log_stride,

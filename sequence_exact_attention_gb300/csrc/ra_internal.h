@@ -25,6 +25,7 @@ struct Geometry {
   int nt;          // tiles per segment
   float scale;     // softmax scale
   float scale_log2;  // scale * log2(e)
+  int withhold_v0;   // test only: the producer never loads V of key tile 0
 };
 
 // Host-side planning helpers (plan.cpp).
@@ -41,6 +42,10 @@ ra_status launch_attn_simt(const Geometry& g, const float* q, const float* k,
                            const float* v, void* out, float* lse,
                            int* visit_log, int log_stride, int* dev_status,
                            cudaStream_t stream);
+// Same kernel with the V load of key tile 0 withheld (expiry-path test).
+ra_status launch_attn_tc_withheld(const Geometry& g, const void* q, const void* k,
+                                  const void* v, void* out, float* lse, int* dev_status,
+                                  int sm_count, cudaStream_t stream);
 ra_status launch_attn_tc(const Geometry& g, const void* q, const void* k,
                          const void* v, void* out, float* lse, int* visit_log,
                          int log_stride, int* dev_status, int sm_count,
