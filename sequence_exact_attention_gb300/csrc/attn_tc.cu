@@ -319,7 +319,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ======================= S = Q K^T issuer =======================
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTile, false);
-      const uint32_t q_smem = base + C::kQOff;
+      // Descriptors differ only in the start-address field (bits 0-13, in
+      // 16-byte units, no carry: shared addresses are < 256 KB), so they are
+      // built once and offset per K step and slot.
+      const uint64_t q_desc = sw128_desc(base + C::kQOff, 16, 1024);
+      const uint64_t k_desc = sw128_desc(base + C::kKOff, 16, 1024);
       bool ok = mbar_wait(bar(C::bQFull), 0, abort_flag, kTimeoutNs);
       for (int j = 0; ok; ++j) {
         const int bb = j % kBuf;
@@ -330,12 +334,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (j >= kBuf) ok = mbar_wait(bar(C::bODone + bb), (u - 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t k_smem = base + C::kKOff + bb * C::kTileBytes;
+        const uint64_t kb_desc = k_desc + (uint64_t)((bb * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
-          umma_ss(tmem + s_col(bb), sw128_desc(q_smem + off, 16, 1024),
-                  sw128_desc(k_smem + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t off16 = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
+          umma_ss(tmem + s_col(bb), q_desc + off16, kb_desc + off16, idesc_s,
+                  kk > 0 ? 1u : 0u);
         }
         umma_commit(bar(C::bSFull + bb));
       }
@@ -348,6 +352,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ======================= O += P V issuer =======================
     if (lane == 0) {
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
+      const uint64_t v_desc = sw128_desc(base + C::kVOff, kBoxBytes, 1024);
       KvIter it;
       it.init(g, r, q_lo, q_valid);
       KvTile kv;
@@ -361,11 +366,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
              mbar_wait(bar(C::bPFull + bb), u & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t v_smem = base + C::kVOff + vb * C::kTileBytes;
+        const uint64_t vb_desc = v_desc + (uint64_t)((vb * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ts(tmem + kOCol, tmem + s_col(bb) + kk * 8,
-                  sw128_desc(v_smem + kk * 2048, kBoxBytes, 1024), idesc_o,
+          umma_ts(tmem + kOCol, tmem + s_col(bb) + kk * 8, vb_desc + (kk * 2048 >> 4), idesc_o,
                   (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar(C::bODone + bb));
         ++j;

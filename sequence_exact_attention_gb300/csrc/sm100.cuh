@@ -37,14 +37,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// Suspends the thread until the phase completes or about `hint_ns` passed
+// (a hint: the thread sleeps instead of spinning and issuing instructions).
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity,
+                                              uint32_t hint_ns = 1000000u) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -69,15 +72,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int* abort, uint64_t limit_ns) {
   if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  uint32_t spins = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 15u) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > limit_ns) {
-        *abort = 1;
-        return false;
-      }
+    // each try sleeps up to 20 us, so an abort is seen within that
+    if (mbar_try_wait(bar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      return false;
     }
   }
 }
