@@ -37,17 +37,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-// Suspends the thread until the phase completes or about `hint_ns` passed
-// (a hint: the thread sleeps instead of spinning and issuing instructions).
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity,
-                                              uint32_t hint_ns = 1000000u) {
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -72,13 +69,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int* abort, uint64_t limit_ns) {
   if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
+  uint32_t spins = 0;
   while (true) {
-    // each try sleeps up to 20 us, so an abort is seen within that
-    if (mbar_try_wait(bar, parity, 20000u)) return true;
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > limit_ns) {
-      *abort = 1;
-      return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++spins & 15u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        *abort = 1;
+        return false;
+      }
     }
   }
 }
