@@ -18,6 +18,10 @@ Everything here is float64 NumPy, written to be read against the pages:
   attention over one chunk, folded with the log-sum-exp merge.
 * ``lse_merge`` / ``lse_merge_n`` - the exact merge of partial softmax results
   (same glossary, §Implementation Considerations, "Numerical Stability").
+* ``attention_backward`` - dq, dk, dv from the chain rule through the
+  forward definition (same glossary, §Implementation Considerations: the
+  backward pass runs over the same ring); ``ring_attention_backward``
+  restates it per (rank, step); ``backward_rows`` evaluates sampled rows.
 * ``tile_visits``       - expands the chunk-level schedule into the sequence of
   fixed-size key tiles a tiled kernel must visit, classifying every tile by
   brute force over its (query, key) pairs.
@@ -35,6 +39,7 @@ from .schedule import (
     rank_segments, ring_schedule, schedule_table, tile_visits,
 )
 from .ring import ring_attention
+from .backward import attention_backward, ring_attention_backward, backward_rows
 
 __all__ = [
     "attention_naive", "attention_rows", "partial_attention",
@@ -42,4 +47,5 @@ __all__ = [
     "SKIP", "FULL", "PARTIAL", "ORDER_CONTIGUOUS", "ORDER_ZIGZAG",
     "rank_segments", "ring_schedule", "schedule_table", "tile_visits",
     "ring_attention",
+    "attention_backward", "ring_attention_backward", "backward_rows",
 ]
