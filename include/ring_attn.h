@@ -143,6 +143,57 @@ ra_status ring_attn_visit_log_len(int B, int H_q, int S, int D, int P,
                                   long long* len);
 
 /*
+ * ring_attn_bwd_workspace - bytes of device workspace ring_attn_bwd needs
+ * for this shape (written to *bytes). Host only; never touches the GPU.
+ * The workspace holds two float32 statistics per query row of the forward
+ * result (its lse in base 2 and delta_i = <dout_i, out_i>), stored per
+ * (b, h, query tile) with every tile padded to the kernels' tile height.
+ * Errors: RA_ERR_NULL (bytes NULL), RA_ERR_SHAPE, RA_ERR_HEADDIM,
+ * RA_ERR_DTYPE (order), RA_ERR_RANGE.
+ */
+ra_status ring_attn_bwd_workspace(int B, int H_q, int S, int D, int P,
+                                  int order, size_t* bytes);
+
+/*
+ * ring_attn_bwd - gradients of ring attention with respect to q, k and v,
+ * bfloat16 (glossary "sequence parallelism transformers", §Implementation
+ * Considerations: the backward pass runs over the same ring as the forward).
+ *
+ * For an upstream gradient dout = dL/d(out), with p_ij = exp(s_ij - lse_i)
+ * on the allowed pairs of the forward definition above:
+ *     dV_j = sum_i p_ij dout_i
+ *     ds_ij = p_ij (<dout_i, v_j> - delta_i),   delta_i = <dout_i, out_i>
+ *     dQ_i = scale * sum_j ds_ij k_j,   dK_j = scale * sum_i ds_ij q_i
+ * A key/value head's dk and dv sum over the query heads of its group.
+ * Ring structure: the dq of a query tile is accumulated on chip over the key
+ * tiles in the forward's ring order; the dk, dv of a key tile over the query
+ * tiles of ranks src, src+1, ..., src+P-1 (mod P) in step order, which is
+ * the order in which the block, travelling the ring, meets them on its way
+ * back to its owner. All P steps run; there is no single-step mode.
+ *
+ * q [B,S,H_q,D], k and v [B,S,H_kv,D], out and dout [B,S,H_q,D]: bfloat16
+ *   device tensors; out and lse are the forward's results for the same
+ *   arguments (lse float32 [B,H_q,S], natural log, as ring_attn_fwd_ex
+ *   writes it).
+ * dq [B,S,H_q,D], dk and dv [B,S,H_kv,D]: bfloat16, overwritten (not
+ *   accumulated into). They must not overlap any input.
+ * dtype RA_BF16 only (RA_ERR_DTYPE otherwise); order as in ring_attn_fwd_ex.
+ * workspace / workspace_bytes: a device buffer of at least
+ *   ring_attn_bwd_workspace(...) bytes (else RA_ERR_BUFFER), 16-byte aligned,
+ *   owned by the caller; its contents on entry are ignored and on return
+ *   undefined. The call allocates no memory of its own.
+ * dev_status as in ring_attn_fwd_ex.
+ * Errors: as ring_attn_fwd_ex, plus RA_ERR_BUFFER.
+ */
+ra_status ring_attn_bwd(const void* q, const void* k, const void* v,
+                        const void* out, const float* lse, const void* dout,
+                        void* dq, void* dk, void* dv,
+                        int B, int H_q, int H_kv, int S, int D, int P,
+                        int causal, float scale, int dtype, int order,
+                        void* workspace, size_t workspace_bytes,
+                        int* dev_status, void* stream);
+
+/*
  * attn_lse_merge - exact merge of two partial attention results over
  * disjoint key sets (glossary "sequence parallelism transformers",
  * §Ring Attention and §Implementation Considerations):

@@ -23,6 +23,7 @@ MERGE_MAX_N = 16
 
 # every entry point declared in include/ring_attn.h
 EXPORTS = ("ring_attn_fwd", "ring_attn_fwd_ex", "ring_attn_visit_log_len",
+           "ring_attn_bwd_workspace", "ring_attn_bwd",
            "attn_lse_merge", "attn_lse_merge_n", "ring_attn_plan",
            "ring_attn_expiry_test", "ring_attn_strerror", "ring_attn_version")
 
@@ -55,6 +56,11 @@ def load():
     lib.ring_attn_visit_log_len.restype = c_int
     lib.ring_attn_visit_log_len.argtypes = [c_int] * 7 + [ip, ip, ip, ip,
                                                           ctypes.POINTER(ctypes.c_longlong)]
+    lib.ring_attn_bwd_workspace.restype = c_int
+    lib.ring_attn_bwd_workspace.argtypes = [c_int] * 6 + [ctypes.POINTER(ctypes.c_size_t)]
+    lib.ring_attn_bwd.restype = c_int
+    lib.ring_attn_bwd.argtypes = ([vp] * 9 + [c_int] * 7 + [c_float, c_int, c_int, vp,
+                                                             ctypes.c_size_t, vp, vp])
     lib.attn_lse_merge.restype = c_int
     lib.attn_lse_merge.argtypes = [vp] * 6 + [c_int] * 5 + [vp]
     lib.attn_lse_merge_n.restype = c_int
@@ -183,6 +189,58 @@ def ring_attn_fwd_plain(q, k, v, out, lse, P, causal, scale=None, stream=None):
                            _stream(stream))
     _check(st, "ring_attn_fwd")
     return out, lse
+
+
+def bwd_workspace_bytes(B, H_q, S, D, P, order="contiguous"):
+    """Bytes of device workspace ``ring_attn_bwd`` needs for this shape."""
+    lib = load()
+    n = ctypes.c_size_t()
+    _check(lib.ring_attn_bwd_workspace(B, H_q, S, D, P, ORDERS[order], ctypes.byref(n)),
+           "ring_attn_bwd_workspace")
+    return n.value
+
+
+def ring_attn_bwd(q, k, v, out, lse, dout, P, causal, scale=None, order="contiguous",
+                  dq=None, dk=None, dv=None, workspace=None, dev_status=None, stream=None):
+    """Gradients (dq, dk, dv) of ring attention for the upstream gradient dout.
+
+    ``out`` and ``lse`` are the forward's results for the same arguments. All
+    tensors are bf16 CUDA tensors (lse float32 [B, H_q, S]). ``workspace``
+    (a uint8 CUDA tensor of at least ``bwd_workspace_bytes`` bytes) is
+    allocated here when not given; the library itself allocates nothing.
+    """
+    import torch
+    lib = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (lse, "lse"), (dout, "dout")):
+        _dev(t, n)
+    B, S, H_q, D = q.shape
+    H_kv = k.shape[2]
+    if k.shape != (B, S, H_kv, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, S, H_kv, D] matching q")
+    if out.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("out and dout must be shaped like q")
+    code = _dtype_code(q.dtype)
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    need = bwd_workspace_bytes(B, H_q, S, D, P, order)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv"), (workspace, "workspace"),
+                 (dev_status, "dev_status")):
+        if t is not None:
+            _dev(t, n)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    st = lib.ring_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                           _ptr(dq), _ptr(dk), _ptr(dv), B, H_q, H_kv, S, D, P,
+                           int(bool(causal)), sc, code, ORDERS[order], _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                           _stream(stream))
+    _check(st, "ring_attn_bwd")
+    return dq, dk, dv
 
 
 def attn_lse_merge(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):

@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT, "libringattn.so")
 
-SOURCES = ["plan.cpp", "api.cpp", "merge.cu", "attn_simt.cu", "attn_tc.cu"]
+SOURCES = ["plan.cpp", "api.cpp", "tensor_map.cpp", "merge.cu", "attn_simt.cu", "attn_tc.cu",
+           "attn_bwd.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -99,6 +99,49 @@ ra_status ring_attn_expiry_test(const void* q, const void* k, const void* v, voi
                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
+ra_status ring_attn_bwd_workspace(int B, int H_q, int S, int D, int P, int order,
+                                  size_t* bytes) {
+  if (!bytes) return RA_ERR_NULL;
+  if (D != 64 && D != 128) return RA_ERR_HEADDIM;
+  Geometry g;
+  ra_status st = make_geometry(B, H_q, 1, S, D, P, 0, 0.f, order, -1,
+                               tile_rows_for(RA_BF16, D), &g);
+  if (st != RA_OK) return st;
+  const long long n = bwd_workspace_floats(g);
+  if (n / 2 > kMaxElems) return RA_ERR_RANGE;
+  *bytes = (size_t)n * sizeof(float);
+  return RA_OK;
+}
+
+ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                        int B, int H_q, int H_kv, int S, int D, int P, int causal,
+                        float scale, int dtype, int order, void* workspace,
+                        size_t workspace_bytes, int* dev_status, void* stream) {
+  if (!lse || !dout || !dq || !dk || !dv || !workspace) return RA_ERR_NULL;
+  ra_status st = check_attn_args(q, k, v, out, lse, B, H_q, H_kv, S, D, dtype, -1,
+                                 nullptr, dev_status);
+  if (st != RA_OK) return st;
+  if (dtype != RA_BF16) return RA_ERR_DTYPE;
+  if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(workspace, 16))
+    return RA_ERR_ALIGN;
+  Geometry g;
+  st = make_geometry(B, H_q, H_kv, S, D, P, causal, scale, order, -1,
+                     tile_rows_for(dtype, D), &g);
+  if (st != RA_OK) return st;
+  size_t need = 0;
+  st = ring_attn_bwd_workspace(B, H_q, S, D, P, order, &need);
+  if (st != RA_OK) return st;
+  if (workspace_bytes < need) return RA_ERR_BUFFER;
+  int sms = 0;
+  st = check_device(&sms);
+  if (st != RA_OK) return st;
+  return launch_attn_bwd(g, q, k, v, out, lse, dout, dq, dk, dv,
+                         static_cast<float*>(workspace), dev_status,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
 ra_status attn_lse_merge_n(const void* const* o, const float* const* lse,
                            int n, void* out, float* out_lse, int B, int H,
                            int S, int D, int dtype, void* stream) {

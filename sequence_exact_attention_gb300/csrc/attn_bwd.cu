@@ -1,0 +1,714 @@
+// Backward pass of exact ring attention on the tensor cores: bf16 in and
+// out, float32 accumulation in tensor memory.
+//
+// Glossary "sequence parallelism transformers", §Implementation
+// Considerations: the backward pass runs over the same ring as the forward.
+// For an upstream gradient dO and the forward's lse, with
+// p_ij = exp(s_ij - lse_i) on the allowed pairs:
+//   dV_j = sum_i p_ij dO_i            ds_ij = p_ij (<dO_i, v_j> - delta_i)
+//   dQ_i = scale sum_j ds_ij k_j      dK_j = scale sum_i ds_ij q_i
+//   delta_i = <dO_i, o_i>
+// Three launches on the caller's stream:
+//  1. bwd_prep_kernel: per query row, lse in base 2 and delta, into the
+//     caller's workspace, tile-padded (padding rows get lse = +inf, which
+//     makes their p exactly 0, and delta = 0).
+//  2. bwd_dkdv_kernel: one CTA per key tile of one kv head. It walks the
+//     query tiles that see the tile in ring order -- the owner rank's own
+//     queries first (step 0), then ranks src+1, src+2, ... (the block's trip
+//     around the ring back to its owner) -- over every query head of the
+//     group. Per visit:
+//       S^T = K Q^T, dP^T = V dO^T      tensor cores, float32 in TMEM
+//       P^T, dS^T in bf16               CUDA cores, one thread per key row
+//       dV += P^T dO, dK += dS^T Q      tensor cores, A operand from TMEM
+//  3. bwd_dq_kernel: one CTA per query tile, walking the key tiles in the
+//     forward's ring order: S = Q K^T, dP = dO V^T, dS, dQ += dS K.
+// The two gradient kernels both recompute S and dP; in exchange neither needs
+// atomics, and each gradient is accumulated on chip and written once.
+//
+// Roles (192 threads): warps 0-3 compute (TMEM lane quarter = warp), warp 4
+// TMA producer, warp 5 tensor-core issuer and TMEM owner. Every wait is
+// bounded (two seconds, then the CTA gives up, drains what it issued, frees
+// its TMEM and reports RA_ERR_TIMEOUT in the status word).
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "ra_internal.h"
+#include "ring_iter.cuh"
+#include "sm100.cuh"
+
+namespace ra {
+namespace {
+
+using namespace sm100;
+
+constexpr int kT = 128;                         // tile rows (queries or keys)
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;                   // S or S^T, then P / dS in bf16
+constexpr uint32_t kColDP = 128;                // dP or dP^T, then dS^T in bf16
+constexpr uint32_t kColAcc = 256;               // accumulators: dV | dK, or dQ
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr int kBoxBytes = kT * 64 * 2;          // one TMA box: 128 rows x 64 bf16
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct Cfg {
+  static constexpr int kTileBytes = kT * D * 2;
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kFixA = 0;                          // K (dk/dv) or Q (dq)
+  static constexpr int kFixB = kTileBytes;                 // V (dk/dv) or dO (dq)
+  static constexpr int kStage0 = 2 * kTileBytes;
+  static constexpr int kStatBytes = 2 * kT * 4;            // lse2 and delta of a query tile
+  static constexpr int kStageBytes = 2 * kTileBytes + kStatBytes;
+  static constexpr int kBarOff = kStage0 + 2 * kStageBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kUsed = kBarOff + kBarBytes + 1024;  // + alignment slack
+  // More than half an SM's shared memory: one CTA per SM, so the 512-column
+  // TMEM allocation never waits for another CTA.
+  static constexpr int kSmemBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
+  static constexpr int bFix = 0;
+  static constexpr int bFull = 1;     // [2] stage loaded
+  static constexpr int bFree = 3;     // [2] stage no longer read by the tensor cores
+  static constexpr int bSdp = 5;      // S and dP ready in TMEM
+  static constexpr int bP = 6;        // 128 arrivals: P / dS written to TMEM
+  static constexpr int bAcc = 7;      // accumulating MMAs of a visit done
+  static constexpr int bFinal = 8;
+  static constexpr int kHolderOff = kBarBytes - 16;
+  static constexpr int kNeverOff = kBarBytes - 12;
+  static constexpr int kAbortOff = kBarBytes - 8;
+  static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+// Offset (in floats) of the first row of query tile `ti` of segment `seg`,
+// batch-head `bh`, in each half of the workspace.
+__host__ __device__ __forceinline__ long long ws_tile(const Geometry& g, int bh, int seg,
+                                                      int ti) {
+  return (((long long)bh * g.n_seg + seg) * g.nt + ti) * kT;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// ------------------------------------------------------------------ prep
+// 8 threads per padded query row; each reads D/8 elements of out and dout.
+template <int D>
+__global__ void __launch_bounds__(256)
+bwd_prep_kernel(const Geometry g, const __nv_bfloat16* __restrict__ out,
+                const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
+                float* __restrict__ lse2, float* __restrict__ delta, long long rows) {
+  const long long gid = (long long)blockIdx.x * 32 + (threadIdx.x >> 3);
+  const int sub = threadIdx.x & 7;
+  if (gid >= rows) return;               // rows is a multiple of 32: whole blocks
+  const int row = (int)(gid % kT);
+  long long rest = gid / kT;
+  const int ti = (int)(rest % g.nt);
+  rest /= g.nt;
+  const int seg = (int)(rest % g.n_seg);
+  const int bh = (int)(rest / g.n_seg);
+  const int b = bh / g.H_q, h = bh % g.H_q;
+  const int in_seg = ti * kT + row;
+  const bool valid = in_seg < g.seg_len;
+  const int pos = seg * g.seg_len + in_seg;
+  float acc = 0.f;
+  if (valid) {
+    constexpr int E = D / 8;
+    const size_t off = (((size_t)b * g.S + pos) * g.H_q + h) * D + (size_t)sub * E;
+    const uint4* po = reinterpret_cast<const uint4*>(out + off);
+    const uint4* pd = reinterpret_cast<const uint4*>(dout + off);
+#pragma unroll
+    for (int v = 0; v < E / 8; ++v) {
+      const uint4 a = po[v], d = pd[v];
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, dw[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        acc = fmaf(bf_lo(aw[w]), bf_lo(dw[w]), acc);
+        acc = fmaf(bf_hi(aw[w]), bf_hi(dw[w]), acc);
+      }
+    }
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  if (sub == 0) {
+    lse2[gid] = valid ? lse[(size_t)bh * g.S + pos] * kLog2e : INFINITY;
+    delta[gid] = valid ? acc : 0.f;
+  }
+}
+
+// ------------------------------------------------------------------ query walk
+// The query tiles that see key rows [kv_lo, kv_hi], in ring order: query
+// heads [h, h_end) of the group, then ring steps t = 0..P-1 (rank src + t),
+// the rank's segments in position order, tiles in order. Under the causal
+// rule a tile whose last query precedes the first key sees nothing; since
+// positions grow along a segment, such tiles form a prefix of it.
+struct QTile {
+  int h, seg, ti, lo, valid;
+  bool mask;    // some (query, key) pair of the tile is masked
+};
+
+struct QIter {
+  int h, h_end, t, r, which, ti, src, kv_lo, kv_hi;
+
+  __device__ __forceinline__ void start_segment(const Geometry& g) {
+    const int s0 = rank_seg(g, r, which) * g.seg_len;
+    if (!g.causal || kv_lo <= s0) ti = 0;
+    else if (s0 + g.seg_len - 1 < kv_lo) ti = g.nt;
+    else ti = (kv_lo - s0) / kT;
+  }
+  __device__ __forceinline__ void init(const Geometry& g, int src_, int kv_lo_, int kv_valid,
+                                       int h_begin, int h_end_) {
+    h = h_begin; h_end = h_end_;
+    src = src_; t = 0; r = src_; which = 0;
+    kv_lo = kv_lo_; kv_hi = kv_lo_ + kv_valid - 1;
+    start_segment(g);
+  }
+  __device__ __forceinline__ bool next(const Geometry& g, QTile& o) {
+    while (h < h_end) {
+      if (ti < g.nt) {
+        const int seg = rank_seg(g, r, which);
+        o.h = h;
+        o.seg = seg;
+        o.ti = ti;
+        o.lo = seg * g.seg_len + ti * kT;
+        o.valid = min(kT, g.seg_len - ti * kT);
+        o.mask = g.causal && kv_hi > o.lo;
+        ++ti;
+        return true;
+      }
+      if (++which >= g.segs_per_rank) {
+        which = 0;
+        if (++t >= g.P) { t = 0; ++h; }
+        r = src + t;
+        if (r >= g.P) r -= g.P;
+      }
+      if (h < h_end) start_segment(g);
+    }
+    return false;
+  }
+};
+
+// K-major SW128 descriptor offset of K step kk (16 elements) in a tile made
+// of 64-column boxes.
+__device__ __forceinline__ uint64_t kstep_off(int kk) {
+  return (uint64_t)(((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4);
+}
+
+// Stores 32 float32 values of one row, times `mul`, as bf16 (64 bytes).
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&u)[32],
+                                            float mul) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    w[i] = pack_bf16x2(__uint_as_float(u[2 * i]) * mul, __uint_as_float(u[2 * i + 1]) * mul);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+// ------------------------------------------------------------------ dK, dV
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v,
+                const __grid_constant__ CUtensorMap tm_do, const Geometry g,
+                const float* __restrict__ lse2, const float* __restrict__ delta,
+                __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                int* __restrict__ status) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  auto bar = [&](int i) -> uint32_t { return base + C::kBarOff + 8u * (uint32_t)i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kBarOff + C::kAbortOff);
+  volatile int* never = reinterpret_cast<volatile int*>(base_ptr + C::kBarOff + C::kNeverOff);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + C::kBarOff + C::kHolderOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // work item: key tile kt of kv head hk; (batch, kv head) outermost so that
+  // the CTAs resident together read the queries of one group from L2; key
+  // tiles in position order (most causal work first).
+  const int grp = g.H_q / g.H_kv;
+  const int n_kt = g.n_seg * g.nt;
+  const int kt = (int)(blockIdx.x % n_kt);
+  const int bhk = (int)(blockIdx.x / n_kt);
+  const int b = bhk / g.H_kv, hk = bhk % g.H_kv;
+  const int kseg = kt / g.nt, kti = kt % g.nt;
+  const int src = seg_owner(g, kseg);
+  const int kv_lo = kseg * g.seg_len + kti * kT;
+  const int kv_valid = min(kT, g.seg_len - kti * kT);
+  const int h0 = hk * grp;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::bFix), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(C::bFull + i), 1);
+      mbar_init(bar(C::bFree + i), 1);
+    }
+    mbar_init(bar(C::bSdp), 1);
+    mbar_init(bar(C::bP), 128);
+    mbar_init(bar(C::bAcc), 1);
+    mbar_init(bar(C::bFinal), 1);
+    *abort_flag = 0;
+    *never = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(C::bFix), 2 * C::kTileBytes);
+      for (int bx = 0; bx < C::kBoxes; ++bx) {
+        tma_load_4d(base + C::kFixA + bx * kBoxBytes, &tm_k, bar(C::bFix), bx * 64, hk, kv_lo, b);
+        tma_load_4d(base + C::kFixB + bx * kBoxBytes, &tm_v, bar(C::bFix), bx * 64, hk, kv_lo, b);
+      }
+      QIter it;
+      it.init(g, src, kv_lo, kv_valid, h0, h0 + grp);
+      QTile qt;
+      int j = 0;
+      while (it.next(g, qt)) {
+        const int st = j & 1;
+        if (j >= 2 &&
+            !mbar_wait(bar(C::bFree + st), (uint32_t)((j >> 1) - 1) & 1, abort_flag, kTimeoutNs))
+          break;
+        const uint32_t sb = base + C::kStage0 + st * C::kStageBytes;
+        mbar_arrive_expect_tx(bar(C::bFull + st), 2 * C::kTileBytes + C::kStatBytes);
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+          tma_load_4d(sb + bx * kBoxBytes, &tm_q, bar(C::bFull + st), bx * 64, qt.h, qt.lo, b);
+          tma_load_4d(sb + C::kTileBytes + bx * kBoxBytes, &tm_do, bar(C::bFull + st), bx * 64,
+                      qt.h, qt.lo, b);
+        }
+        const long long wi = ws_tile(g, b * g.H_q + qt.h, qt.seg, qt.ti);
+        bulk_load(sb + 2 * C::kTileBytes, lse2 + wi, kT * 4, bar(C::bFull + st));
+        bulk_load(sb + 2 * C::kTileBytes + kT * 4, delta + wi, kT * 4, bar(C::bFull + st));
+        ++j;
+      }
+      // every issued copy lands before the CTA leaves
+      for (int jj = (j > 2 ? j - 2 : 0); jj < j; ++jj)
+        mbar_wait(bar(C::bFull + (jj & 1)), (uint32_t)(jj >> 1) & 1, never, kTimeoutNs);
+      mbar_wait(bar(C::bFix), 0, never, kTimeoutNs);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, kT, false);
+      constexpr uint32_t id_acc = idesc_bf16_f32(128, D, true);
+      const uint64_t k_kmaj = sw128_desc(base + C::kFixA, 16, 1024);
+      const uint64_t v_kmaj = sw128_desc(base + C::kFixB, 16, 1024);
+      const uint64_t q_kmaj = sw128_desc(base + C::kStage0, 16, 1024);
+      const uint64_t do_kmaj = sw128_desc(base + C::kStage0 + C::kTileBytes, 16, 1024);
+      const uint64_t q_mn = sw128_desc(base + C::kStage0, kBoxBytes, 1024);
+      const uint64_t do_mn = sw128_desc(base + C::kStage0 + C::kTileBytes, kBoxBytes, 1024);
+      bool ok = mbar_wait(bar(C::bFix), 0, abort_flag, kTimeoutNs);
+      QIter it;
+      it.init(g, src, kv_lo, kv_valid, h0, h0 + grp);
+      QTile qt;
+      int j = 0;
+      while (ok && it.next(g, qt)) {
+        const int st = j & 1;
+        const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
+        ok = mbar_wait(bar(C::bFull + st), (uint32_t)(j >> 1) & 1, abort_flag, kTimeoutNs);
+        // S^T and dP^T overwrite the P^T, dS^T that the previous visit's
+        // accumulating MMAs read
+        if (ok && j > 0) ok = mbar_wait(bar(C::bAcc), (uint32_t)(j - 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + kColS, k_kmaj + kstep_off(kk), q_kmaj + so + kstep_off(kk), id_s,
+                  kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + kColDP, v_kmaj + kstep_off(kk), do_kmaj + so + kstep_off(kk), id_s,
+                  kk > 0 ? 1u : 0u);
+        umma_commit(bar(C::bSdp));
+        ok = mbar_wait(bar(C::bP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          umma_ts(tmem + kColAcc, tmem + kColS + kk * 8, do_mn + so + (uint64_t)(kk * 2048 >> 4),
+                  id_acc, (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          umma_ts(tmem + kColAcc + D, tmem + kColDP + kk * 8, q_mn + so + (uint64_t)(kk * 2048 >> 4),
+                  id_acc, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(C::bAcc));
+        umma_commit(bar(C::bFree + st));
+        ++j;
+      }
+      umma_commit(bar(C::bFinal));
+      mbar_wait(bar(C::bFinal), 0, never, kTimeoutNs);
+    }
+    __syncwarp();
+  } else {
+    // ============ compute: thread = key row (TMEM lane), 128 query columns
+    const int row = warp * 32 + lane;
+    const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
+    const int kpos = kv_lo + row;
+    const float sl2 = g.scale_log2;
+    QIter it;
+    it.init(g, src, kv_lo, kv_valid, h0, h0 + grp);
+    QTile qt;
+    int j = 0;
+    bool ok = true;
+    while (it.next(g, qt)) {
+      const int st = j & 1;
+      if (ok) ok = mbar_wait(bar(C::bSdp), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+      if (!ok) { ++j; continue; }
+      tc_fence_after();
+      const float* stat =
+          reinterpret_cast<const float*>(base_ptr + C::kStage0 + st * C::kStageBytes + 2 * C::kTileBytes);
+      const float2* l2v = reinterpret_cast<const float2*>(stat);
+      const float2* dlv = reinterpret_cast<const float2*>(stat + kT);
+      const int lim = qt.mask ? kpos - qt.lo : -1;      // query column c is masked iff c < lim
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pp[32], pd[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int col = half * 64 + c * 32;
+          uint32_t us[32], ud[32];
+          tmem_ld32(tmem + t_lane + kColS + col, us);
+          tmem_ld32(tmem + t_lane + kColDP + col, ud);
+          tmem_ld_wait();
+          reg_fence(us);
+          reg_fence(ud);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float2 l2 = l2v[(col + i) >> 1];
+            const float2 dl = dlv[(col + i) >> 1];
+            float p0 = ex2_approx(fmaf(__uint_as_float(us[i]), sl2, -l2.x));
+            float p1 = ex2_approx(fmaf(__uint_as_float(us[i + 1]), sl2, -l2.y));
+            if (col + i < lim) p0 = 0.f;
+            if (col + i + 1 < lim) p1 = 0.f;
+            const float d0 = p0 * (__uint_as_float(ud[i]) - dl.x);
+            const float d1 = p1 * (__uint_as_float(ud[i + 1]) - dl.y);
+            pp[c * 16 + i / 2] = pack_bf16x2(p0, p1);
+            pd[c * 16 + i / 2] = pack_bf16x2(d0, d1);
+          }
+        }
+        // columns [32 half, 32 half + 32) were read above (loads in order)
+        tmem_st32(tmem + t_lane + kColS + half * 32, pp);
+        tmem_st32(tmem + t_lane + kColDP + half * 32, pd);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::bP));
+      ++j;
+    }
+    // ---- epilogue: dV, and dK times scale, as bf16 rows
+    if (ok && j > 0) ok = mbar_wait(bar(C::bAcc), (uint32_t)(j - 1) & 1, abort_flag, kTimeoutNs);
+    if (ok) {
+      tc_fence_after();
+      const bool row_ok = row < kv_valid;
+      const size_t off = (((size_t)b * g.S + kpos) * g.H_kv + hk) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        __nv_bfloat16* dst = (which ? dk : dv) + off;
+        const float mul = which ? g.scale : 1.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tmem + t_lane + kColAcc + which * D + c * 32, u);
+          tmem_ld_wait(u);
+          if (j == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = 0u;
+          }
+          if (row_ok) store_row32(dst + c * 32, u, mul);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0 && (*abort_flag || *never) && status)
+    atomicExch(status, (int)RA_ERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ dQ
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
+              const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v,
+              const __grid_constant__ CUtensorMap tm_do, const Geometry g,
+              const float* __restrict__ lse2, const float* __restrict__ delta,
+              __nv_bfloat16* __restrict__ dq, int* __restrict__ status) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  auto bar = [&](int i) -> uint32_t { return base + C::kBarOff + 8u * (uint32_t)i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::kBarOff + C::kAbortOff);
+  volatile int* never = reinterpret_cast<volatile int*>(base_ptr + C::kBarOff + C::kNeverOff);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + C::kBarOff + C::kHolderOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // work item: one query tile, ordered as the forward's (kv head outermost,
+  // query tiles by decreasing position, the group's heads innermost)
+  const int grp = g.H_q / g.H_kv;
+  const int n_qt = g.n_seg * g.nt;
+  const int hg = (int)(blockIdx.x % grp);
+  const int rest = (int)(blockIdx.x / grp);
+  const int qt = n_qt - 1 - rest % n_qt;
+  const int bhk = rest / n_qt;
+  const int b = bhk / g.H_kv, hk = bhk % g.H_kv;
+  const int h = hk * grp + hg;
+  const int bh = b * g.H_q + h;
+  const int seg = qt / g.nt;
+  const int ti = qt % g.nt;
+  const int r = seg_owner(g, seg);
+  const int q_lo = seg * g.seg_len + ti * kT;
+  const int q_valid = min(kT, g.seg_len - ti * kT);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::bFix), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(C::bFull + i), 1);
+      mbar_init(bar(C::bFree + i), 1);
+    }
+    mbar_init(bar(C::bSdp), 1);
+    mbar_init(bar(C::bP), 128);
+    mbar_init(bar(C::bAcc), 1);
+    mbar_init(bar(C::bFinal), 1);
+    *abort_flag = 0;
+    *never = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(C::bFix), 2 * C::kTileBytes);
+      for (int bx = 0; bx < C::kBoxes; ++bx) {
+        tma_load_4d(base + C::kFixA + bx * kBoxBytes, &tm_q, bar(C::bFix), bx * 64, h, q_lo, b);
+        tma_load_4d(base + C::kFixB + bx * kBoxBytes, &tm_do, bar(C::bFix), bx * 64, h, q_lo, b);
+      }
+      KvIter it;
+      it.init(g, r, q_lo, q_valid);
+      KvTile kv;
+      int j = 0;
+      while (it.next(g, kv)) {
+        const int st = j & 1;
+        if (j >= 2 &&
+            !mbar_wait(bar(C::bFree + st), (uint32_t)((j >> 1) - 1) & 1, abort_flag, kTimeoutNs))
+          break;
+        const uint32_t sb = base + C::kStage0 + st * C::kStageBytes;
+        mbar_arrive_expect_tx(bar(C::bFull + st), 2 * C::kTileBytes);
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+          tma_load_4d(sb + bx * kBoxBytes, &tm_k, bar(C::bFull + st), bx * 64, hk, kv.lo, b);
+          tma_load_4d(sb + C::kTileBytes + bx * kBoxBytes, &tm_v, bar(C::bFull + st), bx * 64, hk,
+                      kv.lo, b);
+        }
+        ++j;
+      }
+      for (int jj = (j > 2 ? j - 2 : 0); jj < j; ++jj)
+        mbar_wait(bar(C::bFull + (jj & 1)), (uint32_t)(jj >> 1) & 1, never, kTimeoutNs);
+      mbar_wait(bar(C::bFix), 0, never, kTimeoutNs);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, kT, false);
+      constexpr uint32_t id_acc = idesc_bf16_f32(128, D, true);
+      const uint64_t q_kmaj = sw128_desc(base + C::kFixA, 16, 1024);
+      const uint64_t do_kmaj = sw128_desc(base + C::kFixB, 16, 1024);
+      const uint64_t k_kmaj = sw128_desc(base + C::kStage0, 16, 1024);
+      const uint64_t v_kmaj = sw128_desc(base + C::kStage0 + C::kTileBytes, 16, 1024);
+      const uint64_t k_mn = sw128_desc(base + C::kStage0, kBoxBytes, 1024);
+      bool ok = mbar_wait(bar(C::bFix), 0, abort_flag, kTimeoutNs);
+      KvIter it;
+      it.init(g, r, q_lo, q_valid);
+      KvTile kv;
+      int j = 0;
+      while (ok && it.next(g, kv)) {
+        const int st = j & 1;
+        const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
+        ok = mbar_wait(bar(C::bFull + st), (uint32_t)(j >> 1) & 1, abort_flag, kTimeoutNs);
+        // S and dP overwrite the dS that the previous dQ MMA reads
+        if (ok && j > 0) ok = mbar_wait(bar(C::bAcc), (uint32_t)(j - 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + kColS, q_kmaj + kstep_off(kk), k_kmaj + so + kstep_off(kk), id_s,
+                  kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + kColDP, do_kmaj + kstep_off(kk), v_kmaj + so + kstep_off(kk), id_s,
+                  kk > 0 ? 1u : 0u);
+        umma_commit(bar(C::bSdp));
+        ok = mbar_wait(bar(C::bP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          umma_ts(tmem + kColAcc, tmem + kColS + kk * 8, k_mn + so + (uint64_t)(kk * 2048 >> 4),
+                  id_acc, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(C::bAcc));
+        umma_commit(bar(C::bFree + st));
+        ++j;
+      }
+      umma_commit(bar(C::bFinal));
+      mbar_wait(bar(C::bFinal), 0, never, kTimeoutNs);
+    }
+    __syncwarp();
+  } else {
+    // ============ compute: thread = query row (TMEM lane), 128 key columns
+    const int row = warp * 32 + lane;
+    const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
+    const int q_pos = q_lo + row;
+    const float sl2 = g.scale_log2;
+    const long long wi = ws_tile(g, bh, seg, ti) + row;
+    const float l2_row = lse2[wi];      // +inf on padding rows: p = 0
+    const float dl_row = delta[wi];
+    KvIter it;
+    it.init(g, r, q_lo, q_valid);
+    KvTile kv;
+    int j = 0;
+    bool ok = true;
+    while (it.next(g, kv)) {
+      if (ok) ok = mbar_wait(bar(C::bSdp), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+      if (!ok) { ++j; continue; }
+      tc_fence_after();
+      // key column c is allowed iff c < lim
+      const int lim = kv.work == kMask
+                          ? (g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid)
+                          : kT;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pd[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int col = half * 64 + c * 32;
+          uint32_t us[32], ud[32];
+          tmem_ld32(tmem + t_lane + kColS + col, us);
+          tmem_ld32(tmem + t_lane + kColDP + col, ud);
+          tmem_ld_wait();
+          reg_fence(us);
+          reg_fence(ud);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float p0 = ex2_approx(fmaf(__uint_as_float(us[i]), sl2, -l2_row));
+            float p1 = ex2_approx(fmaf(__uint_as_float(us[i + 1]), sl2, -l2_row));
+            if (col + i >= lim) p0 = 0.f;
+            if (col + i + 1 >= lim) p1 = 0.f;
+            pd[c * 16 + i / 2] = pack_bf16x2(p0 * (__uint_as_float(ud[i]) - dl_row),
+                                             p1 * (__uint_as_float(ud[i + 1]) - dl_row));
+          }
+        }
+        // columns [32 half, 32 half + 32) were read above (loads in order)
+        tmem_st32(tmem + t_lane + kColS + half * 32, pd);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::bP));
+      ++j;
+    }
+    if (ok && j > 0) ok = mbar_wait(bar(C::bAcc), (uint32_t)(j - 1) & 1, abort_flag, kTimeoutNs);
+    if (ok) {
+      tc_fence_after();
+      const bool row_ok = row < q_valid;
+      __nv_bfloat16* dst = dq + (((size_t)b * g.S + q_pos) * g.H_q + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem + t_lane + kColAcc + c * 32, u);
+        tmem_ld_wait(u);
+        if (j == 0) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = 0u;
+        }
+        if (row_ok) store_row32(dst + c * 32, u, g.scale);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0 && (*abort_flag || *never) && status)
+    atomicExch(status, (int)RA_ERR_TIMEOUT);
+}
+
+template <int D>
+ra_status launch_d(const Geometry& g, const CUtensorMap& mq, const CUtensorMap& mk,
+                   const CUtensorMap& mv, const CUtensorMap& mdo, const void* out,
+                   const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                   float* ws, int* status, cudaStream_t stream) {
+  using C = Cfg<D>;
+  const long long rows = bwd_workspace_floats(g) / 2;
+  float* lse2 = ws;
+  float* delta = ws + rows;
+  const long long prep_blocks = rows / 32;
+  const long long n_tiles = (long long)g.n_seg * g.nt;
+  const long long grid_kv = n_tiles * g.B * g.H_kv;
+  const long long grid_q = n_tiles * g.B * g.H_q;
+  if (prep_blocks > 0x7fffffffLL || grid_q > 0x7fffffffLL) return RA_ERR_RANGE;
+  bwd_prep_kernel<D><<<(unsigned)prep_blocks, 256, 0, stream>>>(
+      g, static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse,
+      lse2, delta, rows);
+  if (cudaGetLastError() != cudaSuccess) return RA_ERR_LAUNCH;
+  if (cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes) != cudaSuccess)
+    return RA_ERR_LAUNCH;
+  bwd_dkdv_kernel<D><<<(unsigned)grid_kv, kThreads, C::kSmemBytes, stream>>>(
+      mq, mk, mv, mdo, g, lse2, delta, static_cast<__nv_bfloat16*>(dk),
+      static_cast<__nv_bfloat16*>(dv), status);
+  if (cudaGetLastError() != cudaSuccess) return RA_ERR_LAUNCH;
+  bwd_dq_kernel<D><<<(unsigned)grid_q, kThreads, C::kSmemBytes, stream>>>(
+      mq, mk, mv, mdo, g, lse2, delta, static_cast<__nv_bfloat16*>(dq), status);
+  return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+long long bwd_workspace_floats(const Geometry& g) {
+  return 2 * ws_tile(g, g.B * g.H_q, 0, 0);
+}
+
+ra_status launch_attn_bwd(const Geometry& g, const void* q, const void* k, const void* v,
+                          const void* out, const float* lse, const void* dout, void* dq,
+                          void* dk, void* dv, float* workspace, int* dev_status,
+                          cudaStream_t stream) {
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_bshd_map(&mq, q, g.B, g.S, g.H_q, g.D, kT) ||
+      !make_bshd_map(&mk, k, g.B, g.S, g.H_kv, g.D, kT) ||
+      !make_bshd_map(&mv, v, g.B, g.S, g.H_kv, g.D, kT) ||
+      !make_bshd_map(&mdo, dout, g.B, g.S, g.H_q, g.D, kT))
+    return RA_ERR_LAUNCH;
+  if (g.D == 64)
+    return launch_d<64>(g, mq, mk, mv, mdo, out, lse, dout, dq, dk, dv, workspace, dev_status,
+                        stream);
+  return launch_d<128>(g, mq, mk, mv, mdo, out, lse, dout, dq, dk, dv, workspace, dev_status,
+                       stream);
+}
+
+}  // namespace ra

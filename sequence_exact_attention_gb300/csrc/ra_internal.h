@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "ring_attn.h"
@@ -50,6 +51,19 @@ ra_status launch_attn_tc(const Geometry& g, const void* q, const void* k,
                          const void* v, void* out, float* lse, int* visit_log,
                          int log_stride, int* dev_status, int sm_count,
                          cudaStream_t stream);
+
+// TMA map of a [B, S, H, D] bf16 tensor: box = 64 columns x 1 head x
+// `box_rows` rows x 1 batch, 128-byte swizzle (tensor_map.cpp).
+bool make_bshd_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D,
+                   int box_rows);
+
+// Backward pass (attn_bwd.cu). `workspace` holds bwd_workspace_floats(g)
+// floats: per (b, h, query tile) 128 base-2 lse values, then as many deltas.
+long long bwd_workspace_floats(const Geometry& g);
+ra_status launch_attn_bwd(const Geometry& g, const void* q, const void* k, const void* v,
+                          const void* out, const float* lse, const void* dout, void* dq,
+                          void* dk, void* dv, float* workspace, int* dev_status,
+                          cudaStream_t stream);
 
 struct MergeArgs {
   const void* o[RA_MERGE_MAX_N];

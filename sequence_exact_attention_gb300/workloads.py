@@ -13,7 +13,9 @@ Recipe (every tensor drawn on the CPU with ``torch.Generator().manual_seed``):
 draw q, then k, then v, each float32 N(0, std^2) in [B, S, H, D] order; for
 the GQA workload add +3.0 to every odd sequence row of k (all heads, all
 components) before the cast; cast to the target dtype with round-to-nearest-
-even (``Tensor.to``). Merge partials: n float32 N(0, 1) outputs [B, S, H, D],
+even (``Tensor.to``). Backward workloads add the upstream gradient dout,
+float32 N(0, std^2) [B, S, H_q, D] from its own generator seeded with
+seed + 500000, cast the same way. Merge partials: n float32 N(0, 1) outputs [B, S, H, D],
 then n lse tensors U(-20, 20) [B, H, S].
 """
 
@@ -93,6 +95,13 @@ MERGE_WORKLOADS = {
                                    seed=1005),
 }
 
+# Backward workloads: the forward shapes of the causal bf16 workloads.
+BWD_WORKLOADS = {
+    "bf16_s4k_causal_bwd": WORKLOADS["bf16_s4k_causal"].scaled(name="bf16_s4k_causal_bwd"),
+    "bf16_s32k_causal_zigzag_bwd": WORKLOADS["bf16_s32k_causal_zigzag"].scaled(
+        name="bf16_s32k_causal_zigzag_bwd"),
+}
+
 HEADLINE = "bf16_s32k_causal_zigzag"
 
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
@@ -112,6 +121,19 @@ def make_qkv(w: AttnWorkload):
         k[:, 1::2] += w.k_shift_odd
     dt = _TORCH_DTYPE[w.dtype]
     return q.to(dt), k.to(dt), v.to(dt)
+
+
+def make_dout(w: AttnWorkload):
+    """Upstream gradient dout [B,S,H_q,D] for the backward pass, CPU tensor."""
+    g = torch.Generator().manual_seed(w.seed + 500000)
+    d = torch.randn(w.B, w.S, w.H_q, w.D, generator=g) * w.std
+    return d.to(_TORCH_DTYPE[w.dtype])
+
+
+def bwd_flop(w: AttnWorkload):
+    """Algorithmic FLOP of the backward pass: 2.5x the forward's (five
+    products of the forward's size: S and dP recomputed, dV, dK, dQ)."""
+    return 2.5 * w.flop
 
 
 def make_merge_parts(w: MergeWorkload):

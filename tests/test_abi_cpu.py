@@ -143,9 +143,53 @@ def test_merge_argument_errors(lib):
                                 None) == RA_ERR_SHAPE
 
 
+def _ws_bytes(lib, B=1, Hq=2, S=256, D=64, P=4, order=0):
+    n = ctypes.c_size_t()
+    st = lib.ring_attn_bwd_workspace(B, Hq, S, D, P, order, ctypes.byref(n))
+    return st, n.value
+
+
+def test_bwd_workspace_size(lib):
+    # per (b, h, query tile): 128 base-2 lse values and 128 deltas, float32;
+    # tiles are 128 rows, cut per segment (the last tile of a segment padded)
+    st, n = _ws_bytes(lib, B=2, Hq=3, S=1000, D=128, P=4)        # segments of 250: 2 tiles
+    assert st == RA_OK and n == 2 * (2 * 3 * 4 * 2 * 128) * 4
+    st, n = _ws_bytes(lib, B=1, Hq=1, S=512, D=64, P=2, order=1)  # 4 halves of 128: 1 tile
+    assert st == RA_OK and n == 2 * (4 * 1 * 128) * 4
+    assert _ws_bytes(lib, D=96)[0] == RA_ERR_HEADDIM
+    assert _ws_bytes(lib, S=250)[0] == RA_ERR_SHAPE
+    assert _ws_bytes(lib, order=3)[0] == RA_ERR_DTYPE
+    assert lib.ring_attn_bwd_workspace(1, 2, 256, 64, 4, 0, None) == RA_ERR_NULL
+
+
+def _bwd(lib, q=A, k=A, v=A, out=A, lse=A, dout=A, dq=A, dk=A, dv=A, B=1, Hq=2, Hkv=2,
+         S=256, D=64, P=4, causal=1, scale=0.0, dtype=0, order=0, ws=A, ws_bytes=1 << 20,
+         status=None):
+    vp = ctypes.c_void_p
+    return lib.ring_attn_bwd(vp(q), vp(k), vp(v), vp(out), vp(lse), vp(dout), vp(dq), vp(dk),
+                             vp(dv), B, Hq, Hkv, S, D, P, causal, scale, dtype, order, vp(ws),
+                             ws_bytes, vp(status), None)
+
+
+def test_bwd_argument_errors(lib):
+    for name in ("q", "out", "lse", "dout", "dq", "dk", "dv", "ws"):
+        assert _bwd(lib, **{name: 0}) == RA_ERR_NULL, name
+    assert _bwd(lib, S=250) == RA_ERR_SHAPE
+    assert _bwd(lib, Hq=3, Hkv=2) == RA_ERR_SHAPE
+    assert _bwd(lib, D=96) == RA_ERR_HEADDIM
+    assert _bwd(lib, dtype=1) == RA_ERR_DTYPE              # bf16 only
+    assert _bwd(lib, order=2) == RA_ERR_DTYPE
+    assert _bwd(lib, dout=A + 8) == RA_ERR_ALIGN
+    assert _bwd(lib, dk=A + 2) == RA_ERR_ALIGN
+    assert _bwd(lib, ws=A + 4) == RA_ERR_ALIGN
+    need = _ws_bytes(lib)[1]
+    assert _bwd(lib, ws_bytes=need - 1) == RA_ERR_BUFFER
+
+
 def test_valid_call_without_gpu_reports_device_error(lib):
     """With every argument valid the only thing missing here is the GPU."""
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present: this case would launch on fake pointers")
     assert _fwd(lib) == RA_ERR_DEVICE
+    assert _bwd(lib) == RA_ERR_DEVICE
