@@ -395,6 +395,195 @@ def run_ours(args, w):
     return 0
 
 
+BWD_METRIC = "ring-attn bwd TFLOP/s (2.5x forward FLOP), bf16, causal, 1 GB300"
+
+
+def _bwd_pairs(w):
+    return w.B * w.H_q * w.S * w.S / (2.0 if w.causal else 1.0)
+
+
+def _oracle_bwd_sample_rate(w, q, k, v, dout, n):
+    """float64 backward oracle on a causal prefix: positions [0, n) of query
+    head 0 and its kv head (a prefix of a causal problem is itself a whole
+    problem). Returns (TFLOP/s by 10*D FLOP per allowed pair, seconds)."""
+    from oracle.backward import attention_backward
+    hk = 0
+    t0 = time.perf_counter()
+    attention_backward(q[:1, :n, :1], k[:1, :n, hk:hk + 1], v[:1, :n, hk:hk + 1],
+                       dout[:1, :n, :1], w.causal, w.scale)
+    dt = time.perf_counter() - t0
+    pairs = n * (n + 1) / 2 if w.causal else float(n * n)
+    return 10.0 * w.D * pairs / dt / 1e12, dt
+
+
+def run_bwd(args, w):
+    """The backward pass (prep, dK/dV, dQ kernels) on its workload."""
+    import torch
+    from sequence_exact_attention_gb300 import binding
+    from sequence_exact_attention_gb300.workloads import bwd_flop, make_dout, make_qkv
+
+    world, rank, local, dist = _dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load()
+    q, k, v = make_qkv(w)
+    dout = make_dout(w)
+    qd, kd, vd, dd = (t.to(dev) for t in (q, k, v, dout))
+    stream = torch.cuda.current_stream(dev)
+    out, lse = binding.ring_attn_fwd(qd, kd, vd, w.P, w.causal, w.scale, w.order, stream=stream)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(binding.bwd_workspace_bytes(w.B, w.H_q, w.S, w.D, w.P, w.order),
+                     dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    phases = (("bwd_prep_kernel", binding.BWD_PREP), ("bwd_dkdv_kernel", binding.BWD_DKDV),
+              ("bwd_dq_kernel", binding.BWD_DQ))
+
+    def step(ev=None):
+        for i, (_, ph) in enumerate(phases):
+            if ev is not None:
+                ev[i][0].record(stream)
+            binding.ring_attn_bwd(qd, kd, vd, out, lse, dd, w.P, w.causal, w.scale, w.order,
+                                  dq=dq, dk=dk, dv=dv, workspace=ws, dev_status=status,
+                                  stream=stream, phases=ph)
+            if ev is not None:
+                ev[i][1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError("device-side wait expired during warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in phases] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError("device-side wait expired in the timed region")
+    total_ms = t0.elapsed_time(t1)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flop = bwd_flop(w)
+    value = world * flop * args.steps / (total_ms / 1e3) / 1e12
+    phase_ms = {name: statistics.mean(e[i][0].elapsed_time(e[i][1]) for e in evs)
+                for i, (name, _) in enumerate(phases)}
+
+    # end to end: host buffers, inputs copied in and gradients copied out every step
+    e2e = None
+    if not args.no_e2e:
+        hosts_in = [t.pin_memory() for t in (q, k, v, dout)]
+        out_h, lse_h = out.cpu().pin_memory(), lse.cpu().pin_memory()
+        hosts_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+
+        def e2e_step():
+            for hsrc, ddst in zip(hosts_in + [out_h, lse_h], (qd, kd, vd, dd, out, lse)):
+                ddst.copy_(hsrc, non_blocking=True)
+            step()
+            for dsrc, hdst in zip((dq, dk, dv), hosts_out):
+                hdst.copy_(dsrc, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b_ = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = a.elapsed_time(b_)
+        if dist:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * flop * args.steps / (e_ms / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size()
+                                         for t in hosts_in + [out_h, lse_h]),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hosts_out),
+               "pipelined": "no: copies and kernels in order on one stream"}
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = _peaks()
+    pairs = _bwd_pairs(w)
+    dkdv_flop = 8.0 * w.D * pairs      # S^T, dP^T, dV, dK
+    dq_flop = 6.0 * w.D * pairs        # S, dP, dQ
+    dom = max(("bwd_dkdv_kernel", "bwd_dq_kernel"), key=lambda n: phase_ms[n])
+    dom_flop = dkdv_flop if dom == "bwd_dkdv_kernel" else dq_flop
+    achieved = dom_flop / (phase_ms[dom] / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n = args.cpu_prefix
+        rate, dt = _oracle_bwd_sample_rate(w, q, k, v, dout, n)
+        cpu = {"value": rate, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+               "sample": f"causal prefix of {n} positions, query head 0, float64 NumPy "
+                         f"backward oracle, {dt:.1f} s"}
+    line = {
+        "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": _config(w),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 dense (burst)", "kernel": f"{dom}<{w.D}>",
+                     "kernel_ms": phase_ms[dom],
+                     "algorithmic_flop": "dK/dV kernel 8*D per allowed pair (S^T, dP^T, dV, "
+                                         "dK); dQ kernel 6*D (S, dP, dQ)",
+                     "phase_ms": phase_ms,
+                     "frac_of_sustained_peak": achieved / float(peaks["bf16_tflops_sustained"])},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clk,
+        "gpu_launches": 3 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_bwd_reference(args, w):
+    world, rank, _, _ = _dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    from sequence_exact_attention_gb300.workloads import make_dout, make_qkv
+    q, k, v = make_qkv(w)
+    dout = make_dout(w)
+    n = args.cpu_prefix
+    for _ in range(args.warmup):
+        _oracle_bwd_sample_rate(w, q, k, v, dout, n)
+    flops, secs = 0.0, 0.0
+    for _ in range(args.steps):
+        rate, dt = _oracle_bwd_sample_rate(w, q, k, v, dout, n)
+        flops += rate * dt * 1e12
+        secs += dt
+    value = flops / secs / 1e12
+    sample = f"causal prefix of {n} positions, query head 0, per step (float64 NumPy oracle)"
+    print(json.dumps({
+        "impl": "reference", "metric": BWD_METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": _config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    return 0
+
+
 def run_merge(args, w):
     """The standalone n-way LSE merge on its workload; HBM-bound, GB/s."""
     import torch
@@ -463,16 +652,19 @@ def run_merge(args, w):
 
 
 def main():
-    from sequence_exact_attention_gb300.workloads import WORKLOADS, HEADLINE, MERGE_WORKLOADS
+    from sequence_exact_attention_gb300.workloads import (BWD_WORKLOADS, HEADLINE,
+                                                          MERGE_WORKLOADS, WORKLOADS)
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,
-                    choices=sorted(WORKLOADS) + sorted(MERGE_WORKLOADS))
+                    choices=sorted(WORKLOADS) + sorted(MERGE_WORKLOADS) + sorted(BWD_WORKLOADS))
     ap.add_argument("--cpu-rows", type=int, default=768)
     ap.add_argument("--ref-rows", type=int, default=24)
+    ap.add_argument("--cpu-prefix", type=int, default=16384,
+                    help="backward workloads: causal prefix length of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seq-len", type=int, default=0,
@@ -480,6 +672,11 @@ def main():
     args = ap.parse_args()
     if args.workload in MERGE_WORKLOADS:
         return run_merge(args, MERGE_WORKLOADS[args.workload])
+    if args.workload in BWD_WORKLOADS:
+        w = BWD_WORKLOADS[args.workload]
+        if args.seq_len:
+            w = w.scaled(S=args.seq_len, name=f"{w.name}@S={args.seq_len}")
+        return run_bwd_reference(args, w) if args.impl == "reference" else run_bwd(args, w)
     w = WORKLOADS[args.workload]
     if args.seq_len:
         w = w.scaled(S=args.seq_len, name=f"{w.name}@S={args.seq_len}")

@@ -193,6 +193,27 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v,
                         void* workspace, size_t workspace_bytes,
                         int* dev_status, void* stream);
 
+/* Phases of the backward pass (bit flags) for ring_attn_bwd_ex. */
+enum { RA_BWD_PREP = 1, RA_BWD_DKDV = 2, RA_BWD_DQ = 4, RA_BWD_ALL = 7 };
+
+/*
+ * ring_attn_bwd_ex - ring_attn_bwd restricted to the phases in `phases` (a
+ * nonzero OR of RA_BWD_*, else RA_ERR_RANGE), enqueued in the order prep,
+ * dK/dV, dQ; one kernel launch per phase. The prep phase writes the
+ * workspace (lse in base 2 and delta per query row); the dK/dV phase
+ * (writes dk, dv) and the dQ phase (writes dq) read it and are independent
+ * of each other, so after the prep phase they may run on two streams at
+ * once. A phase needs the prep phase of the same arguments to have run
+ * before it on the device. ring_attn_bwd is phases = RA_BWD_ALL.
+ */
+ra_status ring_attn_bwd_ex(const void* q, const void* k, const void* v,
+                           const void* out, const float* lse, const void* dout,
+                           void* dq, void* dk, void* dv,
+                           int B, int H_q, int H_kv, int S, int D, int P,
+                           int causal, float scale, int dtype, int order,
+                           void* workspace, size_t workspace_bytes, int phases,
+                           int* dev_status, void* stream);
+
 /*
  * attn_lse_merge - exact merge of two partial attention results over
  * disjoint key sets (glossary "sequence parallelism transformers",

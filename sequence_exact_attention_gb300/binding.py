@@ -23,7 +23,7 @@ MERGE_MAX_N = 16
 
 # every entry point declared in include/ring_attn.h
 EXPORTS = ("ring_attn_fwd", "ring_attn_fwd_ex", "ring_attn_visit_log_len",
-           "ring_attn_bwd_workspace", "ring_attn_bwd",
+           "ring_attn_bwd_workspace", "ring_attn_bwd", "ring_attn_bwd_ex",
            "attn_lse_merge", "attn_lse_merge_n", "ring_attn_plan",
            "ring_attn_expiry_test", "ring_attn_strerror", "ring_attn_version")
 
@@ -61,6 +61,9 @@ def load():
     lib.ring_attn_bwd.restype = c_int
     lib.ring_attn_bwd.argtypes = ([vp] * 9 + [c_int] * 7 + [c_float, c_int, c_int, vp,
                                                              ctypes.c_size_t, vp, vp])
+    lib.ring_attn_bwd_ex.restype = c_int
+    lib.ring_attn_bwd_ex.argtypes = ([vp] * 9 + [c_int] * 7 + [c_float, c_int, c_int, vp,
+                                                                ctypes.c_size_t, c_int, vp, vp])
     lib.attn_lse_merge.restype = c_int
     lib.attn_lse_merge.argtypes = [vp] * 6 + [c_int] * 5 + [vp]
     lib.attn_lse_merge_n.restype = c_int
@@ -200,14 +203,20 @@ def bwd_workspace_bytes(B, H_q, S, D, P, order="contiguous"):
     return n.value
 
 
+BWD_PREP, BWD_DKDV, BWD_DQ, BWD_ALL = 1, 2, 4, 7
+
+
 def ring_attn_bwd(q, k, v, out, lse, dout, P, causal, scale=None, order="contiguous",
-                  dq=None, dk=None, dv=None, workspace=None, dev_status=None, stream=None):
+                  dq=None, dk=None, dv=None, workspace=None, dev_status=None, stream=None,
+                  phases=BWD_ALL):
     """Gradients (dq, dk, dv) of ring attention for the upstream gradient dout.
 
     ``out`` and ``lse`` are the forward's results for the same arguments. All
     tensors are bf16 CUDA tensors (lse float32 [B, H_q, S]). ``workspace``
     (a uint8 CUDA tensor of at least ``bwd_workspace_bytes`` bytes) is
     allocated here when not given; the library itself allocates nothing.
+    ``phases`` other than BWD_ALL selects kernels (ring_attn_bwd_ex); a split
+    call must reuse the workspace the prep phase filled.
     """
     import torch
     lib = load()
@@ -234,11 +243,13 @@ def ring_attn_bwd(q, k, v, out, lse, dout, P, causal, scale=None, order="contigu
         if t is not None:
             _dev(t, n)
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
-    st = lib.ring_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
-                           _ptr(dq), _ptr(dk), _ptr(dv), B, H_q, H_kv, S, D, P,
-                           int(bool(causal)), sc, code, ORDERS[order], _ptr(workspace),
-                           workspace.numel() * workspace.element_size(), _ptr(dev_status),
-                           _stream(stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+            _ptr(dv), B, H_q, H_kv, S, D, P, int(bool(causal)), sc, code, ORDERS[order],
+            _ptr(workspace), workspace.numel() * workspace.element_size())
+    if phases == BWD_ALL:
+        st = lib.ring_attn_bwd(*args, _ptr(dev_status), _stream(stream))
+    else:
+        st = lib.ring_attn_bwd_ex(*args, int(phases), _ptr(dev_status), _stream(stream))
     _check(st, "ring_attn_bwd")
     return dq, dk, dv
 

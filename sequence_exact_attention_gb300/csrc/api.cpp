@@ -113,12 +113,14 @@ ra_status ring_attn_bwd_workspace(int B, int H_q, int S, int D, int P, int order
   return RA_OK;
 }
 
-ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
-                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                        int B, int H_q, int H_kv, int S, int D, int P, int causal,
-                        float scale, int dtype, int order, void* workspace,
-                        size_t workspace_bytes, int* dev_status, void* stream) {
+ra_status ring_attn_bwd_ex(const void* q, const void* k, const void* v, const void* out,
+                           const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                           int B, int H_q, int H_kv, int S, int D, int P, int causal,
+                           float scale, int dtype, int order, void* workspace,
+                           size_t workspace_bytes, int phases, int* dev_status,
+                           void* stream) {
   if (!lse || !dout || !dq || !dk || !dv || !workspace) return RA_ERR_NULL;
+  if (phases <= 0 || phases > RA_BWD_ALL) return RA_ERR_RANGE;
   ra_status st = check_attn_args(q, k, v, out, lse, B, H_q, H_kv, S, D, dtype, -1,
                                  nullptr, dev_status);
   if (st != RA_OK) return st;
@@ -138,8 +140,18 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
   st = check_device(&sms);
   if (st != RA_OK) return st;
   return launch_attn_bwd(g, q, k, v, out, lse, dout, dq, dk, dv,
-                         static_cast<float*>(workspace), dev_status,
+                         static_cast<float*>(workspace), phases, dev_status,
                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                        int B, int H_q, int H_kv, int S, int D, int P, int causal,
+                        float scale, int dtype, int order, void* workspace,
+                        size_t workspace_bytes, int* dev_status, void* stream) {
+  return ring_attn_bwd_ex(q, k, v, out, lse, dout, dq, dk, dv, B, H_q, H_kv, S, D, P, causal,
+                          scale, dtype, order, workspace, workspace_bytes, RA_BWD_ALL,
+                          dev_status, stream);
 }
 
 ra_status attn_lse_merge_n(const void* const* o, const float* const* lse,

@@ -660,7 +660,7 @@ template <int D>
 ra_status launch_d(const Geometry& g, const CUtensorMap& mq, const CUtensorMap& mk,
                    const CUtensorMap& mv, const CUtensorMap& mdo, const void* out,
                    const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                   float* ws, int* status, cudaStream_t stream) {
+                   float* ws, int phases, int* status, cudaStream_t stream) {
   using C = Cfg<D>;
   const long long rows = bwd_workspace_floats(g) / 2;
   float* lse2 = ws;
@@ -670,22 +670,30 @@ ra_status launch_d(const Geometry& g, const CUtensorMap& mq, const CUtensorMap& 
   const long long grid_kv = n_tiles * g.B * g.H_kv;
   const long long grid_q = n_tiles * g.B * g.H_q;
   if (prep_blocks > 0x7fffffffLL || grid_q > 0x7fffffffLL) return RA_ERR_RANGE;
-  bwd_prep_kernel<D><<<(unsigned)prep_blocks, 256, 0, stream>>>(
-      g, static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse,
-      lse2, delta, rows);
-  if (cudaGetLastError() != cudaSuccess) return RA_ERR_LAUNCH;
-  if (cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kSmemBytes) != cudaSuccess)
-    return RA_ERR_LAUNCH;
-  bwd_dkdv_kernel<D><<<(unsigned)grid_kv, kThreads, C::kSmemBytes, stream>>>(
-      mq, mk, mv, mdo, g, lse2, delta, static_cast<__nv_bfloat16*>(dk),
-      static_cast<__nv_bfloat16*>(dv), status);
-  if (cudaGetLastError() != cudaSuccess) return RA_ERR_LAUNCH;
-  bwd_dq_kernel<D><<<(unsigned)grid_q, kThreads, C::kSmemBytes, stream>>>(
-      mq, mk, mv, mdo, g, lse2, delta, static_cast<__nv_bfloat16*>(dq), status);
-  return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
+  if (phases & RA_BWD_PREP) {
+    bwd_prep_kernel<D><<<(unsigned)prep_blocks, 256, 0, stream>>>(
+        g, static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout),
+        lse, lse2, delta, rows);
+    if (cudaGetLastError() != cudaSuccess) return RA_ERR_LAUNCH;
+  }
+  if (phases & RA_BWD_DKDV) {
+    if (cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+      return RA_ERR_LAUNCH;
+    bwd_dkdv_kernel<D><<<(unsigned)grid_kv, kThreads, C::kSmemBytes, stream>>>(
+        mq, mk, mv, mdo, g, lse2, delta, static_cast<__nv_bfloat16*>(dk),
+        static_cast<__nv_bfloat16*>(dv), status);
+    if (cudaGetLastError() != cudaSuccess) return RA_ERR_LAUNCH;
+  }
+  if (phases & RA_BWD_DQ) {
+    if (cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+      return RA_ERR_LAUNCH;
+    bwd_dq_kernel<D><<<(unsigned)grid_q, kThreads, C::kSmemBytes, stream>>>(
+        mq, mk, mv, mdo, g, lse2, delta, static_cast<__nv_bfloat16*>(dq), status);
+    if (cudaGetLastError() != cudaSuccess) return RA_ERR_LAUNCH;
+  }
+  return RA_OK;
 }
 
 }  // namespace
@@ -696,8 +704,8 @@ long long bwd_workspace_floats(const Geometry& g) {
 
 ra_status launch_attn_bwd(const Geometry& g, const void* q, const void* k, const void* v,
                           const void* out, const float* lse, const void* dout, void* dq,
-                          void* dk, void* dv, float* workspace, int* dev_status,
-                          cudaStream_t stream) {
+                          void* dk, void* dv, float* workspace, int phases,
+                          int* dev_status, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mdo;
   if (!make_bshd_map(&mq, q, g.B, g.S, g.H_q, g.D, kT) ||
       !make_bshd_map(&mk, k, g.B, g.S, g.H_kv, g.D, kT) ||
@@ -705,10 +713,10 @@ ra_status launch_attn_bwd(const Geometry& g, const void* q, const void* k, const
       !make_bshd_map(&mdo, dout, g.B, g.S, g.H_q, g.D, kT))
     return RA_ERR_LAUNCH;
   if (g.D == 64)
-    return launch_d<64>(g, mq, mk, mv, mdo, out, lse, dout, dq, dk, dv, workspace, dev_status,
-                        stream);
-  return launch_d<128>(g, mq, mk, mv, mdo, out, lse, dout, dq, dk, dv, workspace, dev_status,
-                       stream);
+    return launch_d<64>(g, mq, mk, mv, mdo, out, lse, dout, dq, dk, dv, workspace, phases,
+                        dev_status, stream);
+  return launch_d<128>(g, mq, mk, mv, mdo, out, lse, dout, dq, dk, dv, workspace, phases,
+                       dev_status, stream);
 }
 
 }  // namespace ra

@@ -62,8 +62,8 @@ bool make_bshd_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D,
 long long bwd_workspace_floats(const Geometry& g);
 ra_status launch_attn_bwd(const Geometry& g, const void* q, const void* k, const void* v,
                           const void* out, const float* lse, const void* dout, void* dq,
-                          void* dk, void* dv, float* workspace, int* dev_status,
-                          cudaStream_t stream);
+                          void* dk, void* dv, float* workspace, int phases,
+                          int* dev_status, cudaStream_t stream);
 
 struct MergeArgs {
   const void* o[RA_MERGE_MAX_N];

@@ -184,6 +184,11 @@ def test_bwd_argument_errors(lib):
     assert _bwd(lib, ws=A + 4) == RA_ERR_ALIGN
     need = _ws_bytes(lib)[1]
     assert _bwd(lib, ws_bytes=need - 1) == RA_ERR_BUFFER
+    vp = ctypes.c_void_p
+    for bad in (0, 8, -1):
+        assert lib.ring_attn_bwd_ex(vp(A), vp(A), vp(A), vp(A), vp(A), vp(A), vp(A), vp(A),
+                                    vp(A), 1, 2, 2, 256, 64, 4, 1, 0.0, 0, 0, vp(A), 1 << 20,
+                                    bad, None, None) == RA_ERR_RANGE
 
 
 def test_valid_call_without_gpu_reports_device_error(lib):

@@ -95,6 +95,32 @@ def test_backward_is_independent_of_P_and_order():
         check(f"P={P} {order} dv", dv, rv)
 
 
+def test_backward_phases_split_equal_whole_call():
+    """Prep, then dK/dV and dQ on two streams at once, equals the single call."""
+    w = AttnWorkload("phases", "bf16", 1, 4, 2, 1024, 128, 4, True, "zigzag", std=1.0, seed=2150)
+    dev = torch.device("cuda")
+    q, k, v = (t.to(dev) for t in make_qkv(w))
+    dout = make_dout(w).to(dev)
+    out, lse = binding.ring_attn_fwd(q, k, v, w.P, True, w.scale, w.order)
+    dq, dk, dv = binding.ring_attn_bwd(q, k, v, out, lse, dout, w.P, True, w.scale, w.order)
+    ws = torch.empty(binding.bwd_workspace_bytes(w.B, w.H_q, w.S, w.D, w.P, w.order),
+                     dtype=torch.uint8, device=dev)
+    dq2, dk2, dv2 = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+    kw = dict(dq=dq2, dk=dk2, dv=dv2, workspace=ws)
+    main = torch.cuda.current_stream()
+    binding.ring_attn_bwd(q, k, v, out, lse, dout, w.P, True, w.scale, w.order,
+                          phases=binding.BWD_PREP, stream=main, **kw)
+    side = torch.cuda.Stream()
+    side.wait_stream(main)
+    binding.ring_attn_bwd(q, k, v, out, lse, dout, w.P, True, w.scale, w.order,
+                          phases=binding.BWD_DKDV, stream=main, **kw)
+    binding.ring_attn_bwd(q, k, v, out, lse, dout, w.P, True, w.scale, w.order,
+                          phases=binding.BWD_DQ, stream=side, **kw)
+    main.wait_stream(side)
+    torch.cuda.synchronize()
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+
+
 def test_backward_headline_shape_sampled():
     """The 32K causal zig-zag shape in the launch configuration the bench
     times, checked on sampled query rows and key rows of two heads."""
