@@ -25,8 +25,9 @@
 // The two gradient kernels both recompute S and dP; in exchange neither needs
 // atomics, and each gradient is accumulated on chip and written once.
 //
-// Roles (192 threads): warps 0-3 compute (TMEM lane quarter = warp), warp 4
-// TMA producer, warp 5 tensor-core issuer and TMEM owner. Every wait is
+// Roles (320 threads): warps 0-7 compute (TMEM lane quarter = warp mod 4,
+// column half = warp / 4), warp 8 TMA producer, warp 9 tensor-core issuer
+// and TMEM owner. Every wait is
 // bounded (two seconds, then the CTA gives up, drains what it issued, frees
 // its TMEM and reports RA_ERR_TIMEOUT in the status word).
 #include <cuda.h>
@@ -42,9 +43,9 @@ namespace {
 using namespace sm100;
 
 constexpr int kT = 128;                         // tile rows (queries or keys)
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;                   // S or S^T, then P / dS in bf16
 constexpr uint32_t kColDP = 128;                // dP or dP^T, then dS^T in bf16
@@ -71,10 +72,14 @@ struct Cfg {
   static constexpr int bFix = 0;
   static constexpr int bFull = 1;     // [2] stage loaded
   static constexpr int bFree = 3;     // [2] stage no longer read by the tensor cores
-  static constexpr int bSdp = 5;      // S and dP ready in TMEM
-  static constexpr int bP = 6;        // 128 arrivals: P / dS written to TMEM
-  static constexpr int bAcc = 7;      // accumulating MMAs of a visit done
-  static constexpr int bFinal = 8;
+  static constexpr int bS = 5;        // S (or S^T) in TMEM
+  static constexpr int bDP = 6;       // dP (or dP^T) in TMEM
+  static constexpr int bP = 7;        // 256 arrivals: pass 1 done (P^T stored / S read)
+  static constexpr int bDS = 8;       // 256 arrivals: pass 2 done (dS stored)
+  static constexpr int bAccV = 9;     // dV MMA of a visit done
+  static constexpr int bAccK = 10;    // dK MMA (or dQ MMA) of a visit done
+  static constexpr int bAcc = bAccK;
+  static constexpr int bFinal = 11;
   static constexpr int kHolderOff = kBarBytes - 16;
   static constexpr int kNeverOff = kBarBytes - 12;
   static constexpr int kAbortOff = kBarBytes - 8;
@@ -87,6 +92,35 @@ struct Cfg {
 __host__ __device__ __forceinline__ long long ws_tile(const Geometry& g, int bh, int seg,
                                                       int ti) {
   return (((long long)bh * g.n_seg + seg) * g.nt + ti) * kT;
+}
+
+// TMEM column (relative to the S or dP range) of the bf16 operand columns
+// that K step kk (16 rows of the reduction) reads: the two 64-column halves
+// keep their 32 packed columns at the start of their own range.
+__device__ __forceinline__ uint32_t pcol(int kk) {
+  return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8);
+}
+
+template <class C, class BarFn>
+__device__ __forceinline__ void init_barriers(BarFn bar, volatile int* abort_flag,
+                                              volatile int* never) {
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::bFix), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(C::bFull + i), 1);
+      mbar_init(bar(C::bFree + i), 1);
+    }
+    mbar_init(bar(C::bS), 1);
+    mbar_init(bar(C::bDP), 1);
+    mbar_init(bar(C::bP), 256);
+    mbar_init(bar(C::bDS), 256);
+    mbar_init(bar(C::bAccV), 1);
+    mbar_init(bar(C::bAccK), 1);
+    mbar_init(bar(C::bFinal), 1);
+    *abort_flag = 0;
+    *never = 0;
+    fence_mbar_init();
+  }
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -209,6 +243,12 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
 }
 
 // ------------------------------------------------------------------ dK, dV
+// Per visit the tensor cores run S^T, dP^T, dV, dK in that order and the
+// compute warps run two passes: P^T (from S^T) while dP^T is computed, then
+// dS^T (from dP^T and the P^T kept in registers) while dV is accumulated.
+// Warp w covers key rows 32 (w mod 4) .. +31 and query columns 64 (w / 4)
+// .. +63; its bf16 P^T and dS^T go into the first 32 columns of its own
+// S^T and dP^T column ranges, so no warp writes columns another one reads.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -243,20 +283,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int kv_valid = min(kT, g.seg_len - kti * kT);
   const int h0 = hk * grp;
 
-  if (threadIdx.x == 0) {
-    mbar_init(bar(C::bFix), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(C::bFull + i), 1);
-      mbar_init(bar(C::bFree + i), 1);
-    }
-    mbar_init(bar(C::bSdp), 1);
-    mbar_init(bar(C::bP), 128);
-    mbar_init(bar(C::bAcc), 1);
-    mbar_init(bar(C::bFinal), 1);
-    *abort_flag = 0;
-    *never = 0;
-    fence_mbar_init();
-  }
+  init_barriers<C>(bar, abort_flag, never);
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
@@ -317,34 +344,43 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
       int j = 0;
       while (ok && it.next(g, qt)) {
         const int st = j & 1;
+        const uint32_t pj = (uint32_t)(j - 1) & 1;     // parity of visit j-1
         const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
         ok = mbar_wait(bar(C::bFull + st), (uint32_t)(j >> 1) & 1, abort_flag, kTimeoutNs);
-        // S^T and dP^T overwrite the P^T, dS^T that the previous visit's
-        // accumulating MMAs read
-        if (ok && j > 0) ok = mbar_wait(bar(C::bAcc), (uint32_t)(j - 1) & 1, abort_flag, kTimeoutNs);
+        // S^T(j) overwrites the P^T(j-1) that dV(j-1) reads
+        if (ok && j > 0) ok = mbar_wait(bar(C::bAccV), pj, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + kColS, k_kmaj + kstep_off(kk), q_kmaj + so + kstep_off(kk), id_s,
                   kk > 0 ? 1u : 0u);
+        umma_commit(bar(C::bS));
+        // dP^T(j) overwrites the dS^T(j-1) that dK(j-1) reads
+        if (j > 0) ok = mbar_wait(bar(C::bAccK), pj, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + kColDP, v_kmaj + kstep_off(kk), do_kmaj + so + kstep_off(kk), id_s,
                   kk > 0 ? 1u : 0u);
-        umma_commit(bar(C::bSdp));
+        umma_commit(bar(C::bDP));
         ok = mbar_wait(bar(C::bP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
-          umma_ts(tmem + kColAcc, tmem + kColS + kk * 8, do_mn + so + (uint64_t)(kk * 2048 >> 4),
+          umma_ts(tmem + kColAcc, tmem + kColS + pcol(kk), do_mn + so + (uint64_t)(kk * 2048 >> 4),
                   id_acc, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(C::bAccV));
+        ok = mbar_wait(bar(C::bDS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
-          umma_ts(tmem + kColAcc + D, tmem + kColDP + kk * 8, q_mn + so + (uint64_t)(kk * 2048 >> 4),
-                  id_acc, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(C::bAcc));
+          umma_ts(tmem + kColAcc + D, tmem + kColDP + pcol(kk),
+                  q_mn + so + (uint64_t)(kk * 2048 >> 4), id_acc, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(C::bAccK));
         umma_commit(bar(C::bFree + st));
         ++j;
       }
@@ -353,9 +389,11 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     __syncwarp();
   } else {
-    // ============ compute: thread = key row (TMEM lane), 128 query columns
-    const int row = warp * 32 + lane;
-    const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
+    // ============ compute: key row = TMEM lane, 64 query columns per warp
+    const int wq = warp & 3, hf = warp >> 2;
+    const int row = wq * 32 + lane;
+    const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
+    const uint32_t c0 = (uint32_t)(hf * 64);          // this warp's first column
     const int kpos = kv_lo + row;
     const float sl2 = g.scale_log2;
     QIter it;
@@ -365,51 +403,67 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
     bool ok = true;
     while (it.next(g, qt)) {
       const int st = j & 1;
-      if (ok) ok = mbar_wait(bar(C::bSdp), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+      if (ok) ok = mbar_wait(bar(C::bS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
       if (!ok) { ++j; continue; }
       tc_fence_after();
       const float* stat =
           reinterpret_cast<const float*>(base_ptr + C::kStage0 + st * C::kStageBytes + 2 * C::kTileBytes);
-      const float2* l2v = reinterpret_cast<const float2*>(stat);
-      const float2* dlv = reinterpret_cast<const float2*>(stat + kT);
-      const int lim = qt.mask ? kpos - qt.lo : -1;      // query column c is masked iff c < lim
+      const float2* l2v = reinterpret_cast<const float2*>(stat + c0);
+      const float2* dlv = reinterpret_cast<const float2*>(stat + kT + c0);
+      const int lim = qt.mask ? kpos - qt.lo - (int)c0 : -1;   // column c masked iff c < lim
+      // ---- pass 1: P^T = exp2(S^T * scale * log2 e - lse2), bf16 into TMEM
+      float p[64];
+      {
+        uint32_t u0[32], u1[32];
+        tmem_ld32(tmem + t_lane + kColS + c0, u0);
+        tmem_ld32(tmem + t_lane + kColS + c0 + 32, u1);
+        tmem_ld_wait();
+        reg_fence(u0);
+        reg_fence(u1);
+        uint32_t pk[32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pp[32], pd[32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int col = half * 64 + c * 32;
-          uint32_t us[32], ud[32];
-          tmem_ld32(tmem + t_lane + kColS + col, us);
-          tmem_ld32(tmem + t_lane + kColDP + col, ud);
-          tmem_ld_wait();
-          reg_fence(us);
-          reg_fence(ud);
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float2 l2 = l2v[(col + i) >> 1];
-            const float2 dl = dlv[(col + i) >> 1];
-            float p0 = ex2_approx(fmaf(__uint_as_float(us[i]), sl2, -l2.x));
-            float p1 = ex2_approx(fmaf(__uint_as_float(us[i + 1]), sl2, -l2.y));
-            if (col + i < lim) p0 = 0.f;
-            if (col + i + 1 < lim) p1 = 0.f;
-            const float d0 = p0 * (__uint_as_float(ud[i]) - dl.x);
-            const float d1 = p1 * (__uint_as_float(ud[i + 1]) - dl.y);
-            pp[c * 16 + i / 2] = pack_bf16x2(p0, p1);
-            pd[c * 16 + i / 2] = pack_bf16x2(d0, d1);
-          }
+        for (int i = 0; i < 64; i += 2) {
+          const float2 l2 = l2v[i >> 1];
+          const uint32_t s0 = i < 32 ? u0[i] : u1[i - 32];
+          const uint32_t s1 = i < 32 ? u0[i + 1] : u1[i - 31];
+          p[i] = i < lim ? 0.f : ex2_approx(fmaf(__uint_as_float(s0), sl2, -l2.x));
+          p[i + 1] = i + 1 < lim ? 0.f : ex2_approx(fmaf(__uint_as_float(s1), sl2, -l2.y));
+          pk[i >> 1] = pack_bf16x2(p[i], p[i + 1]);
         }
-        // columns [32 half, 32 half + 32) were read above (loads in order)
-        tmem_st32(tmem + t_lane + kColS + half * 32, pp);
-        tmem_st32(tmem + t_lane + kColDP + half * 32, pd);
+        tmem_st32(tmem + t_lane + kColS + c0, pk);
+        tmem_st_wait();
       }
-      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(C::bP));
+      // ---- pass 2: dS^T = P^T * (dP^T - delta), bf16 into TMEM
+      ok = mbar_wait(bar(C::bDP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+      if (!ok) { ++j; continue; }
+      tc_fence_after();
+      {
+        uint32_t u0[32], u1[32];
+        tmem_ld32(tmem + t_lane + kColDP + c0, u0);
+        tmem_ld32(tmem + t_lane + kColDP + c0 + 32, u1);
+        tmem_ld_wait();
+        reg_fence(u0);
+        reg_fence(u1);
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const float2 dl = dlv[i >> 1];
+          const uint32_t d0 = i < 32 ? u0[i] : u1[i - 32];
+          const uint32_t d1 = i < 32 ? u0[i + 1] : u1[i - 31];
+          pk[i >> 1] = pack_bf16x2(p[i] * (__uint_as_float(d0) - dl.x),
+                                   p[i + 1] * (__uint_as_float(d1) - dl.y));
+        }
+        tmem_st32(tmem + t_lane + kColDP + c0, pk);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::bDS));
       ++j;
     }
-    // ---- epilogue: dV, and dK times scale, as bf16 rows
-    if (ok && j > 0) ok = mbar_wait(bar(C::bAcc), (uint32_t)(j - 1) & 1, abort_flag, kTimeoutNs);
+    // ---- epilogue: this warp's half of the dV and dK columns, as bf16 rows
+    if (ok && j > 0) ok = mbar_wait(bar(C::bAccK), (uint32_t)(j - 1) & 1, abort_flag, kTimeoutNs);
     if (ok) {
       tc_fence_after();
       const bool row_ok = row < kv_valid;
@@ -419,15 +473,16 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
         __nv_bfloat16* dst = (which ? dk : dv) + off;
         const float mul = which ? g.scale : 1.f;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
+          const int col = hf * (D / 2) + c * 32;
           uint32_t u[32];
-          tmem_ld32(tmem + t_lane + kColAcc + which * D + c * 32, u);
+          tmem_ld32(tmem + t_lane + kColAcc + which * D + col, u);
           tmem_ld_wait(u);
           if (j == 0) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) u[i] = 0u;
           }
-          if (row_ok) store_row32(dst + c * 32, u, mul);
+          if (row_ok) store_row32(dst + col, u, mul);
         }
       }
     }
@@ -442,6 +497,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
 }
 
 // ------------------------------------------------------------------ dQ
+// Per visit the tensor cores run S, dP, dQ; the compute warps read S (pass 1,
+// P kept in registers) and then dP (pass 2), writing bf16 dS into the first
+// 32 columns of their own dP column range. S of the next key tile is issued
+// as soon as pass 1 has read S, so it runs while dS and dQ are computed.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -478,20 +537,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int q_lo = seg * g.seg_len + ti * kT;
   const int q_valid = min(kT, g.seg_len - ti * kT);
 
-  if (threadIdx.x == 0) {
-    mbar_init(bar(C::bFix), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(C::bFull + i), 1);
-      mbar_init(bar(C::bFree + i), 1);
-    }
-    mbar_init(bar(C::bSdp), 1);
-    mbar_init(bar(C::bP), 128);
-    mbar_init(bar(C::bAcc), 1);
-    mbar_init(bar(C::bFinal), 1);
-    *abort_flag = 0;
-    *never = 0;
-    fence_mbar_init();
-  }
+  init_barriers<C>(bar, abort_flag, never);
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
@@ -544,30 +590,53 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
       KvIter it;
       it.init(g, r, q_lo, q_valid);
       KvTile kv;
+      bool have = ok && it.next(g, kv);
+      // S(0)
+      if (have) {
+        ok = mbar_wait(bar(C::bFull + 0), 0, abort_flag, kTimeoutNs);
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + kColS, q_kmaj + kstep_off(kk), k_kmaj + kstep_off(kk), id_s,
+                    kk > 0 ? 1u : 0u);
+          umma_commit(bar(C::bS));
+        }
+      }
       int j = 0;
-      while (ok && it.next(g, kv)) {
+      while (ok && have) {
         const int st = j & 1;
         const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
-        ok = mbar_wait(bar(C::bFull + st), (uint32_t)(j >> 1) & 1, abort_flag, kTimeoutNs);
-        // S and dP overwrite the dS that the previous dQ MMA reads
-        if (ok && j > 0) ok = mbar_wait(bar(C::bAcc), (uint32_t)(j - 1) & 1, abort_flag, kTimeoutNs);
+        // dP(j) overwrites the dS(j-1) that dQ(j-1) reads
+        if (j > 0) ok = mbar_wait(bar(C::bAcc), (uint32_t)(j - 1) & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColS, q_kmaj + kstep_off(kk), k_kmaj + so + kstep_off(kk), id_s,
-                  kk > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + kColDP, do_kmaj + kstep_off(kk), v_kmaj + so + kstep_off(kk), id_s,
                   kk > 0 ? 1u : 0u);
-        umma_commit(bar(C::bSdp));
-        ok = mbar_wait(bar(C::bP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+        umma_commit(bar(C::bDP));
+        // S(j+1), once pass 1 of tile j has read S(j)
+        have = it.next(g, kv);
+        if (have) {
+          const int sn = (j + 1) & 1;
+          ok = mbar_wait(bar(C::bFull + sn), (uint32_t)((j + 1) >> 1) & 1, abort_flag, kTimeoutNs) &&
+               mbar_wait(bar(C::bP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t son = (uint64_t)((sn * C::kStageBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + kColS, q_kmaj + kstep_off(kk), k_kmaj + son + kstep_off(kk), id_s,
+                    kk > 0 ? 1u : 0u);
+          umma_commit(bar(C::bS));
+        }
+        ok = mbar_wait(bar(C::bDS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
-          umma_ts(tmem + kColAcc, tmem + kColS + kk * 8, k_mn + so + (uint64_t)(kk * 2048 >> 4),
+          umma_ts(tmem + kColAcc, tmem + kColDP + pcol(kk), k_mn + so + (uint64_t)(kk * 2048 >> 4),
                   id_acc, (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar(C::bAcc));
         umma_commit(bar(C::bFree + st));
@@ -578,9 +647,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     __syncwarp();
   } else {
-    // ============ compute: thread = query row (TMEM lane), 128 key columns
-    const int row = warp * 32 + lane;
-    const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
+    // ============ compute: query row = TMEM lane, 64 key columns per warp
+    const int wq = warp & 3, hf = warp >> 2;
+    const int row = wq * 32 + lane;
+    const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
+    const uint32_t c0 = (uint32_t)(hf * 64);
     const int q_pos = q_lo + row;
     const float sl2 = g.scale_log2;
     const long long wi = ws_tile(g, bh, seg, ti) + row;
@@ -592,41 +663,54 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
     int j = 0;
     bool ok = true;
     while (it.next(g, kv)) {
-      if (ok) ok = mbar_wait(bar(C::bSdp), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+      if (ok) ok = mbar_wait(bar(C::bS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
       if (!ok) { ++j; continue; }
       tc_fence_after();
-      // key column c is allowed iff c < lim
-      const int lim = kv.work == kMask
-                          ? (g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid)
-                          : kT;
+      // key column c of this warp is allowed iff c < lim
+      const int lim = (kv.work == kMask
+                           ? (g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid)
+                           : kT) - (int)c0;
+      // ---- pass 1: P = exp2(S * scale * log2 e - lse2), kept in registers
+      float p[64];
+      {
+        uint32_t u0[32], u1[32];
+        tmem_ld32(tmem + t_lane + kColS + c0, u0);
+        tmem_ld32(tmem + t_lane + kColS + c0 + 32, u1);
+        tmem_ld_wait();
+        reg_fence(u0);
+        reg_fence(u1);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pd[32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int col = half * 64 + c * 32;
-          uint32_t us[32], ud[32];
-          tmem_ld32(tmem + t_lane + kColS + col, us);
-          tmem_ld32(tmem + t_lane + kColDP + col, ud);
-          tmem_ld_wait();
-          reg_fence(us);
-          reg_fence(ud);
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float p0 = ex2_approx(fmaf(__uint_as_float(us[i]), sl2, -l2_row));
-            float p1 = ex2_approx(fmaf(__uint_as_float(us[i + 1]), sl2, -l2_row));
-            if (col + i >= lim) p0 = 0.f;
-            if (col + i + 1 >= lim) p1 = 0.f;
-            pd[c * 16 + i / 2] = pack_bf16x2(p0 * (__uint_as_float(ud[i]) - dl_row),
-                                             p1 * (__uint_as_float(ud[i + 1]) - dl_row));
-          }
+        for (int i = 0; i < 64; ++i) {
+          const uint32_t s = i < 32 ? u0[i] : u1[i - 32];
+          p[i] = i < lim ? ex2_approx(fmaf(__uint_as_float(s), sl2, -l2_row)) : 0.f;
         }
-        // columns [32 half, 32 half + 32) were read above (loads in order)
-        tmem_st32(tmem + t_lane + kColS + half * 32, pd);
       }
-      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::bP));
+      mbar_arrive(bar(C::bP));          // S may be overwritten
+      // ---- pass 2: dS = P * (dP - delta), bf16 into TMEM
+      ok = mbar_wait(bar(C::bDP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+      if (!ok) { ++j; continue; }
+      tc_fence_after();
+      {
+        uint32_t u0[32], u1[32];
+        tmem_ld32(tmem + t_lane + kColDP + c0, u0);
+        tmem_ld32(tmem + t_lane + kColDP + c0 + 32, u1);
+        tmem_ld_wait();
+        reg_fence(u0);
+        reg_fence(u1);
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const uint32_t d0 = i < 32 ? u0[i] : u1[i - 32];
+          const uint32_t d1 = i < 32 ? u0[i + 1] : u1[i - 31];
+          pk[i >> 1] = pack_bf16x2(p[i] * (__uint_as_float(d0) - dl_row),
+                                   p[i + 1] * (__uint_as_float(d1) - dl_row));
+        }
+        tmem_st32(tmem + t_lane + kColDP + c0, pk);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::bDS));
       ++j;
     }
     if (ok && j > 0) ok = mbar_wait(bar(C::bAcc), (uint32_t)(j - 1) & 1, abort_flag, kTimeoutNs);
@@ -635,15 +719,16 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
       const bool row_ok = row < q_valid;
       __nv_bfloat16* dst = dq + (((size_t)b * g.S + q_pos) * g.H_q + h) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = hf * (D / 2) + c * 32;
         uint32_t u[32];
-        tmem_ld32(tmem + t_lane + kColAcc + c * 32, u);
+        tmem_ld32(tmem + t_lane + kColAcc + col, u);
         tmem_ld_wait(u);
         if (j == 0) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) u[i] = 0u;
         }
-        if (row_ok) store_row32(dst + c * 32, u, g.scale);
+        if (row_ok) store_row32(dst + col, u, g.scale);
       }
     }
   }
