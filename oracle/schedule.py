@@ -14,10 +14,15 @@ Sources, glossary "sequence parallelism transformers":
   sequence is cut into 2P equal halves and rank r owns halves r and 2P-1-r.
   Inputs and outputs stay in natural token order; only the ownership changes.
 
-Divisibility (nvFuser PR "Transformer sequence parallel forward" skips a
-sequence-parallel case when s % d != 0; the mvp-engine "sequence-parallel"
-skill asks for seq_len divisible by the split or explicit padding): S must be a
-multiple of P (contiguous) or of 2P (zig-zag).
+Uneven lengths (the mvp-engine "sequence-parallel" skill: seq_len divisible
+by the split, else pad explicitly and mask; the nvFuser PR "Transformer
+sequence parallel forward" skips the s % d != 0 case instead): the sequence
+is padded to the next multiple of P (contiguous) or 2P (zig-zag), so every
+chunk (half) spans L = ceil(S / P) (ceil(S / 2P)) positions starting at a
+multiple of L, and the padding positions, at S and beyond, hold no tokens:
+a chunk's tokens are its positions below S. Ranges are therefore clipped at
+S; a trailing chunk can be shorter than L or empty. When S is a multiple,
+this is the plain even split.
 
 Classes of a (query set, key set) pair under the causal rule j <= i:
 SKIP (no allowed pair), FULL (every pair allowed), PARTIAL (some allowed).
@@ -33,24 +38,29 @@ ORDER_CONTIGUOUS, ORDER_ZIGZAG = 0, 1
 def _check(S, P, order):
     if P <= 0 or S <= 0:
         raise ValueError("S and P must be positive")
-    if order == ORDER_CONTIGUOUS:
-        if S % P:
-            raise ValueError("S must be a multiple of P")
-    elif order == ORDER_ZIGZAG:
-        if S % (2 * P):
-            raise ValueError("zig-zag order needs S to be a multiple of 2P")
-    else:
+    if order not in (ORDER_CONTIGUOUS, ORDER_ZIGZAG):
         raise ValueError("unknown order")
 
 
-def rank_segments(S, P, order):
-    """Per rank, the list of (start, length) token ranges it owns, ascending."""
+def segment_length(S, P, order):
+    """L: positions spanned by one chunk (contiguous) or half (zig-zag) of
+    the padded sequence."""
     _check(S, P, order)
+    parts = P if order == ORDER_CONTIGUOUS else 2 * P
+    return -(-S // parts)
+
+
+def _clip(start, L, S):
+    return (start, max(0, min(L, S - start)))
+
+
+def rank_segments(S, P, order):
+    """Per rank, the list of (start, length) token ranges it owns, ascending.
+    Lengths are clipped at S (possibly 0); starts are multiples of L."""
+    L = segment_length(S, P, order)
     if order == ORDER_CONTIGUOUS:
-        C = S // P
-        return [[(r * C, C)] for r in range(P)]
-    L = S // (2 * P)
-    return [[(r * L, L), ((2 * P - 1 - r) * L, L)] for r in range(P)]
+        return [[_clip(r * L, L, S)] for r in range(P)]
+    return [[_clip(r * L, L, S), _clip((2 * P - 1 - r) * L, L, S)] for r in range(P)]
 
 
 def classify(q_ranges, kv_ranges, causal):
@@ -96,13 +106,15 @@ def ring_schedule(S, P, causal, order):
 
 def schedule_table(S, P, causal, order):
     """The schedule as an int32 table [P*P, 9]:
-    rank, step, src, cls, seg_len, q_a, q_b, kv_a, kv_b (-1 where a rank has
-    a single segment). Same row order as ``ring_schedule``."""
+    rank, step, src, cls, L (the padded segment length), q_a, q_b, kv_a, kv_b
+    (segment starts; -1 where a rank has a single segment). Same row order as
+    ``ring_schedule``."""
+    L = segment_length(S, P, order)
     rows = []
     for e in ring_schedule(S, P, causal, order):
         q = [s for s, _ in e["q"]] + [-1] * (2 - len(e["q"]))
         kv = [s for s, _ in e["kv"]] + [-1] * (2 - len(e["kv"]))
-        rows.append([e["rank"], e["step"], e["src"], e["cls"], e["q"][0][1],
+        rows.append([e["rank"], e["step"], e["src"], e["cls"], L,
                      q[0], q[1], kv[0], kv[1]])
     return np.asarray(rows, dtype=np.int32)
 
@@ -118,7 +130,8 @@ def tile_visits(S, P, causal, order, tile):
     """Expected key-tile visits of a tiled kernel, per query tile.
 
     Every segment is cut into tiles of ``tile`` rows (the last one shorter if
-    the segment length is not a multiple). Tiles are numbered globally:
+    the segment length is not a multiple; tiles at or past S are empty and
+    visit nothing, and tiles are clipped at S). Tiles are numbered globally:
     segment index g in position order times tiles-per-segment plus the tile
     index inside the segment. For the query tile (g, i) owned by rank r, the
     visits are, in order: for t = 0..P-1, src = (r - t) mod P, for each
@@ -129,7 +142,7 @@ def tile_visits(S, P, causal, order, tile):
     Returns a list indexed by query tile id of lists of 4-tuples.
     """
     flat = segments_in_position_order(S, P, order)
-    seg_len = flat[0][1]
+    seg_len = segment_length(S, P, order)
     nt = -(-seg_len // tile)
     seg_index = {s: g for g, (s, _, _) in enumerate(flat)}
     segs = rank_segments(S, P, order)
@@ -139,7 +152,7 @@ def tile_visits(S, P, causal, order, tile):
         res = []
         for i in range(nt):
             lo = start + i * tile
-            n = min(tile, start + seg_len - lo)
+            n = max(0, min(tile, start + seg_len - lo, S - lo))
             res.append((g * nt + i, lo, n))
         return res
 
@@ -151,6 +164,8 @@ def tile_visits(S, P, causal, order, tile):
                 src = (r - t) % P
                 for kv_start, _ in segs[src]:
                     for kid, klo, kn in tiles_of(kv_start):
+                        if qn <= 0 or kn <= 0:
+                            continue
                         c = classify([(qlo, qn)], [(klo, kn)], causal)
                         if c != SKIP:
                             seq.append((t, src, kid, c))

@@ -248,12 +248,11 @@ def test_rows_and_partial_match_full():
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("order", [0, 1])
 @pytest.mark.parametrize("P", [1, 2, 4, 8])
-def test_ring_equals_full_attention(causal, order, P):
-    B, S, Hq, Hkv, D = 1, 48, 4, 2, 8
+@pytest.mark.parametrize("S", [48, 45])          # 45: uneven chunks, padded
+def test_ring_equals_full_attention(causal, order, P, S):
+    B, Hq, Hkv, D = 1, 4, 2, 8
     q = _rand((B, S, Hq, D), 30)
     k, v = _rand((B, S, Hkv, D), 31), _rand((B, S, Hkv, D), 32)
-    if order == 1 and S % (2 * P):
-        pytest.skip("zig-zag needs S % 2P == 0")
     o1, l1 = attention_naive(q, k, v, causal, 0.35)
     o2, l2 = ring_attention(q, k, v, causal, 0.35, P, order)
     np.testing.assert_allclose(o2, o1, rtol=0, atol=TOL)
@@ -335,17 +334,21 @@ def _pairs(ranges_q, ranges_k):
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("order", [0, 1])
-@pytest.mark.parametrize("S,P", [(16, 2), (48, 4), (64, 8), (24, 3)])
+@pytest.mark.parametrize("S,P", [(16, 2), (48, 4), (64, 8), (24, 3), (10, 4), (7, 3),
+                                 (5, 4), (3, 8)])
 def test_schedule_covers_every_pair_once(S, P, causal, order):
-    if order == 1 and S % (2 * P):
-        pytest.skip("zig-zag needs S % 2P == 0")
     segs = rank_segments(S, P, order)
+    parts = P if order == 0 else 2 * P
+    L = -(-S // parts)                       # padded to a multiple of the split
     owner = np.full(S, -1)
+    starts = []
     for r, lst in enumerate(segs):
         for s, n in lst:
-            assert n == (S // P if order == 0 else S // (2 * P))
+            assert s % L == 0 and n == max(0, min(L, S - s))
+            starts.append(s)
             assert np.all(owner[s:s + n] == -1)
             owner[s:s + n] = r
+    assert sorted(starts) == [i * L for i in range(parts)]
     assert np.all(owner >= 0)
     count = np.zeros((S, S), int)
     for e in ring_schedule(S, P, causal, order):
@@ -366,20 +369,18 @@ def test_schedule_covers_every_pair_once(S, P, causal, order):
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("order", [0, 1])
 @pytest.mark.parametrize("S,P,T", [(64, 2, 8), (96, 4, 5), (40, 2, 16),
-                                   (128, 8, 4)])
+                                   (128, 8, 4), (50, 4, 4), (37, 2, 5), (9, 4, 2)])
 def test_tile_visits_by_brute_force(S, P, T, causal, order):
-    if order == 1 and S % (2 * P):
-        pytest.skip("zig-zag needs S % 2P == 0")
     visits = tile_visits(S, P, causal, order, T)
     segs = sorted((s, n, r) for r, lst in enumerate(rank_segments(S, P, order))
                   for s, n in lst)
-    L = segs[0][1]
+    L = -(-S // (P if order == 0 else 2 * P))
     nt = -(-L // T)
 
     def tile_range(tid):
         g, i = divmod(tid, nt)
         lo = segs[g][0] + i * T
-        return lo, min(T, segs[g][0] + L - lo), segs[g][2]
+        return lo, max(0, min(T, segs[g][0] + L - lo, S - lo)), segs[g][2]
 
     covered = np.zeros((S, S), int)
     for qid, seq in enumerate(visits):

@@ -134,8 +134,9 @@ def test_grouped_heads_equal_repeated_heads():
 @pytest.mark.parametrize("P,order", [(1, ORDER_CONTIGUOUS), (2, ORDER_ZIGZAG),
                                      (4, ORDER_CONTIGUOUS), (4, ORDER_ZIGZAG)])
 @pytest.mark.parametrize("causal", [False, True])
-def test_ring_restatement_equals_definition(P, order, causal):
-    B, S, H_q, H_kv, D = 1, 48, 2, 1, 6
+@pytest.mark.parametrize("S", [48, 45])          # 45: uneven chunks, padded
+def test_ring_restatement_equals_definition(P, order, causal, S):
+    B, H_q, H_kv, D = 1, 2, 1, 6
     q = _rand((B, S, H_q, D), 21)
     k, v = _rand((B, S, H_kv, D), 22), _rand((B, S, H_kv, D), 23)
     dout = _rand((B, S, H_q, D), 24)
