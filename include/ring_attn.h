@@ -13,10 +13,14 @@
  *    Balancing"): partial results are combined with an exact log-sum-exp
  *    merge; the zig-zag chunk order (2P halves, rank r owns halves r and
  *    2P-1-r) balances causal work across ranks.
- * Divisibility follows the nvFuser PR "Transformer sequence parallel
- * forward" (a sequence-parallel case with s % d != 0 is skipped) and the
- * mvp-engine "sequence-parallel" skill (seq_len divisible by the split, else
- * pad explicitly): S % P != 0, or S % 2P != 0 in zig-zag order, is an error.
+ * Uneven lengths follow the mvp-engine "sequence-parallel" skill (seq_len
+ * divisible by the split, else pad explicitly and mask): the sequence counts
+ * as padded to the next multiple of P (contiguous) or 2P (zig-zag), every
+ * chunk (half) spans L = ceil(S/P) (ceil(S/2P)) positions starting at a
+ * multiple of L, and the padding positions (S and beyond) hold no token:
+ * they are never read, never written and never attended to. A trailing
+ * chunk can therefore be short or empty. The padding is virtual; tensors
+ * keep exactly S rows.
  *
  * For each batch b, query head h and query position i, with key/value head
  * hk = h / (H_q / H_kv) and allowed keys A(i) = {0..S-1} (non-causal) or
@@ -60,7 +64,7 @@ extern "C" {
 typedef enum {
   RA_OK = 0,
   RA_ERR_NULL = 1,     /* a required pointer is NULL                              */
-  RA_ERR_SHAPE = 2,    /* size <= 0, S % P, S % 2P (zig-zag), H_q % H_kv, n range */
+  RA_ERR_SHAPE = 2,    /* a size <= 0, H_q % H_kv != 0, merge n out of range       */
   RA_ERR_HEADDIM = 3,  /* D is not 64 or 128                                       */
   RA_ERR_ALIGN = 4,    /* a data pointer is not 16-byte aligned                    */
   RA_ERR_DTYPE = 5,    /* unknown dtype or order value                             */
@@ -247,7 +251,8 @@ ra_status attn_lse_merge_n(const void* const* o, const float* const* lse,
  * ring_attn_plan - the ring schedule as an int32 table, host only.
  * One row of RA_PLAN_COLS ints per (rank, step), rank-major then step:
  *   rank, step, src = (rank - step) mod P, class of the whole (query chunk,
- *   key chunk) pair, segment length, first and second query segment starts,
+ *   key chunk) pair, segment length L (padded, see above), first and second
+ *   query segment starts,
  *   first and second key segment starts (-1 where a rank owns one segment).
  * `table_len` is the capacity in ints (>= P*P*RA_PLAN_COLS, else
  * RA_ERR_BUFFER). Never touches the GPU.

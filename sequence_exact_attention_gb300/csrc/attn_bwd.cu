@@ -144,7 +144,7 @@ bwd_prep_kernel(const Geometry g, const __nv_bfloat16* __restrict__ out,
   const int bh = (int)(rest / g.n_seg);
   const int b = bh / g.H_q, h = bh % g.H_q;
   const int in_seg = ti * kT + row;
-  const bool valid = in_seg < g.seg_len;
+  const bool valid = in_seg < seg_tokens(g, seg);
   const int pos = seg * g.seg_len + in_seg;
   float acc = 0.f;
   if (valid) {
@@ -184,30 +184,34 @@ struct QTile {
 };
 
 struct QIter {
-  int h, h_end, t, r, which, ti, src, kv_lo, kv_hi;
+  int h, h_end, t, r, which, ti, ti_end, len, src, kv_lo, kv_hi;
 
   __device__ __forceinline__ void start_segment(const Geometry& g) {
-    const int s0 = rank_seg(g, r, which) * g.seg_len;
+    const int seg = rank_seg(g, r, which);
+    const int s0 = seg * g.seg_len;
+    len = seg_tokens(g, seg);
+    ti_end = (len + kT - 1) / kT;               // tiles holding tokens
     if (!g.causal || kv_lo <= s0) ti = 0;
-    else if (s0 + g.seg_len - 1 < kv_lo) ti = g.nt;
+    else if (s0 + len - 1 < kv_lo) ti = ti_end;
     else ti = (kv_lo - s0) / kT;
   }
   __device__ __forceinline__ void init(const Geometry& g, int src_, int kv_lo_, int kv_valid,
                                        int h_begin, int h_end_) {
-    h = h_begin; h_end = h_end_;
+    h = h_begin;
+    h_end = kv_valid > 0 ? h_end_ : h_begin;   // a key tile of padding only: no visit
     src = src_; t = 0; r = src_; which = 0;
     kv_lo = kv_lo_; kv_hi = kv_lo_ + kv_valid - 1;
     start_segment(g);
   }
   __device__ __forceinline__ bool next(const Geometry& g, QTile& o) {
     while (h < h_end) {
-      if (ti < g.nt) {
+      if (ti < ti_end) {
         const int seg = rank_seg(g, r, which);
         o.h = h;
         o.seg = seg;
         o.ti = ti;
         o.lo = seg * g.seg_len + ti * kT;
-        o.valid = min(kT, g.seg_len - ti * kT);
+        o.valid = min(kT, len - ti * kT);
         o.mask = g.causal && kv_hi > o.lo;
         ++ti;
         return true;
@@ -280,7 +284,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int kseg = kt / g.nt, kti = kt % g.nt;
   const int src = seg_owner(g, kseg);
   const int kv_lo = kseg * g.seg_len + kti * kT;
-  const int kv_valid = min(kT, g.seg_len - kti * kT);
+  const int kv_valid = tile_tokens(g, kseg, kti);   // <= 0: padding only
   const int h0 = hk * grp;
 
   init_barriers<C>(bar, abort_flag, never);
@@ -535,7 +539,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int ti = qt % g.nt;
   const int r = seg_owner(g, seg);
   const int q_lo = seg * g.seg_len + ti * kT;
-  const int q_valid = min(kT, g.seg_len - ti * kT);
+  const int q_valid = tile_tokens(g, seg, ti);      // <= 0: padding only
 
   init_barriers<C>(bar, abort_flag, never);
   if (warp == kMmaWarp) {

@@ -54,7 +54,7 @@ attn_simt_kernel(const Geometry g, const float* __restrict__ q,
   const int qid = n_qt - 1 - blockIdx.x / BH;    // later positions first
   const int seg = qid / g.nt, ti = qid % g.nt;
   const int q_lo = seg * g.seg_len + ti * kRows;
-  const int q_valid = min(kRows, g.seg_len - ti * kRows);
+  const int q_valid = tile_tokens(g, seg, ti);     // <= 0: a tile of padding only
   const int r = seg_owner(g, seg);
   const int b = bh / g.H_q, h = bh % g.H_q;
   const int hk = h / (g.H_q / g.H_kv);

@@ -227,7 +227,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int ti = qt % g.nt;
   const int r = seg_owner(g, seg);
   const int q_lo = seg * g.seg_len + ti * kTile;
-  const int q_valid = min(kTile, g.seg_len - ti * kTile);
+  const int q_valid = tile_tokens(g, seg, ti);     // <= 0: a tile of padding only
 
   // ---- set-up: barriers, abort flag, TMEM
   if (threadIdx.x == 0) {

@@ -25,14 +25,14 @@ ra_status make_geometry(int B, int H_q, int H_kv, int S, int D, int P,
   if (H_q % H_kv != 0) return RA_ERR_SHAPE;
   if (order != RA_ORDER_CONTIGUOUS && order != RA_ORDER_ZIGZAG) return RA_ERR_DTYPE;
   const int parts = order == RA_ORDER_ZIGZAG ? 2 * P : P;
-  if (S % parts != 0) return RA_ERR_SHAPE;
   if (step < -1 || step >= P) return RA_ERR_RANGE;
   g->B = B; g->H_q = H_q; g->H_kv = H_kv; g->S = S; g->D = D; g->P = P;
   g->causal = causal ? 1 : 0;
   g->order = order;
   g->step = step;
   g->n_seg = parts;
-  g->seg_len = S / parts;
+  // S counts as padded to a multiple of `parts`; the padding holds no token
+  g->seg_len = (S + parts - 1) / parts;
   g->segs_per_rank = order == RA_ORDER_ZIGZAG ? 2 : 1;
   g->tile = tile;
   g->nt = (g->seg_len + tile - 1) / tile;
@@ -88,16 +88,21 @@ int rank_segment_starts(int r, int P, int order, int seg_len, int out[2]) {
 }
 
 // Class of all pairs (query in any q segment, key in any kv segment) under
-// the causal rule key <= query. One q range [a, a+L) and one kv range
-// [c, c+L): all pairs allowed iff c+L-1 <= a; none iff c > a+L-1.
-int classify_segments(const int* qs, int nq, const int* ks, int nk, int L,
+// the causal rule key <= query. Segments start at multiples of L and hold
+// their positions below S. One q range [a, a+n) and one kv range [c, c+m):
+// all pairs allowed iff c+m-1 <= a; none iff c > a+n-1. Empty ranges hold no
+// pair.
+int classify_segments(const int* qs, int nq, const int* ks, int nk, int L, int S,
                       int causal) {
   if (!causal) return RA_CLASS_FULL;
   bool all_full = true, all_skip = true;
   for (int i = 0; i < nq; ++i)
     for (int j = 0; j < nk; ++j) {
-      if (!(ks[j] + L - 1 <= qs[i])) all_full = false;
-      if (!(ks[j] > qs[i] + L - 1)) all_skip = false;
+      const int n = S - qs[i] < L ? S - qs[i] : L;
+      const int m = S - ks[j] < L ? S - ks[j] : L;
+      if (n <= 0 || m <= 0) continue;
+      if (!(ks[j] + m - 1 <= qs[i])) all_full = false;
+      if (!(ks[j] > qs[i] + n - 1)) all_skip = false;
     }
   if (all_skip) return RA_CLASS_SKIP;
   if (all_full) return RA_CLASS_FULL;
@@ -114,9 +119,8 @@ ra_status ring_attn_plan(int S, int P, int causal, int order, int* table,
   if (S <= 0 || P <= 0) return RA_ERR_SHAPE;
   if (order != RA_ORDER_CONTIGUOUS && order != RA_ORDER_ZIGZAG) return RA_ERR_DTYPE;
   const int parts = order == RA_ORDER_ZIGZAG ? 2 * P : P;
-  if (S % parts != 0) return RA_ERR_SHAPE;
   if ((size_t)P * (size_t)P * RA_PLAN_COLS > table_len) return RA_ERR_BUFFER;
-  const int L = S / parts;
+  const int L = (S + parts - 1) / parts;     // S padded to a multiple of parts
   int* row = table;
   for (int r = 0; r < P; ++r) {
     int qs[2] = {-1, -1};
@@ -128,7 +132,7 @@ ra_status ring_attn_plan(int S, int P, int causal, int order, int* table,
       row[0] = r;
       row[1] = t;
       row[2] = src;
-      row[3] = classify_segments(qs, nq, ks, nk, L, causal);
+      row[3] = classify_segments(qs, nq, ks, nk, L, S, causal);
       row[4] = L;
       row[5] = qs[0];
       row[6] = nq > 1 ? qs[1] : -1;
@@ -164,7 +168,7 @@ const char* ring_attn_strerror(int status) {
   switch (status) {
     case RA_OK: return "ok";
     case RA_ERR_NULL: return "a required pointer is NULL";
-    case RA_ERR_SHAPE: return "invalid shape (sizes must be positive; S divisible by P, or by 2P in zig-zag order; H_q divisible by H_kv)";
+    case RA_ERR_SHAPE: return "invalid shape (sizes must be positive; H_q divisible by H_kv)";
     case RA_ERR_HEADDIM: return "unsupported head dimension (D must be 64 or 128)";
     case RA_ERR_ALIGN: return "misaligned pointer (tensors need 16-byte alignment, lse/log/status 4-byte)";
     case RA_ERR_DTYPE: return "unknown dtype or chunk order";

@@ -26,6 +26,19 @@ __device__ __forceinline__ int rank_seg(const Geometry& g, int r, int which) {
   return which == 0 ? r : 2 * g.P - 1 - r;
 }
 
+// Tokens of segment `seg`: its seg_len positions clipped at S. When S is not
+// a multiple of the split the sequence counts as padded to one, and the
+// padding positions (S and beyond) hold no token: a trailing segment can be
+// short or empty.
+__device__ __forceinline__ int seg_tokens(const Geometry& g, int seg) {
+  return max(0, min(g.seg_len, g.S - seg * g.seg_len));
+}
+
+// Rows of tile `ti` of segment `seg`; <= 0 for a tile that holds no token.
+__device__ __forceinline__ int tile_tokens(const Geometry& g, int seg, int ti) {
+  return min(g.tile, seg_tokens(g, seg) - ti * g.tile);
+}
+
 struct KvTile {
   int step;     // ring step t
   int src;      // rank the block started on
@@ -51,14 +64,14 @@ struct KvIter {
   int which;       // segment of src being walked (0 or 1)
   int lo;          // first position of the next tile
   int id;          // id of the next tile
-  int rem;         // rows of the current segment from `lo` on
+  int rem;         // tokens of the current segment from `lo` on
   int q_lo, q_hi;  // the query tile's first and last valid position
 
   __device__ __forceinline__ void start_segment(const Geometry& g) {
     const int seg = rank_seg(g, src, which);
     lo = seg * g.seg_len;
     id = seg * g.nt;
-    rem = g.seg_len;
+    rem = seg_tokens(g, seg);
   }
 
   __device__ __forceinline__ void init(const Geometry& g, int r, int q_first, int q_valid) {

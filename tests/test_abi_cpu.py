@@ -51,14 +51,10 @@ def test_strerror_covers_every_status(lib):
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("order", ["contiguous", "zigzag"])
 @pytest.mark.parametrize("S,P", [(8, 2), (256, 4), (4096, 8), (32768, 8),
-                                 (131072, 16), (96, 3), (16, 16), (7, 7)])
+                                 (131072, 16), (96, 3), (16, 16), (7, 7),
+                                 (1001, 4), (5, 4), (3, 8), (700, 3)])   # last four uneven
 def test_plan_matches_oracle_schedule(S, P, causal, order):
     o = oracle.ORDER_ZIGZAG if order == "zigzag" else oracle.ORDER_CONTIGUOUS
-    if order == "zigzag" and S % (2 * P):
-        with pytest.raises(binding.RingAttnError) as e:
-            binding.ring_attn_plan(S, P, causal, order)
-        assert e.value.status == RA_ERR_SHAPE
-        return
     got = binding.ring_attn_plan(S, P, causal, order)
     want = oracle.schedule_table(S, P, causal, o)
     np.testing.assert_array_equal(got, want)
@@ -68,7 +64,7 @@ def test_plan_rejects_small_buffer_and_bad_args(lib):
     buf = (ctypes.c_int * 10)()
     assert lib.ring_attn_plan(8, 2, 1, 0, buf, 10) == RA_ERR_BUFFER
     assert lib.ring_attn_plan(8, 2, 1, 0, None, 100) == RA_ERR_NULL
-    assert lib.ring_attn_plan(9, 2, 1, 0, buf, 10) == RA_ERR_SHAPE
+    assert lib.ring_attn_plan(0, 2, 1, 0, buf, 10) == RA_ERR_SHAPE
     assert lib.ring_attn_plan(8, 0, 1, 0, buf, 10) == RA_ERR_SHAPE
     assert lib.ring_attn_plan(8, 2, 1, 7, buf, 10) == RA_ERR_DTYPE
 
@@ -105,8 +101,7 @@ def test_fwd_argument_errors(lib):
     assert _fwd(lib, B=0) == RA_ERR_SHAPE
     assert _fwd(lib, S=0) == RA_ERR_SHAPE
     assert _fwd(lib, S=-5) == RA_ERR_SHAPE
-    assert _fwd(lib, S=250) == RA_ERR_SHAPE               # S % P
-    assert _fwd(lib, S=260, order=1) == RA_ERR_SHAPE      # S % 2P
+    assert _fwd(lib, S=250, Hq=3) == RA_ERR_SHAPE         # uneven S is valid; H_q % H_kv is not
     assert _fwd(lib, Hq=3, Hkv=2) == RA_ERR_SHAPE
     assert _fwd(lib, P=0) == RA_ERR_SHAPE
     assert _fwd(lib, D=96) == RA_ERR_HEADDIM
@@ -157,7 +152,9 @@ def test_bwd_workspace_size(lib):
     st, n = _ws_bytes(lib, B=1, Hq=1, S=512, D=64, P=2, order=1)  # 4 halves of 128: 1 tile
     assert st == RA_OK and n == 2 * (4 * 1 * 128) * 4
     assert _ws_bytes(lib, D=96)[0] == RA_ERR_HEADDIM
-    assert _ws_bytes(lib, S=250)[0] == RA_ERR_SHAPE
+    st, n = _ws_bytes(lib, S=250, P=4)                            # uneven: chunks of 63, 1 tile
+    assert st == RA_OK and n == 2 * (2 * 4 * 1 * 128) * 4
+    assert _ws_bytes(lib, S=0)[0] == RA_ERR_SHAPE
     assert _ws_bytes(lib, order=3)[0] == RA_ERR_DTYPE
     assert lib.ring_attn_bwd_workspace(1, 2, 256, 64, 4, 0, None) == RA_ERR_NULL
 
@@ -174,7 +171,7 @@ def _bwd(lib, q=A, k=A, v=A, out=A, lse=A, dout=A, dq=A, dk=A, dv=A, B=1, Hq=2, 
 def test_bwd_argument_errors(lib):
     for name in ("q", "out", "lse", "dout", "dq", "dk", "dv", "ws"):
         assert _bwd(lib, **{name: 0}) == RA_ERR_NULL, name
-    assert _bwd(lib, S=250) == RA_ERR_SHAPE
+    assert _bwd(lib, S=0) == RA_ERR_SHAPE
     assert _bwd(lib, Hq=3, Hkv=2) == RA_ERR_SHAPE
     assert _bwd(lib, D=96) == RA_ERR_HEADDIM
     assert _bwd(lib, dtype=1) == RA_ERR_DTYPE              # bf16 only

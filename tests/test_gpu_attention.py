@@ -60,6 +60,12 @@ BF16_CASES = [
     (2, 4, 1, 1024, 64, 4, True, "zigzag"),        # MQA, D=64
     (1, 2, 2, 1536, 128, 4, False, "zigzag"),      # non-causal zig-zag
     (1, 2, 2, 130, 128, 2, True, "contiguous"),    # S not a multiple of 128
+    # uneven lengths: S padded to a multiple of the split, padding masked
+    (1, 3, 3, 1000, 128, 3, True, "contiguous"),   # chunks of 334 (last 332 tokens)
+    (1, 2, 2, 1001, 128, 4, True, "zigzag"),       # halves of 126 (last 119)
+    (2, 4, 2, 300, 64, 8, True, "zigzag"),         # halves of 19 (last 15)
+    (1, 2, 2, 5, 128, 4, True, "contiguous"),      # chunks of 2: the last is empty
+    (1, 2, 1, 700, 128, 3, False, "zigzag"),       # non-causal, halves of 117
 ]
 
 
@@ -86,6 +92,8 @@ F32_CASES = [
     (2, 4, 2, 384, 128, 3, True, "zigzag"),        # halves of 64
     (1, 2, 1, 200, 64, 2, True, "contiguous"),     # chunks of 100 (64+36)
     (1, 2, 2, 24, 128, 12, True, "zigzag"),        # one-token halves
+    (1, 2, 2, 250, 64, 4, True, "contiguous"),     # uneven: chunks of 63 (last 61)
+    (1, 2, 2, 99, 128, 4, True, "zigzag"),         # uneven: halves of 13 (last 8)
 ]
 
 
@@ -126,10 +134,11 @@ def test_result_does_not_depend_on_P(dtype):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("order", ["contiguous", "zigzag"])
-def test_single_steps_merge_to_full(dtype, order):
+@pytest.mark.parametrize("S", [768, 700])      # 700: uneven chunks
+def test_single_steps_merge_to_full(dtype, order, S):
     """Each ring step alone gives the oracle's per-step partial; folding the
     partials with the merge kernel gives full attention."""
-    S, P = 768, 3
+    P = 3
     w, q, k, v = _inputs(dtype, 1, 4, 2, S, 64, P, True, order, seed=91)
     want_o, want_l, parts = oracle.ring_attention(q, k, v, True, w.scale, P,
                                                   ORDER[order], return_partials=True)
@@ -191,7 +200,7 @@ def test_errors_raise_and_launch_nothing():
     dev = torch.device("cuda")
     q = torch.zeros(1, 100, 2, 128, dtype=torch.bfloat16, device=dev)
     with pytest.raises(binding.RingAttnError) as e:
-        binding.ring_attn_fwd(q, q, q, 3, True)          # 100 % 3
+        binding.ring_attn_fwd(q[:, :, :1].contiguous(), q, q, 2, True)   # H_q % H_kv
     assert e.value.status == 2
     with pytest.raises(binding.RingAttnError) as e:
         binding.ring_attn_fwd(q, q, q, 2, True, order="zigzag", step=5)

@@ -64,6 +64,9 @@ CASES = [
     ("s600_ragged_zigzag", 1, 2, 2, 600, 128, 4, True, "zigzag"),     # halves of 75 rows
     ("s1000_ragged_d64", 2, 2, 2, 1000, 64, 2, True, "contiguous"),   # 500 = 3 x 128 + 116
     ("s256_p1_noncausal", 1, 3, 3, 256, 128, 1, False, "contiguous"),
+    ("s1001_uneven_zigzag", 1, 2, 2, 1001, 128, 4, True, "zigzag"),   # halves of 126
+    ("s5_uneven_empty_chunk", 1, 2, 1, 5, 64, 4, True, "contiguous"),  # last chunk empty
+    ("s700_uneven_noncausal", 1, 2, 2, 700, 128, 3, False, "zigzag"),
 ]
 
 
