@@ -22,6 +22,8 @@ Everything here is float64 NumPy, written to be read against the pages:
   forward definition (same glossary, §Implementation Considerations: the
   backward pass runs over the same ring); ``ring_attention_backward``
   restates it per (rank, step); ``backward_rows`` evaluates sampled rows.
+* ``attention_varlen`` / ``attention_backward_varlen`` - packed batches of
+  sequences of different lengths, each its own problem.
 * ``tile_visits``       - expands the chunk-level schedule into the sequence of
   fixed-size key tiles a tiled kernel must visit, classifying every tile by
   brute force over its (query, key) pairs.
@@ -40,6 +42,7 @@ from .schedule import (
 )
 from .ring import ring_attention
 from .backward import attention_backward, ring_attention_backward, backward_rows
+from .varlen import attention_varlen, attention_backward_varlen
 
 __all__ = [
     "attention_naive", "attention_rows", "partial_attention",
@@ -48,4 +51,5 @@ __all__ = [
     "rank_segments", "ring_schedule", "schedule_table", "tile_visits",
     "ring_attention",
     "attention_backward", "ring_attention_backward", "backward_rows",
+    "attention_varlen", "attention_backward_varlen",
 ]
