@@ -129,6 +129,33 @@ ra_status ring_attn_fwd_ex(const void* q, const void* k, const void* v,
                            int* visit_log, int* dev_status, void* stream);
 
 /*
+ * ring_attn_fwd_varlen - ring attention over a batch of packed sequences of
+ * different lengths.
+ *
+ * Sequence b occupies rows [cu_seqlens[b], cu_seqlens[b+1]) of the packed
+ * tensors and is its own ring problem: its S_b tokens are cut into P chunks
+ * (or 2P halves) of ceil(S_b / P) (ceil(S_b / 2P)) positions, padded like an
+ * uneven S (see above), and its queries attend only to its own keys. Layouts:
+ *     q, out   [total, H_q,  D]      k, v   [total, H_kv, D]
+ *     lse      [H_q, total]          float32 (may be NULL)
+ * cu_seqlens: DEVICE int32 array of n_seq + 1 nondecreasing offsets with
+ * cu_seqlens[0] = 0 and cu_seqlens[n_seq] = total. max_seqlen >= every S_b
+ * (it sizes the launch). The kernels clamp offsets into [0, total] and
+ * lengths into [0, max_seqlen], so a malformed array never moves an access
+ * outside the tensors (its sequences are then simply wrong). A sequence of
+ * length 0 writes nothing. dtype RA_BF16 or RA_F32; all steps; no visit log.
+ * Errors: RA_ERR_NULL, RA_ERR_SHAPE (n_seq, total or max_seqlen <= 0,
+ * H_q % H_kv), RA_ERR_HEADDIM, RA_ERR_ALIGN (cu_seqlens 4-byte), RA_ERR_DTYPE,
+ * RA_ERR_RANGE, RA_ERR_DEVICE, RA_ERR_LAUNCH.
+ */
+ra_status ring_attn_fwd_varlen(const void* q, const void* k, const void* v,
+                               void* out, float* lse, const int* cu_seqlens,
+                               int n_seq, int total, int max_seqlen,
+                               int H_q, int H_kv, int D, int P, int causal,
+                               float scale, int dtype, int order,
+                               int* dev_status, void* stream);
+
+/*
  * ring_attn_visit_log_len - size of the visit log of ring_attn_fwd_ex.
  *
  * The kernel for `dtype` cuts every chunk (contiguous) or half (zig-zag) of
@@ -217,6 +244,22 @@ ra_status ring_attn_bwd_ex(const void* q, const void* k, const void* v,
                            int causal, float scale, int dtype, int order,
                            void* workspace, size_t workspace_bytes, int phases,
                            int* dev_status, void* stream);
+
+/*
+ * ring_attn_bwd_varlen - ring_attn_bwd for packed sequences, with the
+ * layouts and cu_seqlens / max_seqlen conventions of ring_attn_fwd_varlen
+ * (dout, dq like q; dk, dv like k; lse [H_q, total]). The workspace size is
+ * ring_attn_bwd_workspace(n_seq, H_q, max_seqlen, D, P, order, ...).
+ * bf16 only. Errors: as ring_attn_fwd_varlen, plus RA_ERR_BUFFER.
+ */
+ra_status ring_attn_bwd_varlen(const void* q, const void* k, const void* v,
+                               const void* out, const float* lse, const void* dout,
+                               void* dq, void* dk, void* dv, const int* cu_seqlens,
+                               int n_seq, int total, int max_seqlen,
+                               int H_q, int H_kv, int D, int P, int causal,
+                               float scale, int dtype, int order,
+                               void* workspace, size_t workspace_bytes,
+                               int* dev_status, void* stream);
 
 /*
  * attn_lse_merge - exact merge of two partial attention results over

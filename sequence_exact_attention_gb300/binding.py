@@ -23,6 +23,7 @@ MERGE_MAX_N = 16
 
 # every entry point declared in include/ring_attn.h
 EXPORTS = ("ring_attn_fwd", "ring_attn_fwd_ex", "ring_attn_visit_log_len",
+           "ring_attn_fwd_varlen", "ring_attn_bwd_varlen",
            "ring_attn_bwd_workspace", "ring_attn_bwd", "ring_attn_bwd_ex",
            "attn_lse_merge", "attn_lse_merge_n", "ring_attn_plan",
            "ring_attn_expiry_test", "ring_attn_strerror", "ring_attn_version")
@@ -64,6 +65,12 @@ def load():
     lib.ring_attn_bwd_ex.restype = c_int
     lib.ring_attn_bwd_ex.argtypes = ([vp] * 9 + [c_int] * 7 + [c_float, c_int, c_int, vp,
                                                                 ctypes.c_size_t, c_int, vp, vp])
+    lib.ring_attn_fwd_varlen.restype = c_int
+    lib.ring_attn_fwd_varlen.argtypes = ([vp] * 6 + [c_int] * 8 + [c_float, c_int, c_int,
+                                                                   vp, vp])
+    lib.ring_attn_bwd_varlen.restype = c_int
+    lib.ring_attn_bwd_varlen.argtypes = ([vp] * 10 + [c_int] * 8 + [c_float, c_int, c_int, vp,
+                                                                    ctypes.c_size_t, vp, vp])
     lib.attn_lse_merge.restype = c_int
     lib.attn_lse_merge.argtypes = [vp] * 6 + [c_int] * 5 + [vp]
     lib.attn_lse_merge_n.restype = c_int
@@ -251,6 +258,65 @@ def ring_attn_bwd(q, k, v, out, lse, dout, P, causal, scale=None, order="contigu
     else:
         st = lib.ring_attn_bwd_ex(*args, int(phases), _ptr(dev_status), _stream(stream))
     _check(st, "ring_attn_bwd")
+    return dq, dk, dv
+
+
+def _varlen_args(q, k, cu_seqlens, max_seqlen):
+    for t, n in ((q, "q"), (k, "k"), (cu_seqlens, "cu_seqlens")):
+        _dev(t, n)
+    import torch
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    total, H_q, D = q.shape
+    H_kv = k.shape[1]
+    if k.shape != (total, H_kv, D):
+        raise ValueError("k and v must be [total, H_kv, D] matching q")
+    return total, H_q, H_kv, D, cu_seqlens.numel() - 1, int(max_seqlen)
+
+
+def ring_attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, P, causal, scale=None,
+                         order="contiguous", out=None, lse=None, dev_status=None,
+                         stream=None):
+    """Ring attention of packed sequences: q [total,H_q,D], k/v [total,H_kv,D],
+    cu_seqlens int32 [n+1] (CUDA). Returns (out [total,H_q,D], lse [H_q,total])."""
+    import torch
+    lib = load()
+    _dev(v, "v")
+    total, H_q, H_kv, D, n, mx = _varlen_args(q, k, cu_seqlens, max_seqlen)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(H_q, total, device=q.device, dtype=torch.float32)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    st = lib.ring_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                  _ptr(cu_seqlens), n, total, mx, H_q, H_kv, D, P,
+                                  int(bool(causal)), sc, _dtype_code(q.dtype), ORDERS[order],
+                                  _ptr(dev_status), _stream(stream))
+    _check(st, "ring_attn_fwd_varlen")
+    return out, lse
+
+
+def ring_attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens, max_seqlen, P, causal,
+                         scale=None, order="contiguous", workspace=None, dev_status=None,
+                         stream=None):
+    """Gradients (dq, dk, dv) of ``ring_attn_fwd_varlen`` for the upstream dout."""
+    import torch
+    lib = load()
+    for t, nm in ((v, "v"), (out, "out"), (lse, "lse"), (dout, "dout")):
+        _dev(t, nm)
+    total, H_q, H_kv, D, n, mx = _varlen_args(q, k, cu_seqlens, max_seqlen)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = bwd_workspace_bytes(n, H_q, mx, D, P, order)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    st = lib.ring_attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens), n, total, mx,
+                                  H_q, H_kv, D, P, int(bool(causal)), sc, _dtype_code(q.dtype),
+                                  ORDERS[order], _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(),
+                                  _ptr(dev_status), _stream(stream))
+    _check(st, "ring_attn_bwd_varlen")
     return dq, dk, dv
 
 

@@ -154,6 +154,70 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
                           dev_status, stream);
 }
 
+ra_status ring_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
+                               float* lse, const int* cu_seqlens, int n_seq, int total,
+                               int max_seqlen, int H_q, int H_kv, int D, int P, int causal,
+                               float scale, int dtype, int order, int* dev_status,
+                               void* stream) {
+  if (!cu_seqlens) return RA_ERR_NULL;
+  if (n_seq <= 0 || total <= 0 || max_seqlen <= 0) return RA_ERR_SHAPE;
+  if (!aligned(cu_seqlens, 4)) return RA_ERR_ALIGN;
+  ra_status st = check_attn_args(q, k, v, out, lse, 1, H_q, H_kv, total, D, dtype, -1,
+                                 nullptr, dev_status);
+  if (st != RA_OK) return st;
+  if ((long long)n_seq * max_seqlen * H_q > kMaxElems) return RA_ERR_RANGE;
+  Geometry g;
+  st = make_geometry(n_seq, H_q, H_kv, max_seqlen, D, P, causal, scale, order, -1,
+                     tile_rows_for(dtype, D), &g);
+  if (st != RA_OK) return st;
+  g.cu_seqlens = cu_seqlens;
+  g.total = total;
+  int sms = 0;
+  st = check_device(&sms);
+  if (st != RA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == RA_F32)
+    return launch_attn_simt_varlen(g, static_cast<const float*>(q),
+                                   static_cast<const float*>(k), static_cast<const float*>(v),
+                                   static_cast<float*>(out), lse, s);
+  return launch_attn_tc_varlen(g, q, k, v, out, lse, dev_status, s);
+}
+
+ra_status ring_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* out,
+                               const float* lse, const void* dout, void* dq, void* dk,
+                               void* dv, const int* cu_seqlens, int n_seq, int total,
+                               int max_seqlen, int H_q, int H_kv, int D, int P, int causal,
+                               float scale, int dtype, int order, void* workspace,
+                               size_t workspace_bytes, int* dev_status, void* stream) {
+  if (!cu_seqlens || !lse || !dout || !dq || !dk || !dv || !workspace) return RA_ERR_NULL;
+  if (n_seq <= 0 || total <= 0 || max_seqlen <= 0) return RA_ERR_SHAPE;
+  if (!aligned(cu_seqlens, 4)) return RA_ERR_ALIGN;
+  ra_status st = check_attn_args(q, k, v, out, lse, 1, H_q, H_kv, total, D, dtype, -1,
+                                 nullptr, dev_status);
+  if (st != RA_OK) return st;
+  if (dtype != RA_BF16) return RA_ERR_DTYPE;
+  if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(workspace, 16))
+    return RA_ERR_ALIGN;
+  if ((long long)n_seq * max_seqlen * H_q > kMaxElems) return RA_ERR_RANGE;
+  Geometry g;
+  st = make_geometry(n_seq, H_q, H_kv, max_seqlen, D, P, causal, scale, order, -1,
+                     tile_rows_for(dtype, D), &g);
+  if (st != RA_OK) return st;
+  g.cu_seqlens = cu_seqlens;
+  g.total = total;
+  size_t need = 0;
+  st = ring_attn_bwd_workspace(n_seq, H_q, max_seqlen, D, P, order, &need);
+  if (st != RA_OK) return st;
+  if (workspace_bytes < need) return RA_ERR_BUFFER;
+  int sms = 0;
+  st = check_device(&sms);
+  if (st != RA_OK) return st;
+  return launch_attn_bwd(g, q, k, v, out, lse, dout, dq, dk, dv,
+                         static_cast<float*>(workspace), RA_BWD_ALL, dev_status,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
 ra_status attn_lse_merge_n(const void* const* o, const float* const* lse,
                            int n, void* out, float* out_lse, int B, int H,
                            int S, int D, int dtype, void* stream) {

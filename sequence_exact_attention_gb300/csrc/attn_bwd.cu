@@ -128,28 +128,36 @@ __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 
 
 // ------------------------------------------------------------------ prep
 // 8 threads per padded query row; each reads D/8 elements of out and dout.
-template <int D>
+template <int D, bool kVarlen>
 __global__ void __launch_bounds__(256)
-bwd_prep_kernel(const Geometry g, const __nv_bfloat16* __restrict__ out,
+bwd_prep_kernel(const Geometry gp, const __nv_bfloat16* __restrict__ out,
                 const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
                 float* __restrict__ lse2, float* __restrict__ delta, long long rows) {
   const long long gid = (long long)blockIdx.x * 32 + (threadIdx.x >> 3);
   const int sub = threadIdx.x & 7;
   if (gid >= rows) return;               // rows is a multiple of 32: whole blocks
+  // the workspace is laid out by the grid's geometry (longest sequence);
+  // positions follow the row's own sequence
   const int row = (int)(gid % kT);
   long long rest = gid / kT;
-  const int ti = (int)(rest % g.nt);
-  rest /= g.nt;
-  const int seg = (int)(rest % g.n_seg);
-  const int bh = (int)(rest / g.n_seg);
-  const int b = bh / g.H_q, h = bh % g.H_q;
+  const int ti = (int)(rest % gp.nt);
+  rest /= gp.nt;
+  const int seg = (int)(rest % gp.n_seg);
+  const int bh = (int)(rest / gp.n_seg);
+  const int b = bh / gp.H_q, h = bh % gp.H_q;
+  Geometry gv;
+  int row0 = 0;
+  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0);
+  const Geometry& g = kVarlen ? gv : gp;
+  const size_t srow = kVarlen ? (size_t)row0 : (size_t)b * gp.S;
+  const size_t lrow = kVarlen ? (size_t)h * gp.total + row0 : (size_t)bh * gp.S;
   const int in_seg = ti * kT + row;
   const bool valid = in_seg < seg_tokens(g, seg);
   const int pos = seg * g.seg_len + in_seg;
   float acc = 0.f;
   if (valid) {
     constexpr int E = D / 8;
-    const size_t off = (((size_t)b * g.S + pos) * g.H_q + h) * D + (size_t)sub * E;
+    const size_t off = ((srow + pos) * g.H_q + h) * D + (size_t)sub * E;
     const uint4* po = reinterpret_cast<const uint4*>(out + off);
     const uint4* pd = reinterpret_cast<const uint4*>(dout + off);
 #pragma unroll
@@ -167,7 +175,7 @@ bwd_prep_kernel(const Geometry g, const __nv_bfloat16* __restrict__ out,
   acc += __shfl_xor_sync(0xffffffffu, acc, 2);
   acc += __shfl_xor_sync(0xffffffffu, acc, 4);
   if (sub == 0) {
-    lse2[gid] = valid ? lse[(size_t)bh * g.S + pos] * kLog2e : INFINITY;
+    lse2[gid] = valid ? lse[lrow + pos] * kLog2e : INFINITY;
     delta[gid] = valid ? acc : 0.f;
   }
 }
@@ -253,12 +261,12 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
 // Warp w covers key rows 32 (w mod 4) .. +31 and query columns 64 (w / 4)
 // .. +63; its bf16 P^T and dS^T go into the first 32 columns of its own
 // S^T and dP^T column ranges, so no warp writes columns another one reads.
-template <int D>
+template <int D, bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v,
-                const __grid_constant__ CUtensorMap tm_do, const Geometry g,
+                const __grid_constant__ CUtensorMap tm_do, const Geometry gp,
                 const float* __restrict__ lse2, const float* __restrict__ delta,
                 __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
                 int* __restrict__ status) {
@@ -276,12 +284,20 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
   // work item: key tile kt of kv head hk; (batch, kv head) outermost so that
   // the CTAs resident together read the queries of one group from L2; key
   // tiles in position order (most causal work first).
-  const int grp = g.H_q / g.H_kv;
-  const int n_kt = g.n_seg * g.nt;
+  const int grp = gp.H_q / gp.H_kv;
+  const int n_kt = gp.n_seg * gp.nt;
   const int kt = (int)(blockIdx.x % n_kt);
   const int bhk = (int)(blockIdx.x / n_kt);
-  const int b = bhk / g.H_kv, hk = bhk % g.H_kv;
-  const int kseg = kt / g.nt, kti = kt % g.nt;
+  const int b = bhk / gp.H_kv, hk = bhk % gp.H_kv;
+  const int kseg = kt / gp.nt, kti = kt % gp.nt;
+  // packed variable-length sequences: b is the sequence, `g` its geometry
+  Geometry gv;
+  int row0 = 0;
+  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0);
+  const Geometry& g = kVarlen ? gv : gp;
+  const int trow = kVarlen ? row0 : 0;        // TMA row and batch coordinates
+  const int tbat = kVarlen ? 0 : b;
+  const size_t srow = kVarlen ? (size_t)row0 : (size_t)b * gp.S;
   const int src = seg_owner(g, kseg);
   const int kv_lo = kseg * g.seg_len + kti * kT;
   const int kv_valid = tile_tokens(g, kseg, kti);   // <= 0: padding only
@@ -301,8 +317,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(C::bFix), 2 * C::kTileBytes);
       for (int bx = 0; bx < C::kBoxes; ++bx) {
-        tma_load_4d(base + C::kFixA + bx * kBoxBytes, &tm_k, bar(C::bFix), bx * 64, hk, kv_lo, b);
-        tma_load_4d(base + C::kFixB + bx * kBoxBytes, &tm_v, bar(C::bFix), bx * 64, hk, kv_lo, b);
+        tma_load_4d(base + C::kFixA + bx * kBoxBytes, &tm_k, bar(C::bFix), bx * 64, hk,
+                    trow + kv_lo, tbat);
+        tma_load_4d(base + C::kFixB + bx * kBoxBytes, &tm_v, bar(C::bFix), bx * 64, hk,
+                    trow + kv_lo, tbat);
       }
       QIter it;
       it.init(g, src, kv_lo, kv_valid, h0, h0 + grp);
@@ -316,11 +334,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
         const uint32_t sb = base + C::kStage0 + st * C::kStageBytes;
         mbar_arrive_expect_tx(bar(C::bFull + st), 2 * C::kTileBytes + C::kStatBytes);
         for (int bx = 0; bx < C::kBoxes; ++bx) {
-          tma_load_4d(sb + bx * kBoxBytes, &tm_q, bar(C::bFull + st), bx * 64, qt.h, qt.lo, b);
+          tma_load_4d(sb + bx * kBoxBytes, &tm_q, bar(C::bFull + st), bx * 64, qt.h,
+                      trow + qt.lo, tbat);
           tma_load_4d(sb + C::kTileBytes + bx * kBoxBytes, &tm_do, bar(C::bFull + st), bx * 64,
-                      qt.h, qt.lo, b);
+                      qt.h, trow + qt.lo, tbat);
         }
-        const long long wi = ws_tile(g, b * g.H_q + qt.h, qt.seg, qt.ti);
+        const long long wi = ws_tile(gp, b * gp.H_q + qt.h, qt.seg, qt.ti);
         bulk_load(sb + 2 * C::kTileBytes, lse2 + wi, kT * 4, bar(C::bFull + st));
         bulk_load(sb + 2 * C::kTileBytes + kT * 4, delta + wi, kT * 4, bar(C::bFull + st));
         ++j;
@@ -471,7 +490,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (ok) {
       tc_fence_after();
       const bool row_ok = row < kv_valid;
-      const size_t off = (((size_t)b * g.S + kpos) * g.H_kv + hk) * D;
+      const size_t off = ((srow + kpos) * g.H_kv + hk) * D;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         __nv_bfloat16* dst = (which ? dk : dv) + off;
@@ -505,12 +524,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
 // P kept in registers) and then dP (pass 2), writing bf16 dS into the first
 // 32 columns of their own dP column range. S of the next key tile is issued
 // as soon as pass 1 has read S, so it runs while dS and dQ are computed.
-template <int D>
+template <int D, bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v,
-              const __grid_constant__ CUtensorMap tm_do, const Geometry g,
+              const __grid_constant__ CUtensorMap tm_do, const Geometry gp,
               const float* __restrict__ lse2, const float* __restrict__ delta,
               __nv_bfloat16* __restrict__ dq, int* __restrict__ status) {
   using C = Cfg<D>;
@@ -526,17 +545,25 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   // work item: one query tile, ordered as the forward's (kv head outermost,
   // query tiles by decreasing position, the group's heads innermost)
-  const int grp = g.H_q / g.H_kv;
-  const int n_qt = g.n_seg * g.nt;
+  const int grp = gp.H_q / gp.H_kv;
+  const int n_qt = gp.n_seg * gp.nt;
   const int hg = (int)(blockIdx.x % grp);
   const int rest = (int)(blockIdx.x / grp);
   const int qt = n_qt - 1 - rest % n_qt;
   const int bhk = rest / n_qt;
-  const int b = bhk / g.H_kv, hk = bhk % g.H_kv;
+  const int b = bhk / gp.H_kv, hk = bhk % gp.H_kv;
   const int h = hk * grp + hg;
-  const int bh = b * g.H_q + h;
-  const int seg = qt / g.nt;
-  const int ti = qt % g.nt;
+  const int bh = b * gp.H_q + h;
+  const int seg = qt / gp.nt;
+  const int ti = qt % gp.nt;
+  // packed variable-length sequences: b is the sequence, `g` its geometry
+  Geometry gv;
+  int row0 = 0;
+  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0);
+  const Geometry& g = kVarlen ? gv : gp;
+  const int trow = kVarlen ? row0 : 0;        // TMA row and batch coordinates
+  const int tbat = kVarlen ? 0 : b;
+  const size_t srow = kVarlen ? (size_t)row0 : (size_t)b * gp.S;
   const int r = seg_owner(g, seg);
   const int q_lo = seg * g.seg_len + ti * kT;
   const int q_valid = tile_tokens(g, seg, ti);      // <= 0: padding only
@@ -555,8 +582,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(C::bFix), 2 * C::kTileBytes);
       for (int bx = 0; bx < C::kBoxes; ++bx) {
-        tma_load_4d(base + C::kFixA + bx * kBoxBytes, &tm_q, bar(C::bFix), bx * 64, h, q_lo, b);
-        tma_load_4d(base + C::kFixB + bx * kBoxBytes, &tm_do, bar(C::bFix), bx * 64, h, q_lo, b);
+        tma_load_4d(base + C::kFixA + bx * kBoxBytes, &tm_q, bar(C::bFix), bx * 64, h,
+                    trow + q_lo, tbat);
+        tma_load_4d(base + C::kFixB + bx * kBoxBytes, &tm_do, bar(C::bFix), bx * 64, h,
+                    trow + q_lo, tbat);
       }
       KvIter it;
       it.init(g, r, q_lo, q_valid);
@@ -570,9 +599,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
         const uint32_t sb = base + C::kStage0 + st * C::kStageBytes;
         mbar_arrive_expect_tx(bar(C::bFull + st), 2 * C::kTileBytes);
         for (int bx = 0; bx < C::kBoxes; ++bx) {
-          tma_load_4d(sb + bx * kBoxBytes, &tm_k, bar(C::bFull + st), bx * 64, hk, kv.lo, b);
+          tma_load_4d(sb + bx * kBoxBytes, &tm_k, bar(C::bFull + st), bx * 64, hk,
+                      trow + kv.lo, tbat);
           tma_load_4d(sb + C::kTileBytes + bx * kBoxBytes, &tm_v, bar(C::bFull + st), bx * 64, hk,
-                      kv.lo, b);
+                      trow + kv.lo, tbat);
         }
         ++j;
       }
@@ -658,7 +688,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t c0 = (uint32_t)(hf * 64);
     const int q_pos = q_lo + row;
     const float sl2 = g.scale_log2;
-    const long long wi = ws_tile(g, bh, seg, ti) + row;
+    const long long wi = ws_tile(gp, bh, seg, ti) + row;
     const float l2_row = lse2[wi];      // +inf on padding rows: p = 0
     const float dl_row = delta[wi];
     KvIter it;
@@ -721,7 +751,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (ok) {
       tc_fence_after();
       const bool row_ok = row < q_valid;
-      __nv_bfloat16* dst = dq + (((size_t)b * g.S + q_pos) * g.H_q + h) * D;
+      __nv_bfloat16* dst = dq + ((srow + q_pos) * g.H_q + h) * D;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         const int col = hf * (D / 2) + c * 32;
@@ -745,7 +775,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
     atomicExch(status, (int)RA_ERR_TIMEOUT);
 }
 
-template <int D>
+template <int D, bool kVarlen>
 ra_status launch_d(const Geometry& g, const CUtensorMap& mq, const CUtensorMap& mk,
                    const CUtensorMap& mv, const CUtensorMap& mdo, const void* out,
                    const float* lse, const void* dout, void* dq, void* dk, void* dv,
@@ -760,25 +790,25 @@ ra_status launch_d(const Geometry& g, const CUtensorMap& mq, const CUtensorMap& 
   const long long grid_q = n_tiles * g.B * g.H_q;
   if (prep_blocks > 0x7fffffffLL || grid_q > 0x7fffffffLL) return RA_ERR_RANGE;
   if (phases & RA_BWD_PREP) {
-    bwd_prep_kernel<D><<<(unsigned)prep_blocks, 256, 0, stream>>>(
+    bwd_prep_kernel<D, kVarlen><<<(unsigned)prep_blocks, 256, 0, stream>>>(
         g, static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout),
         lse, lse2, delta, rows);
     if (cudaGetLastError() != cudaSuccess) return RA_ERR_LAUNCH;
   }
   if (phases & RA_BWD_DKDV) {
-    if (cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(bwd_dkdv_kernel<D, kVarlen>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return RA_ERR_LAUNCH;
-    bwd_dkdv_kernel<D><<<(unsigned)grid_kv, kThreads, C::kSmemBytes, stream>>>(
+    bwd_dkdv_kernel<D, kVarlen><<<(unsigned)grid_kv, kThreads, C::kSmemBytes, stream>>>(
         mq, mk, mv, mdo, g, lse2, delta, static_cast<__nv_bfloat16*>(dk),
         static_cast<__nv_bfloat16*>(dv), status);
     if (cudaGetLastError() != cudaSuccess) return RA_ERR_LAUNCH;
   }
   if (phases & RA_BWD_DQ) {
-    if (cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(bwd_dq_kernel<D, kVarlen>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return RA_ERR_LAUNCH;
-    bwd_dq_kernel<D><<<(unsigned)grid_q, kThreads, C::kSmemBytes, stream>>>(
+    bwd_dq_kernel<D, kVarlen><<<(unsigned)grid_q, kThreads, C::kSmemBytes, stream>>>(
         mq, mk, mv, mdo, g, lse2, delta, static_cast<__nv_bfloat16*>(dq), status);
     if (cudaGetLastError() != cudaSuccess) return RA_ERR_LAUNCH;
   }
@@ -795,17 +825,27 @@ ra_status launch_attn_bwd(const Geometry& g, const void* q, const void* k, const
                           const void* out, const float* lse, const void* dout, void* dq,
                           void* dk, void* dv, float* workspace, int phases,
                           int* dev_status, cudaStream_t stream) {
+  // packed variable-length tensors are mapped as one batch of `total` rows
+  const bool varlen = g.cu_seqlens != nullptr;
+  const int mb = varlen ? 1 : g.B, ms = varlen ? g.total : g.S;
   CUtensorMap mq, mk, mv, mdo;
-  if (!make_bshd_map(&mq, q, g.B, g.S, g.H_q, g.D, kT) ||
-      !make_bshd_map(&mk, k, g.B, g.S, g.H_kv, g.D, kT) ||
-      !make_bshd_map(&mv, v, g.B, g.S, g.H_kv, g.D, kT) ||
-      !make_bshd_map(&mdo, dout, g.B, g.S, g.H_q, g.D, kT))
+  if (!make_bshd_map(&mq, q, mb, ms, g.H_q, g.D, kT) ||
+      !make_bshd_map(&mk, k, mb, ms, g.H_kv, g.D, kT) ||
+      !make_bshd_map(&mv, v, mb, ms, g.H_kv, g.D, kT) ||
+      !make_bshd_map(&mdo, dout, mb, ms, g.H_q, g.D, kT))
     return RA_ERR_LAUNCH;
+  if (varlen) {
+    if (g.D == 64)
+      return launch_d<64, true>(g, mq, mk, mv, mdo, out, lse, dout, dq, dk, dv, workspace,
+                                phases, dev_status, stream);
+    return launch_d<128, true>(g, mq, mk, mv, mdo, out, lse, dout, dq, dk, dv, workspace,
+                               phases, dev_status, stream);
+  }
   if (g.D == 64)
-    return launch_d<64>(g, mq, mk, mv, mdo, out, lse, dout, dq, dk, dv, workspace, phases,
-                        dev_status, stream);
-  return launch_d<128>(g, mq, mk, mv, mdo, out, lse, dout, dq, dk, dv, workspace, phases,
-                       dev_status, stream);
+    return launch_d<64, false>(g, mq, mk, mv, mdo, out, lse, dout, dq, dk, dv, workspace,
+                               phases, dev_status, stream);
+  return launch_d<128, false>(g, mq, mk, mv, mdo, out, lse, dout, dq, dk, dv, workspace,
+                              phases, dev_status, stream);
 }
 
 }  // namespace ra

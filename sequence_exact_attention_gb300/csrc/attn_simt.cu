@@ -36,9 +36,9 @@ __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
   return fmaf(a.w, b.w, acc);
 }
 
-template <int D>
+template <int D, bool kVarlen>
 __global__ void __launch_bounds__(kThreads)
-attn_simt_kernel(const Geometry g, const float* __restrict__ q,
+attn_simt_kernel(const Geometry gp, const float* __restrict__ q,
                  const float* __restrict__ k, const float* __restrict__ v,
                  float* __restrict__ out, float* __restrict__ lse,
                  int* __restrict__ vlog, int log_stride) {
@@ -48,16 +48,25 @@ attn_simt_kernel(const Geometry g, const float* __restrict__ q,
   float4* Ks = smem;                 // [kRows][V4]
   float4* Vs = smem + kRows * V4;    // [kRows][V4]
 
-  const int BH = g.B * g.H_q;
+  // With packed variable-length sequences, b is the sequence and the grid is
+  // sized by the longest one; `g` is then this sequence's own geometry.
+  const int BH = gp.B * gp.H_q;
   const int bh = blockIdx.x % BH;
-  const int n_qt = g.n_seg * g.nt;
+  const int n_qt = gp.n_seg * gp.nt;
   const int qid = n_qt - 1 - blockIdx.x / BH;    // later positions first
-  const int seg = qid / g.nt, ti = qid % g.nt;
+  const int seg = qid / gp.nt, ti = qid % gp.nt;
+  const int b = bh / gp.H_q, h = bh % gp.H_q;
+  Geometry gv;
+  int row0 = 0;
+  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0);
+  const Geometry& g = kVarlen ? gv : gp;
   const int q_lo = seg * g.seg_len + ti * kRows;
   const int q_valid = tile_tokens(g, seg, ti);     // <= 0: a tile of padding only
   const int r = seg_owner(g, seg);
-  const int b = bh / g.H_q, h = bh % g.H_q;
   const int hk = h / (g.H_q / g.H_kv);
+  // first row of this sequence in q, k, v, out, and its first lse entry
+  const size_t srow = kVarlen ? (size_t)row0 : (size_t)b * gp.S;
+  const size_t lrow = kVarlen ? (size_t)h * gp.total + row0 : (size_t)bh * gp.S;
 
   const int row = threadIdx.x >> 2, part = threadIdx.x & 3;
   const int q_pos = q_lo + row;
@@ -65,7 +74,7 @@ attn_simt_kernel(const Geometry g, const float* __restrict__ q,
 
   float4 qv[NV], acc[NV];
   const float4* qrow = reinterpret_cast<const float4*>(
-      q + (((size_t)b * g.S + (row_valid ? q_pos : q_lo)) * g.H_q + h) * D);
+      q + ((srow + (row_valid ? q_pos : 0)) * g.H_q + h) * D);
 #pragma unroll
   for (int e = 0; e < NV; ++e) {
     qv[e] = row_valid ? qrow[part + 4 * e] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -89,7 +98,7 @@ attn_simt_kernel(const Geometry g, const float* __restrict__ q,
       const int kr = idx / V4, c = idx % V4;
       float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
       if (kr < kv.valid) {
-        const size_t off = (((size_t)b * g.S + kv.lo + kr) * g.H_kv + hk) * V4 + c;
+        const size_t off = ((srow + kv.lo + kr) * g.H_kv + hk) * V4 + c;
         kk = reinterpret_cast<const float4*>(k)[off];
         vv = reinterpret_cast<const float4*>(v)[off];
       }
@@ -143,35 +152,41 @@ attn_simt_kernel(const Geometry g, const float* __restrict__ q,
   if (row_valid) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
     float4* orow = reinterpret_cast<float4*>(
-        out + (((size_t)b * g.S + q_pos) * g.H_q + h) * D);
+        out + ((srow + q_pos) * g.H_q + h) * D);
 #pragma unroll
     for (int e = 0; e < NV; ++e)
       orow[part + 4 * e] = make_float4(acc[e].x * inv, acc[e].y * inv,
                                        acc[e].z * inv, acc[e].w * inv);
     if (part == 0 && lse)
-      lse[(size_t)bh * g.S + q_pos] =
+      lse[lrow + q_pos] =
           l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
   }
   if (log_base && threadIdx.x == 0) log_base[0] = n_vis;
 }
 
-template <int D>
+template <int D, bool kVarlen = false>
 ra_status launch_d(const Geometry& g, const float* q, const float* k,
                    const float* v, float* out, float* lse, int* vlog,
                    int log_stride, cudaStream_t stream) {
   const int smem = 2 * kRows * D * (int)sizeof(float);
-  if (cudaFuncSetAttribute(attn_simt_kernel<D>,
+  if (cudaFuncSetAttribute(attn_simt_kernel<D, kVarlen>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)
     return RA_ERR_LAUNCH;
   const long long grid = (long long)g.n_seg * g.nt * g.B * g.H_q;
   if (grid > 0x7fffffffLL) return RA_ERR_RANGE;
-  attn_simt_kernel<D><<<(unsigned)grid, kThreads, smem, stream>>>(
+  attn_simt_kernel<D, kVarlen><<<(unsigned)grid, kThreads, smem, stream>>>(
       g, q, k, v, out, lse, vlog, log_stride);
   return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
 }
 
 }  // namespace
+
+ra_status launch_attn_simt_varlen(const Geometry& g, const float* q, const float* k,
+                                  const float* v, float* out, float* lse, cudaStream_t stream) {
+  if (g.D == 64) return launch_d<64, true>(g, q, k, v, out, lse, nullptr, 0, stream);
+  return launch_d<128, true>(g, q, k, v, out, lse, nullptr, 0, stream);
+}
 
 ra_status launch_attn_simt(const Geometry& g, const float* q, const float* k,
                            const float* v, void* out, float* lse,

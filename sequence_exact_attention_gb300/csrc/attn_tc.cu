@@ -184,11 +184,11 @@ __device__ __forceinline__ void exp2_poly2(float x0, float x1, float& p0, float&
   p1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(s1) << 23));
 }
 
-template <int D, bool kOutF32>
+template <int D, bool kOutF32, bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const Geometry g,
+               const __grid_constant__ CUtensorMap tm_v, const Geometry gp,
                void* __restrict__ out, float* __restrict__ lse,
                int* __restrict__ vlog, int log_stride, int* __restrict__ status) {
   using C = Cfg<D>;
@@ -214,20 +214,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   // heads and find them in L2; then query tiles by decreasing position
   // (decreasing causal work, longest first); the query heads sharing the kv
   // head innermost, so they read the same key tiles at the same time.
-  const int grp = g.H_q / g.H_kv;
-  const int n_qt = g.n_seg * g.nt;
+  // With packed variable-length sequences, b is the sequence and the grid is
+  // sized by the longest one; `g` is then this sequence's own geometry.
+  const int grp = gp.H_q / gp.H_kv;
+  const int n_qt = gp.n_seg * gp.nt;
   const int hg = (int)(blockIdx.x % grp);
   const int rest = (int)(blockIdx.x / grp);
   const int qt = n_qt - 1 - rest % n_qt;
   const int bhk = rest / n_qt;
-  const int b = bhk / g.H_kv, hk = bhk % g.H_kv;
+  const int b = bhk / gp.H_kv, hk = bhk % gp.H_kv;
   const int h = hk * grp + hg;
-  const int bh = b * g.H_q + h;
-  const int seg = qt / g.nt;
-  const int ti = qt % g.nt;
+  const int bh = b * gp.H_q + h;
+  const int seg = qt / gp.nt;
+  const int ti = qt % gp.nt;
+  Geometry gv;
+  int row0 = 0;
+  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0);
+  const Geometry& g = kVarlen ? gv : gp;
   const int r = seg_owner(g, seg);
   const int q_lo = seg * g.seg_len + ti * kTile;
   const int q_valid = tile_tokens(g, seg, ti);     // <= 0: a tile of padding only
+  // TMA row and batch coordinates, first output row, first lse entry
+  const int trow = kVarlen ? row0 : 0;
+  const int tbat = kVarlen ? 0 : b;
+  const size_t orow = kVarlen ? (size_t)row0 : (size_t)b * gp.S;
+  const size_t lrow = kVarlen ? (size_t)h * gp.total + row0 : (size_t)bh * gp.S;
 
   // ---- set-up: barriers, abort flag, TMEM
   if (threadIdx.x == 0) {
@@ -260,7 +271,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const uint32_t q_smem = base + C::kQOff;
       mbar_arrive_expect_tx(bar(C::bQFull), C::kTileBytes);
       for (int bx = 0; bx < C::kBoxes; ++bx)
-        tma_load_4d(q_smem + bx * kBoxBytes, &tm_q, bar(C::bQFull), bx * 64, h, q_lo, b);
+        tma_load_4d(q_smem + bx * kBoxBytes, &tm_q, bar(C::bQFull), bx * 64, h, trow + q_lo,
+                    tbat);
       KvIter it;
       it.init(g, r, q_lo, q_valid);
       KvTile kv;
@@ -279,7 +291,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tile_flags[j & 15] = 1u;
         mbar_arrive_expect_tx(bar(C::bKFull + bb), C::kTileBytes);
         for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_load_4d(k_smem + bx * kBoxBytes, &tm_k, bar(C::bKFull + bb), bx * 64, hk, kv.lo, b);
+          tma_load_4d(k_smem + bx * kBoxBytes, &tm_k, bar(C::bKFull + bb), bx * 64, hk,
+                      trow + kv.lo, tbat);
         nk = j + 1;
         // V_j reuses the slot of V_{j-2}: free once PV(j-2) is done
         // (odone of buffer (j-2) mod 3, phase (j-2) / 3)
@@ -294,7 +307,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           mbar_arrive_expect_tx(bar(C::bVFull + vb), C::kTileBytes);
           for (int bx = 0; bx < C::kBoxes; ++bx)
             tma_load_4d(base + C::kVOff + vb * C::kTileBytes + bx * kBoxBytes, &tm_v,
-                        bar(C::bVFull + vb), bx * 64, hk, kv.lo, b);
+                        bar(C::bVFull + vb), bx * 64, hk, trow + kv.lo, tbat);
         }
         nv = j + 1;
         ++j;
@@ -549,7 +562,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     if (ok) {
       const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-      const size_t row_off = (((size_t)b * g.S + q_pos) * g.H_q + h) * D + half * (D / 2);
+      const size_t row_off = ((orow + q_pos) * g.H_q + h) * D + half * (D / 2);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t uo[32];
@@ -584,7 +597,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
       }
       if (row_valid && lse && half == 0)
-        lse[(size_t)bh * g.S + q_pos] =
+        lse[lrow + q_pos] =
             l_tot > 0.f ? (m_run + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
     }
   }
@@ -636,12 +649,12 @@ bool make_bshd_map(CUtensorMap* m, const void* ptr, int B, int S, int H, int D) 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool kOutF32>
+template <int D, bool kOutF32, bool kVarlen = false>
 ra_status launch_typed(const Geometry& g, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, void* out, float* lse, int* vlog,
                        int log_stride, int* status, cudaStream_t stream) {
   using C = Cfg<D>;
-  auto kern = attn_tc_kernel<D, kOutF32>;
+  auto kern = attn_tc_kernel<D, kOutF32, kVarlen>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return RA_ERR_LAUNCH;
@@ -660,6 +673,20 @@ ra_status launch_attn_tc_withheld(const Geometry& g0, const void* q, const void*
   Geometry g = g0;
   g.withhold_v0 = 1;
   return launch_attn_tc(g, q, k, v, out, lse, nullptr, 0, dev_status, sm_count, stream);
+}
+
+ra_status launch_attn_tc_varlen(const Geometry& g, const void* q, const void* k,
+                                const void* v, void* out, float* lse, int* dev_status,
+                                cudaStream_t stream) {
+  // the packed tensors are mapped as one batch of `total` rows
+  CUtensorMap mq, mk, mv;
+  if (!make_bshd_map(&mq, q, 1, g.total, g.H_q, g.D) ||
+      !make_bshd_map(&mk, k, 1, g.total, g.H_kv, g.D) ||
+      !make_bshd_map(&mv, v, 1, g.total, g.H_kv, g.D))
+    return RA_ERR_LAUNCH;
+  if (g.D == 64)
+    return launch_typed<64, false, true>(g, mq, mk, mv, out, lse, nullptr, 0, dev_status, stream);
+  return launch_typed<128, false, true>(g, mq, mk, mv, out, lse, nullptr, 0, dev_status, stream);
 }
 
 ra_status launch_attn_tc(const Geometry& g, const void* q, const void* k, const void* v,

@@ -39,6 +39,8 @@ ra_status make_geometry(int B, int H_q, int H_kv, int S, int D, int P,
   g->scale = scale > 0.f ? scale : 1.0f / __builtin_sqrtf((float)D);
   g->scale_log2 = g->scale * 1.4426950408889634f;
   g->withhold_v0 = 0;
+  g->cu_seqlens = nullptr;
+  g->total = 0;
   return RA_OK;
 }
 

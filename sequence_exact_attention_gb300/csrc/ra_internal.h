@@ -27,6 +27,12 @@ struct Geometry {
   float scale;     // softmax scale
   float scale_log2;  // scale * log2(e)
   int withhold_v0;   // test only: the producer never loads V of key tile 0
+  // Packed variable-length batches (null for fixed-length BSHD tensors):
+  // sequence b occupies rows [cu_seqlens[b], cu_seqlens[b+1]) of tensors of
+  // `total` rows; B is the number of sequences and S their maximum length,
+  // which sizes the grid. Each sequence is its own ring problem.
+  const int* cu_seqlens;
+  int total;
 };
 
 // Host-side planning helpers (plan.cpp).
@@ -47,6 +53,12 @@ ra_status launch_attn_simt(const Geometry& g, const float* q, const float* k,
 ra_status launch_attn_tc_withheld(const Geometry& g, const void* q, const void* k,
                                   const void* v, void* out, float* lse, int* dev_status,
                                   int sm_count, cudaStream_t stream);
+// Packed variable-length launches (g.cu_seqlens set, no visit log, all steps).
+ra_status launch_attn_tc_varlen(const Geometry& g, const void* q, const void* k,
+                                const void* v, void* out, float* lse, int* dev_status,
+                                cudaStream_t stream);
+ra_status launch_attn_simt_varlen(const Geometry& g, const float* q, const float* k,
+                                  const float* v, float* out, float* lse, cudaStream_t stream);
 ra_status launch_attn_tc(const Geometry& g, const void* q, const void* k,
                          const void* v, void* out, float* lse, int* visit_log,
                          int log_stride, int* dev_status, int sm_count,

@@ -39,6 +39,25 @@ __device__ __forceinline__ int tile_tokens(const Geometry& g, int seg, int ti) {
   return min(g.tile, seg_tokens(g, seg) - ti * g.tile);
 }
 
+// Geometry of packed sequence b: the grid's geometry `gp` (sized by the
+// longest sequence) with S = the sequence's own length, so its chunks are
+// ceil(S_b / n_seg) positions, padded like any uneven length. `row0` is the
+// sequence's first row in the packed tensors. Offsets are clamped into
+// [0, total] and lengths to [0, S], so a malformed table cannot move any
+// access outside the tensors.
+__device__ __forceinline__ void varlen_geometry(const Geometry& gp, int b, Geometry& gs,
+                                                int& row0) {
+  int lo = __ldg(gp.cu_seqlens + b);
+  int hi = __ldg(gp.cu_seqlens + b + 1);
+  lo = min(max(lo, 0), gp.total);
+  hi = min(max(hi, lo), gp.total);
+  gs = gp;
+  gs.S = min(hi - lo, gp.S);
+  gs.seg_len = (gs.S + gp.n_seg - 1) / gp.n_seg;
+  gs.nt = (gs.seg_len + gp.tile - 1) / gp.tile;
+  row0 = lo;
+}
+
 struct KvTile {
   int step;     // ring step t
   int src;      // rank the block started on

@@ -188,6 +188,43 @@ def test_bwd_argument_errors(lib):
                                     bad, None, None) == RA_ERR_RANGE
 
 
+def _fwd_varlen(lib, q=A, k=A, v=A, out=A, lse=A, cu=A, n=3, total=600, mx=300, Hq=2,
+                Hkv=2, D=128, P=4, causal=1, dtype=0, order=1):
+    vp = ctypes.c_void_p
+    return lib.ring_attn_fwd_varlen(vp(q), vp(k), vp(v), vp(out), vp(lse), vp(cu), n, total,
+                                    mx, Hq, Hkv, D, P, causal, 0.0, dtype, order, None, None)
+
+
+def test_varlen_argument_errors(lib):
+    assert _fwd_varlen(lib, cu=0) == RA_ERR_NULL
+    assert _fwd_varlen(lib, q=0) == RA_ERR_NULL
+    assert _fwd_varlen(lib, n=0) == RA_ERR_SHAPE
+    assert _fwd_varlen(lib, total=0) == RA_ERR_SHAPE
+    assert _fwd_varlen(lib, mx=0) == RA_ERR_SHAPE
+    assert _fwd_varlen(lib, Hq=3) == RA_ERR_SHAPE
+    assert _fwd_varlen(lib, D=96) == RA_ERR_HEADDIM
+    assert _fwd_varlen(lib, cu=A + 2) == RA_ERR_ALIGN
+    assert _fwd_varlen(lib, q=A + 8) == RA_ERR_ALIGN
+    assert _fwd_varlen(lib, dtype=4) == RA_ERR_DTYPE
+    assert _fwd_varlen(lib, order=5) == RA_ERR_DTYPE
+    assert _fwd_varlen(lib, total=1 << 24, Hq=64, Hkv=64) == RA_ERR_RANGE
+    vp = ctypes.c_void_p
+    args = [vp(A)] * 10
+
+    def bwd(**kw):
+        a = dict(n=3, total=600, mx=300, Hq=2, Hkv=2, D=128, P=4, causal=1, dtype=0, order=0,
+                 ws_bytes=1 << 24)
+        a.update(kw)
+        return lib.ring_attn_bwd_varlen(*args, a["n"], a["total"], a["mx"], a["Hq"], a["Hkv"],
+                                        a["D"], a["P"], a["causal"], 0.0, a["dtype"], a["order"],
+                                        vp(A), a["ws_bytes"], None, None)
+
+    assert bwd(dtype=1) == RA_ERR_DTYPE
+    assert bwd(n=0) == RA_ERR_SHAPE
+    need = _ws_bytes(lib, B=3, Hq=2, S=300, D=128, P=4)[1]
+    assert bwd(ws_bytes=need - 1) == RA_ERR_BUFFER
+
+
 def test_valid_call_without_gpu_reports_device_error(lib):
     """With every argument valid the only thing missing here is the GPU."""
     import torch
@@ -195,3 +232,4 @@ def test_valid_call_without_gpu_reports_device_error(lib):
         pytest.skip("a GPU is present: this case would launch on fake pointers")
     assert _fwd(lib) == RA_ERR_DEVICE
     assert _bwd(lib) == RA_ERR_DEVICE
+    assert _fwd_varlen(lib) == RA_ERR_DEVICE
