@@ -24,6 +24,8 @@ Everything here is float64 NumPy, written to be read against the pages:
   restates it per (rank, step); ``backward_rows`` evaluates sampled rows.
 * ``attention_varlen`` / ``attention_backward_varlen`` - packed batches of
   sequences of different lengths, each its own problem.
+* ``ulysses_attention`` - the Ulysses steps (all-to-all to heads, full
+  attention per head group, all-to-all back) on sequence-sharded tensors.
 * ``tile_visits``       - expands the chunk-level schedule into the sequence of
   fixed-size key tiles a tiled kernel must visit, classifying every tile by
   brute force over its (query, key) pairs.
@@ -43,6 +45,8 @@ from .schedule import (
 from .ring import ring_attention
 from .backward import attention_backward, ring_attention_backward, backward_rows
 from .varlen import attention_varlen, attention_backward_varlen
+from .ulysses import (ulysses_attention, to_sequence_shards, from_sequence_shards,
+                      all_to_all_seq_to_head, all_to_all_head_to_seq)
 
 __all__ = [
     "attention_naive", "attention_rows", "partial_attention",
@@ -52,4 +56,6 @@ __all__ = [
     "ring_attention",
     "attention_backward", "ring_attention_backward", "backward_rows",
     "attention_varlen", "attention_backward_varlen",
+    "ulysses_attention", "to_sequence_shards", "from_sequence_shards",
+    "all_to_all_seq_to_head", "all_to_all_head_to_seq",
 ]
