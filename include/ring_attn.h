@@ -156,6 +156,33 @@ ra_status ring_attn_fwd_varlen(const void* q, const void* k, const void* v,
                                int* dev_status, void* stream);
 
 /*
+ * ring_attn_fwd_ulysses - exact attention in the sequence-parallel layout of
+ * Ulysses-style sequence parallelism (glossary "sequence parallelism
+ * transformers", §Ulysses Sequence Parallelism: an all-to-all turns the
+ * sequence-parallel layout into a head-parallel one, each rank computes full
+ * attention for its subset of heads, and a second all-to-all restores the
+ * sequence-parallel layout).
+ *
+ * Virtual rank p holds the contiguous shard of C = ceil(S/P) positions
+ * [p*C, min((p+1)*C, S)) of every batch and head, and the tensors are the P
+ * ranks' local tensors stacked:
+ *     q, out  [P, B, C, H_q,  D]      k, v  [P, B, C, H_kv, D]
+ *     lse     [P, B, H_q, C]          float32 (may be NULL)
+ * (rows of a last, partly filled shard past S are neither read nor written).
+ * Rank r's head-parallel work is heads [r*H_q/P, (r+1)*H_q/P) (and the kv
+ * heads they read) over all S positions. On one GPU both all-to-alls are an
+ * index map inside the kernel's loads and stores: nothing is copied. The
+ * result is full attention, as for every other entry point. H_q and H_kv
+ * must be multiples of P (else RA_ERR_SHAPE). dtype RA_BF16 or RA_F32; all
+ * steps; no visit log. Errors as ring_attn_fwd_ex.
+ */
+ra_status ring_attn_fwd_ulysses(const void* q, const void* k, const void* v,
+                                void* out, float* lse,
+                                int B, int H_q, int H_kv, int S, int D, int P,
+                                int causal, float scale, int dtype,
+                                int* dev_status, void* stream);
+
+/*
  * ring_attn_visit_log_len - size of the visit log of ring_attn_fwd_ex.
  *
  * The kernel for `dtype` cuts every chunk (contiguous) or half (zig-zag) of

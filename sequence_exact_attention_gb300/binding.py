@@ -23,7 +23,7 @@ MERGE_MAX_N = 16
 
 # every entry point declared in include/ring_attn.h
 EXPORTS = ("ring_attn_fwd", "ring_attn_fwd_ex", "ring_attn_visit_log_len",
-           "ring_attn_fwd_varlen", "ring_attn_bwd_varlen",
+           "ring_attn_fwd_varlen", "ring_attn_bwd_varlen", "ring_attn_fwd_ulysses",
            "ring_attn_bwd_workspace", "ring_attn_bwd", "ring_attn_bwd_ex",
            "attn_lse_merge", "attn_lse_merge_n", "ring_attn_plan",
            "ring_attn_expiry_test", "ring_attn_strerror", "ring_attn_version")
@@ -65,6 +65,8 @@ def load():
     lib.ring_attn_bwd_ex.restype = c_int
     lib.ring_attn_bwd_ex.argtypes = ([vp] * 9 + [c_int] * 7 + [c_float, c_int, c_int, vp,
                                                                 ctypes.c_size_t, c_int, vp, vp])
+    lib.ring_attn_fwd_ulysses.restype = c_int
+    lib.ring_attn_fwd_ulysses.argtypes = [vp] * 5 + [c_int] * 7 + [c_float, c_int, vp, vp]
     lib.ring_attn_fwd_varlen.restype = c_int
     lib.ring_attn_fwd_varlen.argtypes = ([vp] * 6 + [c_int] * 8 + [c_float, c_int, c_int,
                                                                    vp, vp])
@@ -318,6 +320,32 @@ def ring_attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens, max_seqlen, P, cau
                                   _ptr(dev_status), _stream(stream))
     _check(st, "ring_attn_bwd_varlen")
     return dq, dk, dv
+
+
+def ring_attn_fwd_ulysses(q, k, v, S, causal, scale=None, out=None, lse=None,
+                          dev_status=None, stream=None):
+    """Attention of sequence-sharded tensors q [P,B,C,H_q,D], k/v [P,B,C,H_kv,D]
+    (C = ceil(S/P)). Returns (out [P,B,C,H_q,D], lse [P,B,H_q,C])."""
+    import torch
+    lib = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dev(t, n)
+    P, B, C, H_q, D = q.shape
+    H_kv = k.shape[3]
+    if k.shape != (P, B, C, H_kv, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [P, B, C, H_kv, D] matching q")
+    if C != -(-S // P):
+        raise ValueError("shard length must be ceil(S / P)")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(P, B, H_q, C, device=q.device, dtype=torch.float32)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    st = lib.ring_attn_fwd_ulysses(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H_q, H_kv,
+                                   S, D, P, int(bool(causal)), sc, _dtype_code(q.dtype),
+                                   _ptr(dev_status), _stream(stream))
+    _check(st, "ring_attn_fwd_ulysses")
+    return out, lse
 
 
 def attn_lse_merge(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):

@@ -154,6 +154,32 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
                           dev_status, stream);
 }
 
+ra_status ring_attn_fwd_ulysses(const void* q, const void* k, const void* v, void* out,
+                                float* lse, int B, int H_q, int H_kv, int S, int D, int P,
+                                int causal, float scale, int dtype, int* dev_status,
+                                void* stream) {
+  if (P <= 0) return RA_ERR_SHAPE;
+  if (H_q % P != 0 || H_kv % P != 0) return RA_ERR_SHAPE;
+  Geometry g;
+  ra_status st = make_geometry(B, H_q, H_kv, S, D, P, causal, scale, RA_ORDER_CONTIGUOUS, -1,
+                               tile_rows_for(dtype, D), &g);
+  if (st != RA_OK) return st;
+  // the padded shards: P * C rows per batch
+  st = check_attn_args(q, k, v, out, lse, B, H_q, H_kv, P * g.seg_len, D, dtype, -1, nullptr,
+                       dev_status);
+  if (st != RA_OK) return st;
+  g.shard_rows = g.seg_len;
+  int sms = 0;
+  st = check_device(&sms);
+  if (st != RA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == RA_F32)
+    return launch_attn_simt_sharded(g, static_cast<const float*>(q),
+                                    static_cast<const float*>(k), static_cast<const float*>(v),
+                                    static_cast<float*>(out), lse, s);
+  return launch_attn_tc_sharded(g, q, k, v, out, lse, dev_status, s);
+}
+
 ra_status ring_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
                                float* lse, const int* cu_seqlens, int n_seq, int total,
                                int max_seqlen, int H_q, int H_kv, int D, int P, int causal,

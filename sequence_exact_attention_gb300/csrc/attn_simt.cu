@@ -64,9 +64,19 @@ attn_simt_kernel(const Geometry gp, const float* __restrict__ q,
   const int q_valid = tile_tokens(g, seg, ti);     // <= 0: a tile of padding only
   const int r = seg_owner(g, seg);
   const int hk = h / (g.H_q / g.H_kv);
-  // first row of this sequence in q, k, v, out, and its first lse entry
-  const size_t srow = kVarlen ? (size_t)row0 : (size_t)b * gp.S;
-  const size_t lrow = kVarlen ? (size_t)h * gp.total + row0 : (size_t)bh * gp.S;
+  // first row of this sequence in q, k, v, out, and its first lse entry; in
+  // the sequence-sharded layout [P, B, C, H, D] the rows of segment p of
+  // batch b start at ((p * B + b) * C - p * C) + position
+  const bool sharded = !kVarlen && gp.shard_rows > 0;
+  const size_t C_rows = (size_t)gp.shard_rows;
+  size_t srow = kVarlen ? (size_t)row0 : (size_t)b * gp.S;
+  size_t lrow = kVarlen ? (size_t)h * gp.total + row0 : (size_t)bh * gp.S;
+  size_t qrow0 = srow;
+  if (sharded) {
+    const size_t lb = (size_t)seg * gp.B + b;
+    qrow0 = lb * C_rows - (size_t)seg * C_rows;
+    lrow = (lb * gp.H_q + h) * C_rows - (size_t)seg * C_rows;
+  }
 
   const int row = threadIdx.x >> 2, part = threadIdx.x & 3;
   const int q_pos = q_lo + row;
@@ -74,7 +84,7 @@ attn_simt_kernel(const Geometry gp, const float* __restrict__ q,
 
   float4 qv[NV], acc[NV];
   const float4* qrow = reinterpret_cast<const float4*>(
-      q + ((srow + (row_valid ? q_pos : 0)) * g.H_q + h) * D);
+      q + ((qrow0 + (row_valid ? q_pos : q_lo)) * g.H_q + h) * D);
 #pragma unroll
   for (int e = 0; e < NV; ++e) {
     qv[e] = row_valid ? qrow[part + 4 * e] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -94,11 +104,13 @@ attn_simt_kernel(const Geometry gp, const float* __restrict__ q,
     ++n_vis;
 
     __syncthreads();    // the previous tile is no longer read
+    const size_t krow0 =
+        sharded ? ((size_t)kv.seg * gp.B + b) * C_rows - (size_t)kv.seg * C_rows : srow;
     for (int idx = threadIdx.x; idx < kRows * V4; idx += kThreads) {
       const int kr = idx / V4, c = idx % V4;
       float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
       if (kr < kv.valid) {
-        const size_t off = ((srow + kv.lo + kr) * g.H_kv + hk) * V4 + c;
+        const size_t off = ((krow0 + kv.lo + kr) * g.H_kv + hk) * V4 + c;
         kk = reinterpret_cast<const float4*>(k)[off];
         vv = reinterpret_cast<const float4*>(v)[off];
       }
@@ -152,7 +164,7 @@ attn_simt_kernel(const Geometry gp, const float* __restrict__ q,
   if (row_valid) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
     float4* orow = reinterpret_cast<float4*>(
-        out + ((srow + q_pos) * g.H_q + h) * D);
+        out + ((qrow0 + q_pos) * g.H_q + h) * D);
 #pragma unroll
     for (int e = 0; e < NV; ++e)
       orow[part + 4 * e] = make_float4(acc[e].x * inv, acc[e].y * inv,
@@ -186,6 +198,12 @@ ra_status launch_attn_simt_varlen(const Geometry& g, const float* q, const float
                                   const float* v, float* out, float* lse, cudaStream_t stream) {
   if (g.D == 64) return launch_d<64, true>(g, q, k, v, out, lse, nullptr, 0, stream);
   return launch_d<128, true>(g, q, k, v, out, lse, nullptr, 0, stream);
+}
+
+ra_status launch_attn_simt_sharded(const Geometry& g, const float* q, const float* k,
+                                   const float* v, float* out, float* lse, cudaStream_t stream) {
+  if (g.D == 64) return launch_d<64>(g, q, k, v, out, lse, nullptr, 0, stream);
+  return launch_d<128>(g, q, k, v, out, lse, nullptr, 0, stream);
 }
 
 ra_status launch_attn_simt(const Geometry& g, const float* q, const float* k,

@@ -234,11 +234,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int r = seg_owner(g, seg);
   const int q_lo = seg * g.seg_len + ti * kTile;
   const int q_valid = tile_tokens(g, seg, ti);     // <= 0: a tile of padding only
-  // TMA row and batch coordinates, first output row, first lse entry
-  const int trow = kVarlen ? row0 : 0;
-  const int tbat = kVarlen ? 0 : b;
-  const size_t orow = kVarlen ? (size_t)row0 : (size_t)b * gp.S;
-  const size_t lrow = kVarlen ? (size_t)h * gp.total + row0 : (size_t)bh * gp.S;
+  // TMA row and batch coordinates, first output row, first lse entry. In the
+  // sequence-sharded layout [P, B, C, H, D] (mapped as [P*B, C, H, D]) the
+  // query tile's segment is its shard p: batch p*B + b, rows from p*C.
+  const bool sharded = !kVarlen && gp.shard_rows > 0;
+  int trow = kVarlen ? row0 : 0;
+  int tbat = kVarlen ? 0 : b;
+  size_t orow = kVarlen ? (size_t)row0 : (size_t)b * gp.S;
+  size_t lrow = kVarlen ? (size_t)h * gp.total + row0 : (size_t)bh * gp.S;
+  if (sharded) {
+    const size_t lb = (size_t)seg * gp.B + b, rows = (size_t)gp.shard_rows;
+    trow = -seg * gp.shard_rows;
+    tbat = (int)lb;
+    orow = lb * rows - (size_t)seg * rows;
+    lrow = (lb * gp.H_q + h) * rows - (size_t)seg * rows;
+  }
 
   // ---- set-up: barriers, abort flag, TMEM
   if (threadIdx.x == 0) {
@@ -289,10 +299,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           break;
         }
         tile_flags[j & 15] = 1u;
+        // the key tile's own shard in the sequence-sharded layout
+        const int krow = sharded ? -kv.seg * gp.shard_rows : trow;
+        const int kbat = sharded ? kv.seg * gp.B + b : tbat;
         mbar_arrive_expect_tx(bar(C::bKFull + bb), C::kTileBytes);
         for (int bx = 0; bx < C::kBoxes; ++bx)
           tma_load_4d(k_smem + bx * kBoxBytes, &tm_k, bar(C::bKFull + bb), bx * 64, hk,
-                      trow + kv.lo, tbat);
+                      krow + kv.lo, kbat);
         nk = j + 1;
         // V_j reuses the slot of V_{j-2}: free once PV(j-2) is done
         // (odone of buffer (j-2) mod 3, phase (j-2) / 3)
@@ -307,7 +320,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           mbar_arrive_expect_tx(bar(C::bVFull + vb), C::kTileBytes);
           for (int bx = 0; bx < C::kBoxes; ++bx)
             tma_load_4d(base + C::kVOff + vb * C::kTileBytes + bx * kBoxBytes, &tm_v,
-                        bar(C::bVFull + vb), bx * 64, hk, trow + kv.lo, tbat);
+                        bar(C::bVFull + vb), bx * 64, hk, krow + kv.lo, kbat);
         }
         nv = j + 1;
         ++j;
@@ -687,6 +700,20 @@ ra_status launch_attn_tc_varlen(const Geometry& g, const void* q, const void* k,
   if (g.D == 64)
     return launch_typed<64, false, true>(g, mq, mk, mv, out, lse, nullptr, 0, dev_status, stream);
   return launch_typed<128, false, true>(g, mq, mk, mv, out, lse, nullptr, 0, dev_status, stream);
+}
+
+ra_status launch_attn_tc_sharded(const Geometry& g, const void* q, const void* k,
+                                 const void* v, void* out, float* lse, int* dev_status,
+                                 cudaStream_t stream) {
+  // [P, B, C, H, D] mapped as P*B batches of C rows
+  const int nb = g.P * g.B, C = g.shard_rows;
+  CUtensorMap mq, mk, mv;
+  if (!make_bshd_map(&mq, q, nb, C, g.H_q, g.D) || !make_bshd_map(&mk, k, nb, C, g.H_kv, g.D) ||
+      !make_bshd_map(&mv, v, nb, C, g.H_kv, g.D))
+    return RA_ERR_LAUNCH;
+  if (g.D == 64)
+    return launch_typed<64, false>(g, mq, mk, mv, out, lse, nullptr, 0, dev_status, stream);
+  return launch_typed<128, false>(g, mq, mk, mv, out, lse, nullptr, 0, dev_status, stream);
 }
 
 ra_status launch_attn_tc(const Geometry& g, const void* q, const void* k, const void* v,

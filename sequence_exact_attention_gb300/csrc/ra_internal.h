@@ -33,6 +33,10 @@ struct Geometry {
   // which sizes the grid. Each sequence is its own ring problem.
   const int* cu_seqlens;
   int total;
+  // > 0: tensors in the sequence-sharded layout of P virtual ranks,
+  // [P, B, shard_rows, H, D] (rank p's rows [p * shard_rows, ...) of every
+  // batch contiguous), chunks contiguous with shard_rows = seg_len.
+  int shard_rows;
 };
 
 // Host-side planning helpers (plan.cpp).
@@ -59,6 +63,12 @@ ra_status launch_attn_tc_varlen(const Geometry& g, const void* q, const void* k,
                                 cudaStream_t stream);
 ra_status launch_attn_simt_varlen(const Geometry& g, const float* q, const float* k,
                                   const float* v, float* out, float* lse, cudaStream_t stream);
+// Sequence-sharded layout launches (g.shard_rows set, no visit log, all steps).
+ra_status launch_attn_tc_sharded(const Geometry& g, const void* q, const void* k,
+                                 const void* v, void* out, float* lse, int* dev_status,
+                                 cudaStream_t stream);
+ra_status launch_attn_simt_sharded(const Geometry& g, const float* q, const float* k,
+                                   const float* v, float* out, float* lse, cudaStream_t stream);
 ra_status launch_attn_tc(const Geometry& g, const void* q, const void* k,
                          const void* v, void* out, float* lse, int* visit_log,
                          int log_stride, int* dev_status, int sm_count,

@@ -61,6 +61,7 @@ __device__ __forceinline__ void varlen_geometry(const Geometry& gp, int b, Geome
 struct KvTile {
   int step;     // ring step t
   int src;      // rank the block started on
+  int seg;      // segment (position order) the tile belongs to
   int id;       // global tile id = segment * nt + index in segment
   int lo;       // first token position
   int valid;    // rows in this tile (< tile only at a ragged segment end)
@@ -83,11 +84,12 @@ struct KvIter {
   int which;       // segment of src being walked (0 or 1)
   int lo;          // first position of the next tile
   int id;          // id of the next tile
+  int seg;         // segment being walked
   int rem;         // tokens of the current segment from `lo` on
   int q_lo, q_hi;  // the query tile's first and last valid position
 
   __device__ __forceinline__ void start_segment(const Geometry& g) {
-    const int seg = rank_seg(g, src, which);
+    seg = rank_seg(g, src, which);
     lo = seg * g.seg_len;
     id = seg * g.nt;
     rem = seg_tokens(g, seg);
@@ -111,6 +113,7 @@ struct KvIter {
         const int valid = min(g.tile, rem);
         kv.step = t;
         kv.src = src;
+        kv.seg = seg;
         kv.id = id;
         kv.lo = lo;
         kv.valid = valid;

@@ -225,6 +225,22 @@ def test_varlen_argument_errors(lib):
     assert bwd(ws_bytes=need - 1) == RA_ERR_BUFFER
 
 
+def test_ulysses_argument_errors(lib):
+    vp = ctypes.c_void_p
+
+    def call(q=A, B=1, Hq=4, Hkv=4, S=1000, D=128, P=4, dtype=0):
+        return lib.ring_attn_fwd_ulysses(vp(q), vp(A), vp(A), vp(A), vp(A), B, Hq, Hkv, S, D, P,
+                                         1, 0.0, dtype, None, None)
+
+    assert call(q=0) == RA_ERR_NULL
+    assert call(Hq=6, Hkv=6) == RA_ERR_SHAPE          # heads do not split over 4 ranks
+    assert call(Hkv=2) == RA_ERR_SHAPE
+    assert call(P=0) == RA_ERR_SHAPE
+    assert call(D=96) == RA_ERR_HEADDIM
+    assert call(dtype=3) == RA_ERR_DTYPE
+    assert call(q=A + 4) == RA_ERR_ALIGN
+
+
 def test_valid_call_without_gpu_reports_device_error(lib):
     """With every argument valid the only thing missing here is the GPU."""
     import torch
