@@ -34,8 +34,8 @@ UNIT = "TFLOP/s"
 
 # ncu DRAM bytes (read + write) of one launch of the tensor-core kernel on the
 # headline workload, valid only for the kernel source with this digest.
-TRAFFIC = {"attn_tc_sha256_16": "e014e73ad1fb7344", "workload": "bf16_s32k_causal_zigzag",
-           "bytes_per_launch": 806223872 + 254455552}
+TRAFFIC = {"attn_tc_sha256_16": "dc827651013c6fa6", "workload": "bf16_s32k_causal_zigzag",
+           "bytes_per_launch": 805725440 + 254199296}
 
 
 def _env_int(name, default):
@@ -355,7 +355,7 @@ def run_ours(args, w):
     if w.dtype == "bf16":
         bound, peak = "tensor", float(peaks.get("bf16_tflops"))
         peak_note = f"{peak_src} bf16 dense (burst)"
-        kname = f"attn_tc_kernel<{w.D},false>"
+        kname = f"attn_tc_kernel<{w.D},false,false>"
         digest = _kernel_digest()
         traffic = (TRAFFIC["bytes_per_launch"]
                    if TRAFFIC["attn_tc_sha256_16"] == digest and w.name == TRAFFIC.get("workload")
@@ -584,6 +584,143 @@ def run_bwd_reference(args, w):
     return 0
 
 
+def _timed_launches(args, step, dev, stream, dist):
+    """Warm-up, then args.steps steps bracketed by barriers and syncs; returns
+    (total ms, mean per-launch ms from events on the launching stream, clocks)."""
+    import torch
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, statistics.mean(a.elapsed_time(b) for a, b in ev), clk
+
+
+def _layout_line(args, world, metric, w, cfg, flop, total_ms, kernel_ms, clk, cpu):
+    peaks, peak_src = _peaks()
+    achieved = flop / (kernel_ms / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    return {
+        "metric": metric, "value": world * flop * args.steps / (total_ms / 1e3) / 1e12,
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "kernel": f"attn_tc_kernel<{w.D},false,...>", "kernel_ms": kernel_ms,
+                     "frac_of_sustained_peak": achieved / float(peaks["bf16_tflops_sustained"])},
+        "cpu_baseline": cpu, "clocks": clk, "gpu_launches": args.steps,
+    }
+
+
+def run_varlen(args, w):
+    """Packed variable-length batch through ring_attn_fwd_varlen."""
+    import numpy as np
+    import torch
+    from sequence_exact_attention_gb300 import binding
+    from sequence_exact_attention_gb300.workloads import make_varlen
+
+    world, rank, local, dist = _dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load()
+    q, k, v, cu = make_varlen(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    cud = torch.tensor(cu, dtype=torch.int32, device=dev)
+    out, lse = torch.empty_like(qd), torch.empty(w.H_q, w.total, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        binding.ring_attn_fwd_varlen(qd, kd, vd, cud, w.max_seqlen, w.P, w.causal, w.scale,
+                                     w.order, out=out, lse=lse, dev_status=status, stream=stream)
+
+    total_ms, kernel_ms, clk = _timed_launches(args, step, dev, stream, dist)
+    if int(status.item()) != 0:
+        raise RuntimeError("device-side wait expired")
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        n = w.lengths[0]
+        rows = np.sort(np.random.default_rng(7).choice(n, 256, replace=False))
+        t0 = time.perf_counter()
+        oracle.attention_rows(q[None, :n], k[None, :n], v[None, :n], w.causal, w.scale, rows)
+        dt = time.perf_counter() - t0
+        pairs = float((rows + 1).sum()) if w.causal else 256.0 * n
+        cpu = {"value": 4.0 * w.D * pairs * w.H_q / dt / 1e12, "unit": UNIT,
+               "cores": _blas_threads(), "kind": "oracle",
+               "sample": f"256 random query rows of the first sequence ({n} tokens), all "
+                         f"heads, float64 NumPy oracle, {dt:.1f} s"}
+    cfg = {"workload": w.name, "lengths": list(w.lengths), "total": w.total, "H_q": w.H_q,
+           "H_kv": w.H_kv, "D": w.D, "P": w.P, "causal": w.causal, "order": w.order,
+           "layout": "packed [total, H, D], cu_seqlens on the device",
+           "l2": "inputs larger than L2", "parallelism": "replicas"}
+    line = _layout_line(args, world, "ring-attn fwd TFLOP/s, packed variable-length batch, "
+                        "1 GB300", w, cfg, w.flop, total_ms, kernel_ms, clk, cpu)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ulysses(args, w):
+    """Sequence-parallel (Ulysses) layout through ring_attn_fwd_ulysses."""
+    import torch
+    from sequence_exact_attention_gb300 import binding
+    from sequence_exact_attention_gb300.workloads import make_sharded_qkv
+
+    world, rank, local, dist = _dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load()
+    q, k, v = make_sharded_qkv(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    C = q.shape[2]
+    out = torch.empty_like(qd)
+    lse = torch.empty(w.P, w.B, w.H_q, C, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        binding.ring_attn_fwd_ulysses(qd, kd, vd, w.S, w.causal, w.scale, out=out, lse=lse,
+                                      dev_status=status, stream=stream)
+
+    total_ms, kernel_ms, clk = _timed_launches(args, step, dev, stream, dist)
+    if int(status.item()) != 0:
+        raise RuntimeError("device-side wait expired")
+    if rank != 0:
+        return 0
+    cfg = dict(_config(w), layout="sequence-parallel [P, B, C, H, D], C = S/P",
+               parallelism="replicas (P virtual ranks inside one launch)")
+    line = _layout_line(args, world, "ring-attn fwd TFLOP/s, Ulysses sequence-parallel "
+                        "layout, 1 GB300", w, cfg, w.flop, total_ms, kernel_ms, clk, None)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_merge(args, w):
     """The standalone n-way LSE merge on its workload; HBM-bound, GB/s."""
     import torch
@@ -653,14 +790,16 @@ def run_merge(args, w):
 
 def main():
     from sequence_exact_attention_gb300.workloads import (BWD_WORKLOADS, HEADLINE,
-                                                          MERGE_WORKLOADS, WORKLOADS)
+                                                          MERGE_WORKLOADS, ULYSSES_WORKLOADS,
+                                                          VARLEN_WORKLOADS, WORKLOADS)
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,
-                    choices=sorted(WORKLOADS) + sorted(MERGE_WORKLOADS) + sorted(BWD_WORKLOADS))
+                    choices=sorted(WORKLOADS) + sorted(MERGE_WORKLOADS) + sorted(BWD_WORKLOADS)
+                    + sorted(VARLEN_WORKLOADS) + sorted(ULYSSES_WORKLOADS))
     ap.add_argument("--cpu-rows", type=int, default=768)
     ap.add_argument("--ref-rows", type=int, default=24)
     ap.add_argument("--cpu-prefix", type=int, default=16384,
@@ -672,6 +811,10 @@ def main():
     args = ap.parse_args()
     if args.workload in MERGE_WORKLOADS:
         return run_merge(args, MERGE_WORKLOADS[args.workload])
+    if args.workload in VARLEN_WORKLOADS:
+        return run_varlen(args, VARLEN_WORKLOADS[args.workload])
+    if args.workload in ULYSSES_WORKLOADS:
+        return run_ulysses(args, ULYSSES_WORKLOADS[args.workload])
     if args.workload in BWD_WORKLOADS:
         w = BWD_WORKLOADS[args.workload]
         if args.seq_len:

@@ -95,6 +95,80 @@ MERGE_WORKLOADS = {
                                    seed=1005),
 }
 
+@dataclass(frozen=True)
+class VarlenWorkload:
+    """A packed batch of sequences of different lengths."""
+    name: str
+    dtype: str
+    lengths: tuple
+    H_q: int
+    H_kv: int
+    D: int
+    P: int
+    causal: bool
+    order: str
+    std: float = 1.0
+    seed: int = 0
+
+    @property
+    def total(self):
+        return int(sum(self.lengths))
+
+    @property
+    def max_seqlen(self):
+        return int(max(self.lengths))
+
+    @property
+    def scale(self):
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def flop(self):
+        """4*H_q*S_b^2*D per sequence, halved under the causal mask."""
+        f = sum(4.0 * self.H_q * n * n * self.D for n in self.lengths)
+        return f / 2 if self.causal else f
+
+
+def make_varlen(w: VarlenWorkload):
+    """(q [total,H_q,D], k, v [total,H_kv,D], cu_seqlens int32 list) CPU tensors."""
+    g = torch.Generator().manual_seed(w.seed)
+    dt = _TORCH_DTYPE[w.dtype]
+    q = (torch.randn(w.total, w.H_q, w.D, generator=g) * w.std).to(dt)
+    k = (torch.randn(w.total, w.H_kv, w.D, generator=g) * w.std).to(dt)
+    v = (torch.randn(w.total, w.H_kv, w.D, generator=g) * w.std).to(dt)
+    cu = [0]
+    for n in w.lengths:
+        cu.append(cu[-1] + int(n))
+    return q, k, v, cu
+
+
+def make_sharded_qkv(w: AttnWorkload):
+    """(q [P,B,C,H_q,D], k, v [P,B,C,H_kv,D]) drawn directly in the
+    sequence-parallel layout of P ranks (C = ceil(S/P)); CPU tensors."""
+    g = torch.Generator().manual_seed(w.seed)
+    C = -(-w.S // w.P)
+    dt = _TORCH_DTYPE[w.dtype]
+    q = (torch.randn(w.P, w.B, C, w.H_q, w.D, generator=g) * w.std).to(dt)
+    k = (torch.randn(w.P, w.B, C, w.H_kv, w.D, generator=g) * w.std).to(dt)
+    v = (torch.randn(w.P, w.B, C, w.H_kv, w.D, generator=g) * w.std).to(dt)
+    return q, k, v
+
+
+# A packed batch of the headline's total length (32768 tokens) in six
+# sequences of mixed lengths, zig-zag order per sequence.
+VARLEN_WORKLOADS = {
+    "bf16_varlen_32k_causal_zigzag": VarlenWorkload(
+        "bf16_varlen_32k_causal_zigzag", "bf16", (8192, 4096, 11000, 1000, 3000, 5480),
+        32, 32, 128, 8, True, "zigzag", std=0.5, seed=1007),
+}
+
+# Ulysses layout: two sequences of 16K in the sequence-parallel layout of 8 ranks.
+ULYSSES_WORKLOADS = {
+    "bf16_ulysses_s16k_b2_causal": AttnWorkload(
+        "bf16_ulysses_s16k_b2_causal", "bf16", 2, 32, 32, 16384, 128, 8, True, "contiguous",
+        std=0.5, seed=1008),
+}
+
 # Backward workloads: the forward shapes of the causal bf16 workloads.
 BWD_WORKLOADS = {
     "bf16_s4k_causal_bwd": WORKLOADS["bf16_s4k_causal"].scaled(name="bf16_s4k_causal_bwd"),
