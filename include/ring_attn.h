@@ -289,6 +289,22 @@ ra_status ring_attn_bwd_varlen(const void* q, const void* k, const void* v,
                                int* dev_status, void* stream);
 
 /*
+ * ring_attn_bwd_ulysses - ring_attn_bwd for tensors in the sequence-parallel
+ * layout of ring_attn_fwd_ulysses (q, out, dout, dq [P, B, C, H_q, D]; k, v,
+ * dk, dv [P, B, C, H_kv, D]; lse [P, B, H_q, C]; C = ceil(S/P)). The
+ * all-to-alls are again index maps in the loads and stores. H_q and H_kv must
+ * be multiples of P. The workspace size is ring_attn_bwd_workspace(B, H_q, S,
+ * D, P, RA_ORDER_CONTIGUOUS, ...). bf16 only. Errors: as ring_attn_bwd.
+ */
+ra_status ring_attn_bwd_ulysses(const void* q, const void* k, const void* v,
+                                const void* out, const float* lse, const void* dout,
+                                void* dq, void* dk, void* dv,
+                                int B, int H_q, int H_kv, int S, int D, int P,
+                                int causal, float scale, int dtype,
+                                void* workspace, size_t workspace_bytes,
+                                int* dev_status, void* stream);
+
+/*
  * attn_lse_merge - exact merge of two partial attention results over
  * disjoint key sets (glossary "sequence parallelism transformers",
  * §Ring Attention and §Implementation Considerations):

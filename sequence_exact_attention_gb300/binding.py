@@ -24,6 +24,7 @@ MERGE_MAX_N = 16
 # every entry point declared in include/ring_attn.h
 EXPORTS = ("ring_attn_fwd", "ring_attn_fwd_ex", "ring_attn_visit_log_len",
            "ring_attn_fwd_varlen", "ring_attn_bwd_varlen", "ring_attn_fwd_ulysses",
+           "ring_attn_bwd_ulysses",
            "ring_attn_bwd_workspace", "ring_attn_bwd", "ring_attn_bwd_ex",
            "attn_lse_merge", "attn_lse_merge_n", "ring_attn_plan",
            "ring_attn_expiry_test", "ring_attn_strerror", "ring_attn_version")
@@ -67,6 +68,9 @@ def load():
                                                                 ctypes.c_size_t, c_int, vp, vp])
     lib.ring_attn_fwd_ulysses.restype = c_int
     lib.ring_attn_fwd_ulysses.argtypes = [vp] * 5 + [c_int] * 7 + [c_float, c_int, vp, vp]
+    lib.ring_attn_bwd_ulysses.restype = c_int
+    lib.ring_attn_bwd_ulysses.argtypes = ([vp] * 9 + [c_int] * 7 + [c_float, c_int, vp,
+                                                                    ctypes.c_size_t, vp, vp])
     lib.ring_attn_fwd_varlen.restype = c_int
     lib.ring_attn_fwd_varlen.argtypes = ([vp] * 6 + [c_int] * 8 + [c_float, c_int, c_int,
                                                                    vp, vp])
@@ -346,6 +350,32 @@ def ring_attn_fwd_ulysses(q, k, v, S, causal, scale=None, out=None, lse=None,
                                    _ptr(dev_status), _stream(stream))
     _check(st, "ring_attn_fwd_ulysses")
     return out, lse
+
+
+def ring_attn_bwd_ulysses(q, k, v, out, lse, dout, S, causal, scale=None, workspace=None,
+                          dev_status=None, stream=None):
+    """Gradients (dq, dk, dv) of ``ring_attn_fwd_ulysses``, all in the
+    sequence-parallel layout [P, B, C, H, D]."""
+    import torch
+    lib = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (lse, "lse"), (dout, "dout")):
+        _dev(t, n)
+    P, B, C, H_q, D = q.shape
+    H_kv = k.shape[3]
+    if C != -(-S // P):
+        raise ValueError("shard length must be ceil(S / P)")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = bwd_workspace_bytes(B, H_q, S, D, P, "contiguous")
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    st = lib.ring_attn_bwd_ulysses(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), B, H_q, H_kv, S, D, P,
+                                   int(bool(causal)), sc, _dtype_code(q.dtype), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(),
+                                   _ptr(dev_status), _stream(stream))
+    _check(st, "ring_attn_bwd_ulysses")
+    return dq, dk, dv
 
 
 def attn_lse_merge(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):

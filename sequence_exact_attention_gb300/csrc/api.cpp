@@ -180,6 +180,38 @@ ra_status ring_attn_fwd_ulysses(const void* q, const void* k, const void* v, voi
   return launch_attn_tc_sharded(g, q, k, v, out, lse, dev_status, s);
 }
 
+ra_status ring_attn_bwd_ulysses(const void* q, const void* k, const void* v, const void* out,
+                                const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                int B, int H_q, int H_kv, int S, int D, int P, int causal,
+                                float scale, int dtype, void* workspace, size_t workspace_bytes,
+                                int* dev_status, void* stream) {
+  if (!lse || !dout || !dq || !dk || !dv || !workspace) return RA_ERR_NULL;
+  if (P <= 0) return RA_ERR_SHAPE;
+  if (H_q % P != 0 || H_kv % P != 0) return RA_ERR_SHAPE;
+  if (dtype != RA_BF16) return RA_ERR_DTYPE;
+  Geometry g;
+  ra_status st = make_geometry(B, H_q, H_kv, S, D, P, causal, scale, RA_ORDER_CONTIGUOUS, -1,
+                               tile_rows_for(dtype, D), &g);
+  if (st != RA_OK) return st;
+  st = check_attn_args(q, k, v, out, lse, B, H_q, H_kv, P * g.seg_len, D, dtype, -1, nullptr,
+                       dev_status);
+  if (st != RA_OK) return st;
+  if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(workspace, 16))
+    return RA_ERR_ALIGN;
+  size_t need = 0;
+  st = ring_attn_bwd_workspace(B, H_q, S, D, P, RA_ORDER_CONTIGUOUS, &need);
+  if (st != RA_OK) return st;
+  if (workspace_bytes < need) return RA_ERR_BUFFER;
+  g.shard_rows = g.seg_len;
+  int sms = 0;
+  st = check_device(&sms);
+  if (st != RA_OK) return st;
+  return launch_attn_bwd(g, q, k, v, out, lse, dout, dq, dk, dv,
+                         static_cast<float*>(workspace), RA_BWD_ALL, dev_status,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
 ra_status ring_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
                                float* lse, const int* cu_seqlens, int n_seq, int total,
                                int max_seqlen, int H_q, int H_kv, int D, int P, int causal,

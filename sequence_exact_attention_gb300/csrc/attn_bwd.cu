@@ -149,8 +149,8 @@ bwd_prep_kernel(const Geometry gp, const __nv_bfloat16* __restrict__ out,
   int row0 = 0;
   if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0);
   const Geometry& g = kVarlen ? gv : gp;
-  const size_t srow = kVarlen ? (size_t)row0 : (size_t)b * gp.S;
-  const size_t lrow = kVarlen ? (size_t)h * gp.total + row0 : (size_t)bh * gp.S;
+  const size_t srow = seg_rows(gp, b, seg, row0, kVarlen).grow;
+  const size_t lrow = lse_base(gp, b, h, seg, row0, kVarlen);
   const int in_seg = ti * kT + row;
   const bool valid = in_seg < seg_tokens(g, seg);
   const int pos = seg * g.seg_len + in_seg;
@@ -295,13 +295,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
   int row0 = 0;
   if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0);
   const Geometry& g = kVarlen ? gv : gp;
-  const int trow = kVarlen ? row0 : 0;        // TMA row and batch coordinates
-  const int tbat = kVarlen ? 0 : b;
-  const size_t srow = kVarlen ? (size_t)row0 : (size_t)b * gp.S;
+  const SegRows kr = seg_rows(gp, b, kseg, row0, kVarlen);   // the key tile's rows
   const int src = seg_owner(g, kseg);
   const int kv_lo = kseg * g.seg_len + kti * kT;
   const int kv_valid = tile_tokens(g, kseg, kti);   // <= 0: padding only
   const int h0 = hk * grp;
+  if (kv_valid <= 0) return;     // no key, no gradient row: the CTA leaves at once
 
   init_barriers<C>(bar, abort_flag, never);
   if (warp == kMmaWarp) {
@@ -318,9 +317,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_arrive_expect_tx(bar(C::bFix), 2 * C::kTileBytes);
       for (int bx = 0; bx < C::kBoxes; ++bx) {
         tma_load_4d(base + C::kFixA + bx * kBoxBytes, &tm_k, bar(C::bFix), bx * 64, hk,
-                    trow + kv_lo, tbat);
+                    kr.trow + kv_lo, kr.tbat);
         tma_load_4d(base + C::kFixB + bx * kBoxBytes, &tm_v, bar(C::bFix), bx * 64, hk,
-                    trow + kv_lo, tbat);
+                    kr.trow + kv_lo, kr.tbat);
       }
       QIter it;
       it.init(g, src, kv_lo, kv_valid, h0, h0 + grp);
@@ -332,12 +331,13 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
             !mbar_wait(bar(C::bFree + st), (uint32_t)((j >> 1) - 1) & 1, abort_flag, kTimeoutNs))
           break;
         const uint32_t sb = base + C::kStage0 + st * C::kStageBytes;
+        const SegRows qr = seg_rows(gp, b, qt.seg, row0, kVarlen);
         mbar_arrive_expect_tx(bar(C::bFull + st), 2 * C::kTileBytes + C::kStatBytes);
         for (int bx = 0; bx < C::kBoxes; ++bx) {
           tma_load_4d(sb + bx * kBoxBytes, &tm_q, bar(C::bFull + st), bx * 64, qt.h,
-                      trow + qt.lo, tbat);
+                      qr.trow + qt.lo, qr.tbat);
           tma_load_4d(sb + C::kTileBytes + bx * kBoxBytes, &tm_do, bar(C::bFull + st), bx * 64,
-                      qt.h, trow + qt.lo, tbat);
+                      qt.h, qr.trow + qt.lo, qr.tbat);
         }
         const long long wi = ws_tile(gp, b * gp.H_q + qt.h, qt.seg, qt.ti);
         bulk_load(sb + 2 * C::kTileBytes, lse2 + wi, kT * 4, bar(C::bFull + st));
@@ -490,7 +490,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (ok) {
       tc_fence_after();
       const bool row_ok = row < kv_valid;
-      const size_t off = ((srow + kpos) * g.H_kv + hk) * D;
+      const size_t off = ((kr.grow + kpos) * g.H_kv + hk) * D;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         __nv_bfloat16* dst = (which ? dk : dv) + off;
@@ -561,12 +561,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
   int row0 = 0;
   if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0);
   const Geometry& g = kVarlen ? gv : gp;
-  const int trow = kVarlen ? row0 : 0;        // TMA row and batch coordinates
-  const int tbat = kVarlen ? 0 : b;
-  const size_t srow = kVarlen ? (size_t)row0 : (size_t)b * gp.S;
+  const SegRows qr = seg_rows(gp, b, seg, row0, kVarlen);    // the query tile's rows
   const int r = seg_owner(g, seg);
   const int q_lo = seg * g.seg_len + ti * kT;
   const int q_valid = tile_tokens(g, seg, ti);      // <= 0: padding only
+  if (q_valid <= 0) return;      // no query, no gradient row: the CTA leaves at once
 
   init_barriers<C>(bar, abort_flag, never);
   if (warp == kMmaWarp) {
@@ -583,9 +582,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_arrive_expect_tx(bar(C::bFix), 2 * C::kTileBytes);
       for (int bx = 0; bx < C::kBoxes; ++bx) {
         tma_load_4d(base + C::kFixA + bx * kBoxBytes, &tm_q, bar(C::bFix), bx * 64, h,
-                    trow + q_lo, tbat);
+                    qr.trow + q_lo, qr.tbat);
         tma_load_4d(base + C::kFixB + bx * kBoxBytes, &tm_do, bar(C::bFix), bx * 64, h,
-                    trow + q_lo, tbat);
+                    qr.trow + q_lo, qr.tbat);
       }
       KvIter it;
       it.init(g, r, q_lo, q_valid);
@@ -597,12 +596,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
             !mbar_wait(bar(C::bFree + st), (uint32_t)((j >> 1) - 1) & 1, abort_flag, kTimeoutNs))
           break;
         const uint32_t sb = base + C::kStage0 + st * C::kStageBytes;
+        const SegRows kr = seg_rows(gp, b, kv.seg, row0, kVarlen);
         mbar_arrive_expect_tx(bar(C::bFull + st), 2 * C::kTileBytes);
         for (int bx = 0; bx < C::kBoxes; ++bx) {
           tma_load_4d(sb + bx * kBoxBytes, &tm_k, bar(C::bFull + st), bx * 64, hk,
-                      trow + kv.lo, tbat);
+                      kr.trow + kv.lo, kr.tbat);
           tma_load_4d(sb + C::kTileBytes + bx * kBoxBytes, &tm_v, bar(C::bFull + st), bx * 64, hk,
-                      trow + kv.lo, tbat);
+                      kr.trow + kv.lo, kr.tbat);
         }
         ++j;
       }
@@ -751,7 +751,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (ok) {
       tc_fence_after();
       const bool row_ok = row < q_valid;
-      __nv_bfloat16* dst = dq + ((srow + q_pos) * g.H_q + h) * D;
+      __nv_bfloat16* dst = dq + ((qr.grow + q_pos) * g.H_q + h) * D;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         const int col = hf * (D / 2) + c * 32;
@@ -825,9 +825,11 @@ ra_status launch_attn_bwd(const Geometry& g, const void* q, const void* k, const
                           const void* out, const float* lse, const void* dout, void* dq,
                           void* dk, void* dv, float* workspace, int phases,
                           int* dev_status, cudaStream_t stream) {
-  // packed variable-length tensors are mapped as one batch of `total` rows
+  // packed variable-length tensors are mapped as one batch of `total` rows,
+  // sequence-sharded ones [P, B, C, H, D] as P*B batches of C rows
   const bool varlen = g.cu_seqlens != nullptr;
-  const int mb = varlen ? 1 : g.B, ms = varlen ? g.total : g.S;
+  const int mb = varlen ? 1 : (g.shard_rows > 0 ? g.P * g.B : g.B);
+  const int ms = varlen ? g.total : (g.shard_rows > 0 ? g.shard_rows : g.S);
   CUtensorMap mq, mk, mv, mdo;
   if (!make_bshd_map(&mq, q, mb, ms, g.H_q, g.D, kT) ||
       !make_bshd_map(&mk, k, mb, ms, g.H_kv, g.D, kT) ||

@@ -82,6 +82,11 @@ attn_simt_kernel(const Geometry gp, const float* __restrict__ q,
   const int q_pos = q_lo + row;
   const bool row_valid = row < q_valid;
 
+  if (q_valid <= 0) {            // a tile of padding only: nothing to compute or write
+    if (vlog && threadIdx.x == 0) vlog[((size_t)bh * n_qt + qid) * log_stride] = 0;
+    return;
+  }
+
   float4 qv[NV], acc[NV];
   const float4* qrow = reinterpret_cast<const float4*>(
       q + ((qrow0 + (row_valid ? q_pos : q_lo)) * g.H_q + h) * D);

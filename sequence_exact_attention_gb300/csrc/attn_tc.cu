@@ -250,6 +250,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     lrow = (lb * gp.H_q + h) * rows - (size_t)seg * rows;
   }
 
+  // A tile of padding only (uneven or packed lengths) has nothing to compute
+  // or write: the whole CTA leaves before it sets anything up.
+  if (q_valid <= 0) {
+    if (vlog && threadIdx.x == 0) vlog[((size_t)bh * n_qt + qt) * log_stride] = 0;
+    return;
+  }
+
   // ---- set-up: barriers, abort flag, TMEM
   if (threadIdx.x == 0) {
     mbar_init(bar(C::bQFull), 1);

@@ -58,6 +58,49 @@ __device__ __forceinline__ void varlen_geometry(const Geometry& gp, int b, Geome
   row0 = lo;
 }
 
+// Where the rows of segment `seg` of batch b live in the tensors' layout.
+// Natural [B, S, H, D]: TMA batch b, positions as rows. Packed sequences:
+// batch 0, rows from the sequence's first row `row0`. Sequence-sharded
+// [P, B, C, H, D] (mapped as [P*B, C, H, D]; segment p is shard p): TMA
+// batch p*B + b, row = position - p*C.
+struct SegRows {
+  int trow;       // added to a position: the TMA row coordinate
+  int tbat;       // the TMA batch coordinate
+  size_t grow;    // added to a position: the row index in units of H*D elements
+};
+
+__device__ __forceinline__ SegRows seg_rows(const Geometry& gp, int b, int seg, int row0,
+                                            bool varlen) {
+  SegRows r;
+  if (varlen) {
+    r.trow = row0;
+    r.tbat = 0;
+    r.grow = (size_t)row0;
+  } else if (gp.shard_rows > 0) {
+    const size_t lb = (size_t)seg * gp.B + b, c = (size_t)gp.shard_rows;
+    r.trow = -seg * gp.shard_rows;
+    r.tbat = (int)lb;
+    r.grow = lb * c - (size_t)seg * c;
+  } else {
+    r.trow = 0;
+    r.tbat = b;
+    r.grow = (size_t)b * gp.S;
+  }
+  return r;
+}
+
+// Index of the lse entry of position 0 of segment `seg`, head h, batch b:
+// natural [B, H, S]; packed [H, total]; sequence-sharded [P, B, H, C].
+__device__ __forceinline__ size_t lse_base(const Geometry& gp, int b, int h, int seg, int row0,
+                                           bool varlen) {
+  if (varlen) return (size_t)h * gp.total + row0;
+  if (gp.shard_rows > 0) {
+    const size_t c = (size_t)gp.shard_rows;
+    return (((size_t)seg * gp.B + b) * gp.H_q + h) * c - (size_t)seg * c;
+  }
+  return ((size_t)b * gp.H_q + h) * gp.S;
+}
+
 struct KvTile {
   int step;     // ring step t
   int src;      // rank the block started on

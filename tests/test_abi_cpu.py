@@ -240,6 +240,16 @@ def test_ulysses_argument_errors(lib):
     assert call(dtype=3) == RA_ERR_DTYPE
     assert call(q=A + 4) == RA_ERR_ALIGN
 
+    def bwd(Hq=4, Hkv=4, dtype=0, ws_bytes=1 << 24, ws=A):
+        return lib.ring_attn_bwd_ulysses(*([vp(A)] * 9), 1, Hq, Hkv, 1000, 128, 4, 1, 0.0, dtype,
+                                         vp(ws), ws_bytes, None, None)
+
+    assert bwd(Hq=6, Hkv=6) == RA_ERR_SHAPE
+    assert bwd(dtype=1) == RA_ERR_DTYPE
+    assert bwd(ws=0) == RA_ERR_NULL
+    need = _ws_bytes(lib, B=1, Hq=4, S=1000, D=128, P=4)[1]
+    assert bwd(ws_bytes=need - 1) == RA_ERR_BUFFER
+
 
 def test_valid_call_without_gpu_reports_device_error(lib):
     """With every argument valid the only thing missing here is the GPU."""

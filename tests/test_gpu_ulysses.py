@@ -64,3 +64,42 @@ def test_ulysses_one_batch_equals_ring_call():
     torch.cuda.synchronize()
     assert torch.equal(o1.view(1, S, H, D), o2)
     assert torch.equal(l1.view(P, H, C).permute(1, 0, 2).reshape(1, H, S), l2)
+
+
+def test_ulysses_backward_one_batch_equals_ring_call():
+    S, P, H, D = 2048, 4, 4, 128
+    w = AttnWorkload("ub1", "bf16", 1, H, H, S, D, P, True, "contiguous", seed=5200)
+    q, k, v = (t.cuda() for t in make_qkv(w))
+    dout = torch.randn(1, S, H, D, generator=torch.Generator().manual_seed(5201)).to(
+        torch.bfloat16).cuda()
+    C = S // P
+    sh = lambda t: t.view(P, 1, C, t.shape[2], D)
+    o1, l1 = binding.ring_attn_fwd_ulysses(sh(q), sh(k), sh(v), S, True)
+    g1 = binding.ring_attn_bwd_ulysses(sh(q), sh(k), sh(v), o1, l1, sh(dout), S, True)
+    o2, l2 = binding.ring_attn_fwd(q, k, v, P, True, order="contiguous")
+    g2 = binding.ring_attn_bwd(q, k, v, o2, l2, dout, P, True, order="contiguous")
+    torch.cuda.synchronize()
+    for a, b in zip(g1, g2):
+        assert torch.equal(a.view(b.shape), b)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,P", [(2, 8, 4, 1000, 128, 4), (3, 4, 2, 301, 64, 2)])
+def test_ulysses_backward_matches_oracle(B, Hq, Hkv, S, D, P):
+    w = AttnWorkload("ub", "bf16", B, Hq, Hkv, S, D, P, True, "contiguous", seed=5300 + S)
+    q, k, v = make_qkv(w)
+    dout = (torch.randn(B, S, Hq, D, generator=torch.Generator().manual_seed(5301)) * 1.0).to(
+        torch.bfloat16)
+    qs, ks, vs, ds = (_sharded(t, P) for t in (q, k, v, dout))
+    out, lse = binding.ring_attn_fwd_ulysses(qs, ks, vs, S, True)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dq, dk, dv = binding.ring_attn_bwd_ulysses(qs, ks, vs, out, lse, ds, S, True,
+                                               dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.attention_backward(q, k, v, dout, True, w.scale)
+    for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        g = oracle.from_sequence_shards(got.double().cpu().numpy(), S)
+        err = np.abs(g - want)
+        rel_max, rel_mean = err.max() / np.abs(want).max(), err.mean() / np.abs(want).mean()
+        # the backward's tolerance (tests/test_gpu_backward.py)
+        assert rel_max <= 2e-2 and rel_mean <= 1e-2, (name, rel_max, rel_mean)
