@@ -65,10 +65,18 @@ namespace {
 using namespace sm100;
 
 constexpr int kTile = 128;
-constexpr int kThreads = 352;
-constexpr int kProducerWarp = 8;
-constexpr int kSIssuerWarp = 9;       // also allocates / frees TMEM
-constexpr int kPVIssuerWarp = 10;
+// Softmax warps per TMEM lane quarter: each row's 128 scores are split over
+// this many warps (kSCols columns each), so 4 * kSplit softmax warps share
+// the SM with the producer and the two issuers. Measured on GB300 (headline
+// workload, 2070 MHz): 2 -> 1456-1464 TFLOP/s, 4 -> 1380 (the four-warp
+// barrier per key tile costs more than the extra warps hide).
+constexpr int kSplit = 2;
+constexpr int kSCols = kTile / kSplit;
+constexpr int kSoftmaxWarps = 4 * kSplit;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
+constexpr int kProducerWarp = kSoftmaxWarps;
+constexpr int kSIssuerWarp = kSoftmaxWarps + 1;   // also allocates / frees TMEM
+constexpr int kPVIssuerWarp = kSoftmaxWarps + 2;
 constexpr int kBuf = 3;               // S/P buffers in TMEM = K slots in smem
 constexpr int kVBuf = 2;              // V slots in smem
 constexpr uint32_t kTmemCols = 512;
@@ -95,7 +103,7 @@ struct Cfg {
   static constexpr int kFlagsOff = kBarBytes;          // 16 x u32: key-tile flags ring
   static constexpr int kFlagsBytes = 64;
   static constexpr int kRedOff = kBarOff + kBarBytes + kFlagsBytes;   // softmax exchange
-  static constexpr int kRedBytes = 768 * 4;   // maxima [2][2][128], sums [2][128]
+  static constexpr int kRedBytes = 3 * kSplit * 128 * 4;   // maxima [2][kSplit][128], sums [kSplit][128]
   static constexpr int kUsed = kRedOff + kRedBytes + 1024;   // + alignment slack
   // Request more than half an SM's shared memory so that one CTA owns the SM
   // and its 512 TMEM columns (the D=64 layout alone would fit two).
@@ -184,6 +192,85 @@ __device__ __forceinline__ void exp2_poly2(float x0, float x1, float& p0, float&
   p1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(s1) << 23));
 }
 
+// P columns of one softmax warp: 32 (two-way split) or 16 (four-way split).
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[32]) {
+  tmem_st32(taddr, r);
+}
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[16]) {
+  tmem_st16(taddr, r);
+}
+
+// Columns [tO, tO + N) of this thread's O row times alpha.
+template <int N>
+__device__ __forceinline__ void scale_cols(uint32_t tO, float alpha) {
+  if constexpr (N >= 32) {
+#pragma unroll
+    for (int c = 0; c < N / 32; ++c) {
+      uint32_t uo[32];
+      tmem_ld32(tO + c * 32, uo);
+      tmem_ld_wait(uo);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) uo[i] = __float_as_uint(__uint_as_float(uo[i]) * alpha);
+      tmem_st32(tO + c * 32, uo);
+    }
+  } else {
+    uint32_t uo[16];
+    tmem_ld16(tO, uo);
+    tmem_ld_wait(uo);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) uo[i] = __float_as_uint(__uint_as_float(uo[i]) * alpha);
+    tmem_st16(tO, uo);
+  }
+}
+
+template <int CH>
+__device__ __forceinline__ void ld_cols(uint32_t taddr, uint32_t (&r)[CH]) {
+  if constexpr (CH == 32) tmem_ld32(taddr, r);
+  else tmem_ld16(taddr, r);
+  tmem_ld_wait(r);
+}
+
+// Epilogue of one softmax warp: its N columns of the O row, times 1/l, to
+// `out` at element offset row_off (bf16, or float32 for single-step
+// partials). Every thread loads (the TMEM load is warp-wide); valid rows store.
+template <int N, bool kOutF32>
+__device__ __forceinline__ void store_out_cols(uint32_t tO, bool have_o, bool row_valid,
+                                               void* out, size_t row_off, float inv_l) {
+  constexpr int CH = N >= 32 ? 32 : 16;
+#pragma unroll
+  for (int c = 0; c < N / CH; ++c) {
+    uint32_t uo[CH];
+    if (have_o) {
+      ld_cols<CH>(tO + c * CH, uo);
+    } else {
+#pragma unroll
+      for (int i = 0; i < CH; ++i) uo[i] = 0u;
+    }
+    if (!row_valid) continue;
+    if constexpr (kOutF32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + row_off + c * CH);
+#pragma unroll
+      for (int i = 0; i < CH / 4; ++i)
+        dst[i] = make_float4(__uint_as_float(uo[4 * i]) * inv_l,
+                             __uint_as_float(uo[4 * i + 1]) * inv_l,
+                             __uint_as_float(uo[4 * i + 2]) * inv_l,
+                             __uint_as_float(uo[4 * i + 3]) * inv_l);
+    } else {
+      uint4* dst =
+          reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + row_off + c * CH);
+#pragma unroll
+      for (int i = 0; i < CH / 8; ++i) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(uo[8 * i + 0]) * inv_l, __uint_as_float(uo[8 * i + 1]) * inv_l);
+        w.y = pack_bf16x2(__uint_as_float(uo[8 * i + 2]) * inv_l, __uint_as_float(uo[8 * i + 3]) * inv_l);
+        w.z = pack_bf16x2(__uint_as_float(uo[8 * i + 4]) * inv_l, __uint_as_float(uo[8 * i + 5]) * inv_l);
+        w.w = pack_bf16x2(__uint_as_float(uo[8 * i + 6]) * inv_l, __uint_as_float(uo[8 * i + 7]) * inv_l);
+        dst[i] = w;
+      }
+    }
+  }
+}
+
 template <int D, bool kOutF32, bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -264,7 +351,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     for (int i = 0; i < kBuf; ++i) {
       mbar_init(bar(C::bKFull + i), 1);
       mbar_init(bar(C::bSFull + i), 1);
-      mbar_init(bar(C::bPFull + i), 256);
+      mbar_init(bar(C::bPFull + i), 32 * kSoftmaxWarps);
       mbar_init(bar(C::bODone + i), 1);
     }
     mbar_init(bar(C::bFinalS), 1);
@@ -412,37 +499,41 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     __syncwarp();
   } else {
-    // ================= softmax: two threads per row, 64 columns each =================
-    // Warps w and w+4 share TMEM lane quarter w % 4 (the same 32 rows); warp
-    // w < 4 handles key columns 0-63 and O columns [0, D/2), warp w+4 the
-    // other halves. The partial row maxima meet in shared memory (one named
-    // barrier per warp pair and key tile); each half keeps its own partial sum.
+    // ================= softmax: kSplit threads per row, kSCols columns each =================
+    // Warps w, w+4, w+8, ... share TMEM lane quarter w % 4 (the same 32 rows);
+    // warp part p = w / 4 handles key columns [p*kSCols, (p+1)*kSCols) and O
+    // columns [p*kOC, (p+1)*kOC). The partial row maxima meet in shared memory
+    // (one named barrier per row group and key tile); each part keeps its own
+    // partial sum.
+    constexpr int kOC = D / kSplit;          // O columns per softmax warp
     const int wq = warp & 3;                 // TMEM lane quarter
-    const int half = warp >> 2;              // column half
+    const int part = warp >> 2;              // column part
     const int row = wq * 32 + lane;
     const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
-    const uint32_t tO = tmem + t_lane + kOCol + half * (D / 2);
+    const uint32_t tO = tmem + t_lane + kOCol + part * kOC;
     const int q_pos = q_lo + row;
     const bool row_valid = row < q_valid;
     const float sl2 = g.scale_log2;
     const uint64_t sl2x2 = pack2(sl2, sl2);
-    const uint32_t pair_bar = 1 + wq;        // named barrier of the warp pair
-    // [2 tile parities][2 halves][128 rows] partial maxima, then partial sums
+    const uint32_t pair_bar = 1 + wq;        // named barrier of the row group
+    constexpr uint32_t kGroup = 32 * kSplit; // threads meeting at that barrier
+    // [2 tile parities][kSplit parts][128 rows] partial maxima, then
+    // [kSplit][128] partial sums
     float* red = reinterpret_cast<float*>(base_ptr + C::kRedOff);
 
     int* log_base = (vlog && threadIdx.x == 0)
                         ? vlog + ((size_t)bh * n_qt + qt) * log_stride
                         : nullptr;
 
-    float m_run = -INFINITY, l_run = 0.f;    // l_run: this half's partial sum
+    float m_run = -INFINITY, l_run = 0.f;    // l_run: this part's partial sum
     int j = 0;               // key tiles done (= P tiles published)
     bool ok = true;
     KvIter it;
     it.init(g, r, q_lo, q_valid);
     KvTile kv, nxt;
-    // Both warps of a pair pass exactly one named barrier per key tile (and
-    // one after the loop), also after an abort: a warp that gave up keeps
-    // walking the tiles and only meets the barriers, so its partner is never
+    // Every warp of a row group passes exactly one named barrier per key tile
+    // (and one after the loop), also after an abort: a warp that gave up
+    // keeps walking the tiles and only meets the barriers, so no partner is
     // left waiting at a barrier that would not complete.
     // The next key tile is looked up while this tile's scores load.
     bool have = it.next(g, kv);
@@ -451,58 +542,63 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (log_base) log_visit(log_base, j, kv, tile_class(g, q_lo, kv));
       const int bb = j % kBuf;
       const uint32_t u = (uint32_t)(j / kBuf);
-      const uint32_t tS = tmem + t_lane + s_col(bb) + half * 64;
+      const uint32_t tS = tmem + t_lane + s_col(bb) + part * kSCols;
       if (ok) ok = mbar_wait(bar(C::bSFull + bb), u & 1, abort_flag, kTimeoutNs);
       if (!ok) {
-        named_bar_sync(pair_bar, 64);
+        named_bar_sync(pair_bar, kGroup);
         ++j;
         have = it.next(g, kv);
         continue;
       }
       tc_fence_after();
 
-      float s[64];
+      float s[kSCols];
       bool have_next;
       {
-        uint32_t u0[32], u1[32];
-        tmem_ld32(tS + 0, u0);
-        tmem_ld32(tS + 32, u1);
+        uint32_t uu[kSCols / 32][32];
+#pragma unroll
+        for (int c = 0; c < kSCols / 32; ++c) tmem_ld32(tS + c * 32, uu[c]);
         have_next = it.next(g, nxt);
         tmem_ld_wait();
-        reg_fence(u0); reg_fence(u1);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          s[i] = __uint_as_float(u0[i]);
-          s[32 + i] = __uint_as_float(u1[i]);
+        for (int c = 0; c < kSCols / 32; ++c) {
+          reg_fence(uu[c]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(uu[c][i]);
         }
       }
       if (work == kMask) {
-        const int lim = (g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid) - half * 64;
+        const int lim =
+            (g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid) - part * kSCols;
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < kSCols; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      // partial row max over 64 columns: 8 chains of 3-input maxima
+      // partial row max over kSCols columns: 8 chains of 3-input maxima
       float m8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = fmax3(s[i], s[8 + i], s[16 + i]);
+      for (int i = 0; i < 8; ++i) m8[i] = s[i];
+      int c8 = 8;
 #pragma unroll
-      for (int c = 24; c < 56; c += 16)
+      for (; c8 + 16 <= kSCols; c8 += 16)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[c + i], s[c + 8 + i]);
+        for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], s[c8 + i], s[c8 + 8 + i]);
+      if (c8 < kSCols) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[56 + i]);
-      const float mx_half = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[c8 + i]);
+      }
+      const float mx_part = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
                                   fmaxf(m8[6], m8[7]));
-      // combine with the partner half of the row
-      // (the barrier also orders both halves' S loads before either half
-      // writes P over the S columns)
-      float* red_j = red + (j & 1) * 256;
-      red_j[half * 128 + row] = mx_half;
+      // combine with the other parts of the row (the barrier also orders all
+      // parts' S loads before any part writes P over the S columns)
+      float* red_j = red + (j & 1) * (kSplit * 128);
+      red_j[part * 128 + row] = mx_part;
       tc_fence_before();
-      named_bar_sync(pair_bar, 64);
+      named_bar_sync(pair_bar, kGroup);
       tc_fence_after();
-      const float mx = fmaxf(mx_half, red_j[(half ^ 1) * 128 + row]);
+      float mx = red_j[row];
+#pragma unroll
+      for (int p2 = 1; p2 < kSplit; ++p2) mx = fmaxf(mx, red_j[p2 * 128 + row]);
 
       const float m_new = fmaxf(m_run, mx * sl2);
       const bool resc = m_new > m_run + kRescaleLog2;
@@ -515,9 +611,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       const uint64_t neg_m2 = pack2(-m_use, -m_use);
       uint64_t sum2a = pack2(0.f, 0.f), sum2b = sum2a;
-      uint32_t pk[32];
+      uint32_t pk[kSCols / 2];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < kSCols / 2; ++i) {
         // (s0, s1) * scale*log2(e) - m in one packed FMA, then two exp2
         const uint64_t x2 = ffma2(pack2(s[2 * i], s[2 * i + 1]), sl2x2, neg_m2);
         float x0, x1;
@@ -533,14 +629,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         else sum2a = fadd2(sum2a, pack2(p0, p1));
         pk[i] = pack_bf16x2(p0, p1);
       }
-      tmem_st32(tmem + t_lane + s_col(bb) + half * 32, pk);   // P columns of this half
+      // P columns of this part (bf16 pairs)
+      tmem_st_cols(tmem + t_lane + s_col(bb) + part * (kSCols / 2), pk);
       {
         float a0, a1;
         unpack2(fadd2(sum2a, sum2b), a0, a1);
         l_run += a0 + a1;
       }
       // O must be scaled by alpha before P(j) V_j is added to it, i.e. after
-      // PV(j-1) is done (both halves take the same decision)
+      // PV(j-1) is done (all parts take the same decision)
       if (__any_sync(0xffffffffu, resc) && j > 0) {
         const int pb = (j - 1) % kBuf;
         ok = mbar_wait(bar(C::bODone + pb), (uint32_t)((j - 1) / kBuf) & 1, abort_flag,
@@ -552,15 +649,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           continue;
         }
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t uo[32];
-          tmem_ld32(tO + c * 32, uo);
-          tmem_ld_wait(uo);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) uo[i] = __float_as_uint(__uint_as_float(uo[i]) * alpha);
-          tmem_st32(tO + c * 32, uo);
-        }
+        scale_cols<kOC>(tO, alpha);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -571,10 +660,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     if (log_base) log_base[0] = j;
 
-    // ---- epilogue: out = O / l, lse = ln2 * (m + log2 l), l = sum of both halves
-    red[512 + half * 128 + row] = l_run;
-    named_bar_sync(pair_bar, 64);
-    const float l_tot = l_run + red[512 + (half ^ 1) * 128 + row];
+    // ---- epilogue: out = O / l, lse = ln2 * (m + log2 l), l = sum of the parts
+    float* red_l = red + 2 * kSplit * 128;
+    red_l[part * 128 + row] = l_run;
+    named_bar_sync(pair_bar, kGroup);
+    float l_tot = 0.f;
+#pragma unroll
+    for (int p2 = 0; p2 < kSplit; ++p2) l_tot += red_l[p2 * 128 + row];
     if (ok && j > 0) {
       ok = mbar_wait(bar(C::bODone + (j - 1) % kBuf), (uint32_t)((j - 1) / kBuf) & 1,
                      abort_flag, kTimeoutNs);
@@ -582,41 +674,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     if (ok) {
       const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-      const size_t row_off = ((orow + q_pos) * g.H_q + h) * D + half * (D / 2);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t uo[32];
-        if (j > 0) {
-          tmem_ld32(tO + c * 32, uo);
-          tmem_ld_wait(uo);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) uo[i] = 0u;
-        }
-        if (row_valid) {
-          if (kOutF32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + row_off + c * 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(uo[4 * i]) * inv_l,
-                                   __uint_as_float(uo[4 * i + 1]) * inv_l,
-                                   __uint_as_float(uo[4 * i + 2]) * inv_l,
-                                   __uint_as_float(uo[4 * i + 3]) * inv_l);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + row_off + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(uo[8 * i + 0]) * inv_l, __uint_as_float(uo[8 * i + 1]) * inv_l);
-              w.y = pack_bf16x2(__uint_as_float(uo[8 * i + 2]) * inv_l, __uint_as_float(uo[8 * i + 3]) * inv_l);
-              w.z = pack_bf16x2(__uint_as_float(uo[8 * i + 4]) * inv_l, __uint_as_float(uo[8 * i + 5]) * inv_l);
-              w.w = pack_bf16x2(__uint_as_float(uo[8 * i + 6]) * inv_l, __uint_as_float(uo[8 * i + 7]) * inv_l);
-              dst[i] = w;
-            }
-          }
-        }
-      }
-      if (row_valid && lse && half == 0)
+      const size_t row_off = ((orow + q_pos) * g.H_q + h) * D + part * kOC;
+      store_out_cols<kOC, kOutF32>(tO, j > 0, row_valid, out, row_off, inv_l);
+      if (row_valid && lse && part == 0)
         lse[lrow + q_pos] =
             l_tot > 0.f ? (m_run + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
     }
