@@ -364,21 +364,30 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
       QIter it;
       it.init(g, src, kv_lo, kv_valid, h0, h0 + grp);
       QTile qt;
-      int j = 0;
-      while (ok && it.next(g, qt)) {
-        const int st = j & 1;
-        const uint32_t pj = (uint32_t)(j - 1) & 1;     // parity of visit j-1
-        const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
-        ok = mbar_wait(bar(C::bFull + st), (uint32_t)(j >> 1) & 1, abort_flag, kTimeoutNs);
-        // S^T(j) overwrites the P^T(j-1) that dV(j-1) reads
-        if (ok && j > 0) ok = mbar_wait(bar(C::bAccV), pj, abort_flag, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
+      // S^T(j+1) is issued as soon as dV(j) has read P^T(j) (they share
+      // columns), before dK(j): the next P^T pass then overlaps dK(j) and
+      // dP^T(j+1).
+      auto issue_s = [&](int jj) {
+        const uint64_t so = (uint64_t)(((jj & 1) * C::kStageBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + kColS, k_kmaj + kstep_off(kk), q_kmaj + so + kstep_off(kk), id_s,
                   kk > 0 ? 1u : 0u);
         umma_commit(bar(C::bS));
+      };
+      bool have = ok && it.next(g, qt);
+      if (have) {
+        ok = mbar_wait(bar(C::bFull + 0), 0, abort_flag, kTimeoutNs);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+        }
+      }
+      int j = 0;
+      while (ok && have) {
+        const int st = j & 1;
+        const uint32_t pj = (uint32_t)(j - 1) & 1;     // parity of visit j-1
+        const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
         // dP^T(j) overwrites the dS^T(j-1) that dK(j-1) reads
         if (j > 0) ok = mbar_wait(bar(C::bAccK), pj, abort_flag, kTimeoutNs);
         if (!ok) break;
@@ -396,6 +405,16 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
           umma_ts(tmem + kColAcc, tmem + kColS + pcol(kk), do_mn + so + (uint64_t)(kk * 2048 >> 4),
                   id_acc, (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar(C::bAccV));
+        // S^T(j+1) overwrites the P^T(j) that dV(j) reads
+        have = it.next(g, qt);
+        if (have) {
+          ok = mbar_wait(bar(C::bFull + ((j + 1) & 1)), (uint32_t)((j + 1) >> 1) & 1, abort_flag,
+                         kTimeoutNs) &&
+               mbar_wait(bar(C::bAccV), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(j + 1);
+        }
         ok = mbar_wait(bar(C::bDS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
