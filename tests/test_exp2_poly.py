@@ -9,7 +9,7 @@ import re
 import numpy as np
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
-                   "sequence_exact_attention_gb300", "csrc", "attn_tc.cu")
+                   "sequence_exact_attention_gb300", "csrc", "fastmath.cuh")
 
 
 def _constants():
