@@ -34,8 +34,8 @@ UNIT = "TFLOP/s"
 
 # ncu DRAM bytes (read + write) of one launch of the tensor-core kernel on the
 # headline workload, valid only for the kernel source with this digest.
-TRAFFIC = {"attn_tc_sha256_16": "dc827651013c6fa6", "workload": "bf16_s32k_causal_zigzag",
-           "bytes_per_launch": 805725440 + 254199296}
+TRAFFIC = {"attn_tc_sha256_16": "64b8b44956c0049f", "workload": "bf16_s32k_causal_zigzag",
+           "bytes_per_launch": 806526464 + 254894336}
 
 
 def _env_int(name, default):
@@ -167,7 +167,7 @@ def run_reference(args, w):
         return 0
     from sequence_exact_attention_gb300.workloads import make_qkv
     q, k, v = make_qkv(w)
-    rows_per_step = args.ref_rows
+    rows_per_step = min(args.ref_rows, w.S)
     for i in range(args.warmup):
         _oracle_sample_rate(w, q, k, v, rows_per_step, seed=100 + i)
     total_flop, total_t = 0.0, 0.0
@@ -369,7 +369,7 @@ def run_ours(args, w):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        n_rows = args.cpu_rows
+        n_rows = min(args.cpu_rows, w.S)
         rate, dt, _ = _oracle_sample_rate(w, q, k, v, n_rows, seed=7)
         cpu = {"value": rate, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
                "sample": f"{n_rows} random query rows x all {w.H_q} heads of the same "
@@ -528,7 +528,7 @@ def run_bwd(args, w):
     peak = float(peaks["bf16_tflops"])
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        n = args.cpu_prefix
+        n = min(args.cpu_prefix, w.S)
         rate, dt = _oracle_bwd_sample_rate(w, q, k, v, dout, n)
         cpu = {"value": rate, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
                "sample": f"causal prefix of {n} positions, query head 0, float64 NumPy "
@@ -562,7 +562,7 @@ def run_bwd_reference(args, w):
     from sequence_exact_attention_gb300.workloads import make_dout, make_qkv
     q, k, v = make_qkv(w)
     dout = make_dout(w)
-    n = args.cpu_prefix
+    n = min(args.cpu_prefix, w.S)
     for _ in range(args.warmup):
         _oracle_bwd_sample_rate(w, q, k, v, dout, n)
     flops, secs = 0.0, 0.0
