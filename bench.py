@@ -125,15 +125,34 @@ class ClockSampler:
                 "samples": len(rows), "reasons": reasons}
 
 
-def _dist_setup(n_gpus):
+def _dist_setup(n_gpus, backend="nccl"):
+    """(world, rank, local rank, torch.distributed or None) from the launcher's
+    environment; one process per GPU, every rank an independent replica."""
     world = _env_int("WORLD_SIZE", 1)
     rank = _env_int("RANK", 0)
     local = _env_int("LOCAL_RANK", 0)
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=None)
+        if not dist.is_initialized():
+            dist.init_process_group(backend)
         return world, rank, local, dist
     return 1, 0, local, None
+
+
+def _max_over_ranks(x, dist, device):
+    """The largest value of x over all ranks (x itself without a process group)."""
+    if not dist:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_rate(world, units_per_step, steps, max_ms):
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time (weak scaling: every rank does the same work)."""
+    return world * units_per_step * steps / (max_ms / 1e3)
 
 
 def _oracle_sample_rate(w, q, k, v, n_rows, seed):
@@ -267,11 +286,8 @@ def _e2e(args, w, q, k, v, qd, kd, vd, out, lse, step, dev, stream, dist, world)
     e1.record(s_in)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = world * flop * args.steps / (e2e_ms / 1e3) / 1e12
+    e2e_ms = _max_over_ranks(e2e_ms, dist, dev)
+    e2e_val = _job_rate(world, flop, args.steps, e2e_ms) / 1e12
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
     d2h = sum(t.numel() * t.element_size() for t in host_out[0])
     return {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -334,12 +350,9 @@ def run_ours(args, w):
     launch_ms = [a.elapsed_time(b) for a, b in ev]
     if int(status.item()) != 0:
         raise RuntimeError("device-side wait expired in the timed region")
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = _max_over_ranks(total_ms, dist, dev)
     flop = w.flop
-    value = world * flop * args.steps / (total_ms / 1e3) / 1e12
+    value = _job_rate(world, flop, args.steps, total_ms) / 1e12
     kernel_ms = statistics.mean(launch_ms)
 
     # ---- end to end through the public API, host buffers, copies timed
@@ -473,12 +486,9 @@ def run_bwd(args, w):
     if int(status.item()) != 0:
         raise RuntimeError("device-side wait expired in the timed region")
     total_ms = t0.elapsed_time(t1)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = _max_over_ranks(total_ms, dist, dev)
     flop = bwd_flop(w)
-    value = world * flop * args.steps / (total_ms / 1e3) / 1e12
+    value = _job_rate(world, flop, args.steps, total_ms) / 1e12
     phase_ms = {name: statistics.mean(e[i][0].elapsed_time(e[i][1]) for e in evs)
                 for i, (name, _) in enumerate(phases)}
 
@@ -506,11 +516,8 @@ def run_bwd(args, w):
         b_.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = a.elapsed_time(b_)
-        if dist:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * flop * args.steps / (e_ms / 1e3) / 1e12, "unit": UNIT,
+        e_ms = _max_over_ranks(e_ms, dist, dev)
+        e2e = {"value": _job_rate(world, flop, args.steps, e_ms) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": sum(t.numel() * t.element_size()
                                          for t in hosts_in + [out_h, lse_h]),
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hosts_out),
@@ -611,10 +618,7 @@ def _timed_launches(args, step, dev, stream, dist):
         dist.barrier()
     clk = clocks.stop()
     total_ms = t0.elapsed_time(t1)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = _max_over_ranks(total_ms, dist, dev)
     return total_ms, statistics.mean(a.elapsed_time(b) for a, b in ev), clk
 
 
@@ -623,7 +627,7 @@ def _layout_line(args, world, metric, w, cfg, flop, total_ms, kernel_ms, clk, cp
     achieved = flop / (kernel_ms / 1e3) / 1e12
     peak = float(peaks["bf16_tflops"])
     return {
-        "metric": metric, "value": world * flop * args.steps / (total_ms / 1e3) / 1e12,
+        "metric": metric, "value": _job_rate(world, flop, args.steps, total_ms) / 1e12,
         "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": cfg,
@@ -760,10 +764,7 @@ def run_merge(args, w):
         dist.barrier()
     clk = clocks.stop()
     total_ms = t0.elapsed_time(t1)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = _max_over_ranks(total_ms, dist, dev)
     if rank != 0:
         return 0
     kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
@@ -771,7 +772,7 @@ def run_merge(args, w):
     gbs = w.bytes / (kernel_ms / 1e3) / 1e9
     line = {
         "metric": "LSE merge GB/s (algorithmic bytes)", "value":
-            world * w.bytes * args.steps / (total_ms / 1e3) / 1e9,
+            _job_rate(world, w.bytes, args.steps, total_ms) / 1e9,
         "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32" if w.dtype == "f32" else "bf16",
