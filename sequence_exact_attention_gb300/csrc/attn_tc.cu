@@ -14,12 +14,15 @@
 // segment of virtual rank r and walks the key tiles of the ring in order,
 // j = 0, 1, ... (tiles wholly after the query tile under a causal mask are
 // left out). "Receiving" a block is a TMA load of its tiles from this GPU's
-// HBM/L2 into shared memory. Warp roles (224 threads):
-//   warps 0-7  softmax: two threads per query row (row = TMEM lane), each
-//              taking 64 of the 128 key columns and half of O's columns
+// HBM/L2 into shared memory. Warp roles (352 threads with kSplit = 2):
+//   warps 0-7  softmax: kSplit = 2 threads per query row (row = TMEM lane),
+//              each taking 64 of the 128 key columns and half of O's columns
 //   warp  8    TMA producer: Q once, then K_j (3 slots) and V_j (2 slots)
 //   warp  9    TMEM allocator; one thread issues the S = Q K^T MMAs
 //   warp 10    one thread issues the O += P V MMAs
+// The same kernel serves the fixed-length [B, S, H, D] layout, packed
+// variable-length sequences (kVarlen) and the sequence-sharded layout
+// (shard_rows > 0); only the rows its loads and stores address differ.
 // Tensor memory (512 columns): three S buffers of 128 f32 columns at 0, 128,
 // 256 (key tile j uses buffer j mod 3; softmax writes P as bf16 over the
 // first 64 columns of that buffer) and the O accumulator at 384.
@@ -32,7 +35,7 @@
 //   kfull[b]            TMA of K_j landed                  (phase u)
 //   vfull[j mod 2]      TMA of V_j landed                  (phase j / 2)
 //   sfull[b]            S(j) done (S issuer's commit)      (phase u)
-//   pfull[b]            P(j) written, O rescaled (256 arrivals)
+//   pfull[b]            P(j) written, O rescaled (one arrival per softmax thread)
 //   odone[b]            PV(j) done (PV issuer's commit)    (phase u)
 // The producer reuses K_j's slot when sfull[b] completes phase u-1 and V_j's
 // (two V slots) once PV(j-2) is done: the completion barriers double as
