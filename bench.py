@@ -34,7 +34,7 @@ UNIT = "TFLOP/s"
 
 # ncu DRAM bytes (read + write) of one launch of the tensor-core kernel on the
 # headline workload, valid only for the kernel source with this digest.
-TRAFFIC = {"attn_tc_sha256_16": "58f5bba1cc3c23fc", "workload": "bf16_s32k_causal_zigzag",
+TRAFFIC = {"attn_tc_sha256_16": "d02032bd774996ab", "workload": "bf16_s32k_causal_zigzag",
            "bytes_per_launch": 806526464 + 254894336}
 
 
@@ -56,15 +56,17 @@ def _peaks():
 
 
 def _kernel_digest():
-    """sha256 (first 16 hex) of the forward kernel's source with // comments
-    and blank lines removed: any code change invalidates the stored traffic,
-    a comment edit does not."""
+    """sha256 (first 16 hex) of the forward kernel's sources -- attn_tc.cu and
+    the headers it includes -- with // comments and blank lines removed: any
+    code change invalidates the stored traffic, a comment edit does not."""
     import re
-    path = os.path.join(ROOT, "sequence_exact_attention_gb300", "csrc", "attn_tc.cu")
-    with open(path, encoding="utf-8") as f:
-        lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in f]
-    code = "\n".join(ln for ln in lines if ln.strip())
-    return hashlib.sha256(code.encode()).hexdigest()[:16]
+    code = []
+    for name in ("attn_tc.cu", "fastmath.cuh", "ring_iter.cuh", "sm100.cuh", "ra_internal.h"):
+        path = os.path.join(ROOT, "sequence_exact_attention_gb300", "csrc", name)
+        with open(path, encoding="utf-8") as f:
+            lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in f]
+        code.append("\n".join(ln for ln in lines if ln.strip()))
+    return hashlib.sha256("\n".join(code).encode()).hexdigest()[:16]
 
 
 class ClockSampler:
