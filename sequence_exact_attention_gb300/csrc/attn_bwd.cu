@@ -80,6 +80,8 @@ struct Cfg {
   static constexpr int bAccK = 10;    // dK MMA (or dQ MMA) of a visit done
   static constexpr int bAcc = bAccK;
   static constexpr int bFinal = 11;
+  static constexpr int bAccB = 12;    // [2] dQ MMA of a visit done, per dS buffer
+  static_assert(kColAcc + D + 128 <= kTmemCols, "dQ kernel: two dS buffers after dQ");
   static constexpr int kHolderOff = kBarBytes - 16;
   static constexpr int kNeverOff = kBarBytes - 12;
   static constexpr int kAbortOff = kBarBytes - 8;
@@ -101,6 +103,15 @@ __device__ __forceinline__ uint32_t pcol(int kk) {
   return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8);
 }
 
+// dQ kernel: the two dS buffers (64 bf16-pair columns each) follow the dQ
+// accumulator; within a buffer the key half hf keeps its 32 columns at
+// hf * 32, so K step kk (16 keys) reads columns (kk / 4) * 32 + (kk % 4) * 8.
+template <int D>
+__host__ __device__ constexpr uint32_t kColDSq() { return kColAcc + D; }
+__device__ __forceinline__ uint32_t dscol(int kk) {
+  return (uint32_t)((kk >> 2) * 32 + (kk & 3) * 8);
+}
+
 template <class C, class BarFn>
 __device__ __forceinline__ void init_barriers(BarFn bar, volatile int* abort_flag,
                                               volatile int* never) {
@@ -117,6 +128,8 @@ __device__ __forceinline__ void init_barriers(BarFn bar, volatile int* abort_fla
     mbar_init(bar(C::bAccV), 1);
     mbar_init(bar(C::bAccK), 1);
     mbar_init(bar(C::bFinal), 1);
+    mbar_init(bar(C::bAccB + 0), 1);
+    mbar_init(bar(C::bAccB + 1), 1);
     *abort_flag = 0;
     *never = 0;
     fence_mbar_init();
@@ -644,7 +657,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
       it.init(g, r, q_lo, q_valid);
       KvTile kv;
       bool have = ok && it.next(g, kv);
-      // S(0)
+      // S(0), dP(0)
       if (have) {
         ok = mbar_wait(bar(C::bFull + 0), 0, abort_flag, kTimeoutNs);
         if (ok) {
@@ -654,30 +667,28 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
             umma_ss(tmem + kColS, q_kmaj + kstep_off(kk), k_kmaj + kstep_off(kk), id_s,
                     kk > 0 ? 1u : 0u);
           umma_commit(bar(C::bS));
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + kColDP, do_kmaj + kstep_off(kk), v_kmaj + kstep_off(kk), id_s,
+                    kk > 0 ? 1u : 0u);
+          umma_commit(bar(C::bDP));
         }
       }
+      // Per visit: S(j+1) once pass 1 has read S(j); dQ(j) once pass 2 has
+      // written dS(j) (into a buffer of its own, alternating); dP(j+1) once
+      // pass 2 has read dP(j). No product waits for another to finish.
       int j = 0;
       while (ok && have) {
         const int st = j & 1;
         const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
-        // dP(j) overwrites the dS(j-1) that dQ(j-1) reads
-        if (j > 0) ok = mbar_wait(bar(C::bAcc), (uint32_t)(j - 1) & 1, abort_flag, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColDP, do_kmaj + kstep_off(kk), v_kmaj + so + kstep_off(kk), id_s,
-                  kk > 0 ? 1u : 0u);
-        umma_commit(bar(C::bDP));
-        // S(j+1), once pass 1 of tile j has read S(j)
         have = it.next(g, kv);
+        const int sn = (j + 1) & 1;
+        const uint64_t son = (uint64_t)((sn * C::kStageBytes) >> 4);
         if (have) {
-          const int sn = (j + 1) & 1;
           ok = mbar_wait(bar(C::bFull + sn), (uint32_t)((j + 1) >> 1) & 1, abort_flag, kTimeoutNs) &&
                mbar_wait(bar(C::bP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t son = (uint64_t)((sn * C::kStageBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             umma_ss(tmem + kColS, q_kmaj + kstep_off(kk), k_kmaj + son + kstep_off(kk), id_s,
@@ -687,12 +698,20 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
         ok = mbar_wait(bar(C::bDS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
+        const uint32_t ds_col = kColDSq<D>() + (uint32_t)(st * 64);
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
-          umma_ts(tmem + kColAcc, tmem + kColDP + pcol(kk), k_mn + so + (uint64_t)(kk * 2048 >> 4),
+          umma_ts(tmem + kColAcc, tmem + ds_col + dscol(kk), k_mn + so + (uint64_t)(kk * 2048 >> 4),
                   id_acc, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(C::bAcc));
+        umma_commit(bar(C::bAccB + st));
         umma_commit(bar(C::bFree + st));
+        if (have) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + kColDP, do_kmaj + kstep_off(kk), v_kmaj + son + kstep_off(kk), id_s,
+                    kk > 0 ? 1u : 0u);
+          umma_commit(bar(C::bDP));
+        }
         ++j;
       }
       umma_commit(bar(C::bFinal));
@@ -759,14 +778,23 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
           pk[i >> 1] = pack_bf16x2(p[i] * (__uint_as_float(d0) - dl_row),
                                    p[i + 1] * (__uint_as_float(d1) - dl_row));
         }
-        tmem_st32(tmem + t_lane + kColDP + c0, pk);
+        // dS buffer j mod 2 was last read by dQ(j-2)
+        if (j >= 2) {
+          ok = mbar_wait(bar(C::bAccB + (j & 1)), (uint32_t)((j >> 1) - 1) & 1, abort_flag,
+                         kTimeoutNs);
+          if (!ok) { ++j; continue; }
+          tc_fence_after();
+        }
+        tmem_st32(tmem + t_lane + kColDSq<D>() + (uint32_t)((j & 1) * 64) + (uint32_t)(hf * 32), pk);
         tmem_st_wait();
       }
       tc_fence_before();
       mbar_arrive(bar(C::bDS));
       ++j;
     }
-    if (ok && j > 0) ok = mbar_wait(bar(C::bAcc), (uint32_t)(j - 1) & 1, abort_flag, kTimeoutNs);
+    if (ok && j > 0)
+      ok = mbar_wait(bar(C::bAccB + ((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1, abort_flag,
+                     kTimeoutNs);
     if (ok) {
       tc_fence_after();
       const bool row_ok = row < q_valid;
