@@ -367,7 +367,8 @@ ra_status ring_attn_expiry_test(const void* q, const void* k, const void* v,
 /* Human-readable text of a status; never NULL. */
 const char* ring_attn_strerror(int status);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor); 103 adds the backward, the
+ * packed variable-length and the Ulysses-layout entry points. */
 int ring_attn_version(void);
 
 #ifdef __cplusplus

@@ -184,6 +184,6 @@ const char* ring_attn_strerror(int status) {
   }
 }
 
-int ring_attn_version(void) { return 100; }
+int ring_attn_version(void) { return 103; }   // 1.03: backward, packed variable lengths, Ulysses layout
 
 }  // extern "C"
