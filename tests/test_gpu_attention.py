@@ -66,6 +66,8 @@ BF16_CASES = [
     (2, 4, 2, 300, 64, 8, True, "zigzag"),         # halves of 19 (last 15)
     (1, 2, 2, 5, 128, 4, True, "contiguous"),      # chunks of 2: the last is empty
     (1, 2, 1, 700, 128, 3, False, "zigzag"),       # non-causal, halves of 117
+    (1, 2, 2, 1, 128, 1, True, "contiguous"),      # a single token
+    (2, 2, 1, 3, 64, 4, True, "zigzag"),           # 3 tokens over 8 halves: most empty
 ]
 
 
@@ -94,6 +96,8 @@ F32_CASES = [
     (1, 2, 2, 24, 128, 12, True, "zigzag"),        # one-token halves
     (1, 2, 2, 250, 64, 4, True, "contiguous"),     # uneven: chunks of 63 (last 61)
     (1, 2, 2, 99, 128, 4, True, "zigzag"),         # uneven: halves of 13 (last 8)
+    (1, 2, 2, 1, 64, 1, False, "contiguous"),      # a single token
+    (1, 2, 2, 3, 64, 4, True, "contiguous"),       # 3 tokens over 4 chunks: one empty
 ]
 
 
