@@ -34,8 +34,8 @@ UNIT = "TFLOP/s"
 
 # ncu DRAM bytes (read + write) of one launch of the tensor-core kernel on the
 # headline workload, valid only for the kernel source with this digest.
-TRAFFIC = {"attn_tc_sha256_16": "d02032bd774996ab", "workload": "bf16_s32k_causal_zigzag",
-           "bytes_per_launch": 806526464 + 254894336}
+TRAFFIC = {"attn_tc_sha256_16": "ced19d8160360adf", "workload": "bf16_s32k_causal_zigzag",
+           "bytes_per_launch": 805783552 + 254530048}
 
 
 def _env_int(name, default):
@@ -61,7 +61,8 @@ def _kernel_digest():
     code change invalidates the stored traffic, a comment edit does not."""
     import re
     code = []
-    for name in ("attn_tc.cu", "fastmath.cuh", "ring_iter.cuh", "sm100.cuh", "ra_internal.h"):
+    for name in ("attn_tc.cu", "checks.cuh", "fastmath.cuh", "ring_iter.cuh", "sm100.cuh",
+                 "ra_internal.h"):
         path = os.path.join(ROOT, "sequence_exact_attention_gb300", "csrc", name)
         with open(path, encoding="utf-8") as f:
             lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in f]

@@ -15,6 +15,8 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libringattn.so")
+LIBRARIES = {"release": LIB_PATH,
+             "debug": os.path.join(_HERE, "_lib", "libringattn_debug.so")}
 
 RA_BF16, RA_F32 = 0, 1
 ORDERS = {"contiguous": 0, "zigzag": 1}
@@ -30,6 +32,7 @@ EXPORTS = ("ring_attn_fwd", "ring_attn_fwd_ex", "ring_attn_visit_log_len",
            "ring_attn_expiry_test", "ring_attn_strerror", "ring_attn_version")
 
 _lib = None
+_lib_path = LIB_PATH
 
 
 class RingAttnError(RuntimeError):
@@ -38,16 +41,28 @@ class RingAttnError(RuntimeError):
         super().__init__(f"{where}: {strerror(status)} (status {status})")
 
 
+def use_library(variant):
+    """Select the library the next calls go through: "release" (the default)
+    or "debug" (the bounds-checked build, same entry points). Returns the
+    variant that was in use."""
+    global _lib, _lib_path
+    prev = next(k for k, p in LIBRARIES.items() if p == _lib_path)
+    if LIBRARIES[variant] != _lib_path:
+        _lib_path = LIBRARIES[variant]
+        _lib = None
+    return prev
+
+
 def load():
-    """Load the shared library once; raises if it was not built."""
+    """Load the selected shared library once; raises if it was not built."""
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
+    if not os.path.exists(_lib_path):
         raise RuntimeError(
-            f"{LIB_PATH} is missing: build it with "
+            f"{_lib_path} is missing: build it with "
             "`python -m sequence_exact_attention_gb300.build` (no CPU fallback)")
-    lib = ctypes.CDLL(LIB_PATH)
+    lib = ctypes.CDLL(_lib_path)
     c_int, c_float, vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
     ip = ctypes.POINTER(ctypes.c_int)
     lib.ring_attn_fwd.restype = c_int

@@ -176,7 +176,7 @@ ra_status ring_attn_fwd_ulysses(const void* q, const void* k, const void* v, voi
   if (dtype == RA_F32)
     return launch_attn_simt_sharded(g, static_cast<const float*>(q),
                                     static_cast<const float*>(k), static_cast<const float*>(v),
-                                    static_cast<float*>(out), lse, s);
+                                    static_cast<float*>(out), lse, dev_status, s);
   return launch_attn_tc_sharded(g, q, k, v, out, lse, dev_status, s);
 }
 
@@ -237,7 +237,7 @@ ra_status ring_attn_fwd_varlen(const void* q, const void* k, const void* v, void
   if (dtype == RA_F32)
     return launch_attn_simt_varlen(g, static_cast<const float*>(q),
                                    static_cast<const float*>(k), static_cast<const float*>(v),
-                                   static_cast<float*>(out), lse, s);
+                                   static_cast<float*>(out), lse, dev_status, s);
   return launch_attn_tc_varlen(g, q, k, v, out, lse, dev_status, s);
 }
 

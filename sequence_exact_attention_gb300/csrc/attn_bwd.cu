@@ -33,6 +33,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "checks.cuh"
 #include "ra_internal.h"
 #include "ring_iter.cuh"
 #include "sm100.cuh"
@@ -145,7 +146,8 @@ template <int D, bool kVarlen>
 __global__ void __launch_bounds__(256)
 bwd_prep_kernel(const Geometry gp, const __nv_bfloat16* __restrict__ out,
                 const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
-                float* __restrict__ lse2, float* __restrict__ delta, long long rows) {
+                float* __restrict__ lse2, float* __restrict__ delta, long long rows,
+                int* __restrict__ status) {
   const long long gid = (long long)blockIdx.x * 32 + (threadIdx.x >> 3);
   const int sub = threadIdx.x & 7;
   if (gid >= rows) return;               // rows is a multiple of 32: whole blocks
@@ -168,9 +170,9 @@ bwd_prep_kernel(const Geometry gp, const __nv_bfloat16* __restrict__ out,
   const bool valid = in_seg < seg_tokens(g, seg);
   const int pos = seg * g.seg_len + in_seg;
   float acc = 0.f;
-  if (valid) {
-    constexpr int E = D / 8;
-    const size_t off = ((srow + pos) * g.H_q + h) * D + (size_t)sub * E;
+  constexpr int E = D / 8;
+  const size_t off = ((srow + pos) * g.H_q + h) * D + (size_t)sub * E;
+  if (valid && in_range((long long)off, E, extent_q(gp), status)) {
     const uint4* po = reinterpret_cast<const uint4*>(out + off);
     const uint4* pd = reinterpret_cast<const uint4*>(dout + off);
 #pragma unroll
@@ -188,7 +190,8 @@ bwd_prep_kernel(const Geometry gp, const __nv_bfloat16* __restrict__ out,
   acc += __shfl_xor_sync(0xffffffffu, acc, 2);
   acc += __shfl_xor_sync(0xffffffffu, acc, 4);
   if (sub == 0) {
-    lse2[gid] = valid ? lse[lrow + pos] * kLog2e : INFINITY;
+    const bool lse_ok = valid && in_range((long long)(lrow + pos), 1, extent_lse(gp), status);
+    lse2[gid] = lse_ok ? lse[lrow + pos] * kLog2e : INFINITY;
     delta[gid] = valid ? acc : 0.f;
   }
 }
@@ -352,7 +355,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
           tma_load_4d(sb + C::kTileBytes + bx * kBoxBytes, &tm_do, bar(C::bFull + st), bx * 64,
                       qt.h, qr.trow + qt.lo, qr.tbat);
         }
-        const long long wi = ws_tile(gp, b * gp.H_q + qt.h, qt.seg, qt.ti);
+        long long wi = ws_tile(gp, b * gp.H_q + qt.h, qt.seg, qt.ti);
+        if (!in_range(wi, kT, ws_tile(gp, gp.B * gp.H_q, 0, 0), status)) wi = 0;
         bulk_load(sb + 2 * C::kTileBytes, lse2 + wi, kT * 4, bar(C::bFull + st));
         bulk_load(sb + 2 * C::kTileBytes + kT * 4, delta + wi, kT * 4, bar(C::bFull + st));
         ++j;
@@ -521,8 +525,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (ok && j > 0) ok = mbar_wait(bar(C::bAccK), (uint32_t)(j - 1) & 1, abort_flag, kTimeoutNs);
     if (ok) {
       tc_fence_after();
-      const bool row_ok = row < kv_valid;
       const size_t off = ((kr.grow + kpos) * g.H_kv + hk) * D;
+      const bool row_ok = row < kv_valid && in_range((long long)off, D, extent_kv(gp), status);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         __nv_bfloat16* dst = (which ? dk : dv) + off;
@@ -727,8 +731,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int q_pos = q_lo + row;
     const float sl2 = g.scale_log2;
     const long long wi = ws_tile(gp, bh, seg, ti) + row;
-    const float l2_row = lse2[wi];      // +inf on padding rows: p = 0
-    const float dl_row = delta[wi];
+    const bool wi_ok = in_range(wi, 1, ws_tile(gp, gp.B * gp.H_q, 0, 0), status);
+    const float l2_row = wi_ok ? lse2[wi] : INFINITY;     // +inf on padding rows: p = 0
+    const float dl_row = wi_ok ? delta[wi] : 0.f;
     KvIter it;
     it.init(g, r, q_lo, q_valid);
     KvTile kv;
@@ -797,8 +802,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                      kTimeoutNs);
     if (ok) {
       tc_fence_after();
-      const bool row_ok = row < q_valid;
-      __nv_bfloat16* dst = dq + ((qr.grow + q_pos) * g.H_q + h) * D;
+      const size_t off = ((qr.grow + q_pos) * g.H_q + h) * D;
+      const bool row_ok = row < q_valid && in_range((long long)off, D, extent_q(gp), status);
+      __nv_bfloat16* dst = dq + off;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         const int col = hf * (D / 2) + c * 32;
@@ -839,7 +845,7 @@ ra_status launch_d(const Geometry& g, const CUtensorMap& mq, const CUtensorMap& 
   if (phases & RA_BWD_PREP) {
     bwd_prep_kernel<D, kVarlen><<<(unsigned)prep_blocks, 256, 0, stream>>>(
         g, static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout),
-        lse, lse2, delta, rows);
+        lse, lse2, delta, rows, status);
     if (cudaGetLastError() != cudaSuccess) return RA_ERR_LAUNCH;
   }
   if (phases & RA_BWD_DKDV) {

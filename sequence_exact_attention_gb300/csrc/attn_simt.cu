@@ -20,6 +20,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "checks.cuh"
 #include "ra_internal.h"
 #include "ring_iter.cuh"
 
@@ -41,7 +42,7 @@ __global__ void __launch_bounds__(kThreads)
 attn_simt_kernel(const Geometry gp, const float* __restrict__ q,
                  const float* __restrict__ k, const float* __restrict__ v,
                  float* __restrict__ out, float* __restrict__ lse,
-                 int* __restrict__ vlog, int log_stride) {
+                 int* __restrict__ vlog, int log_stride, int* __restrict__ status) {
   constexpr int V4 = D / 4;          // float4 per row
   constexpr int NV = V4 / 4;         // float4 per thread
   extern __shared__ float4 smem[];
@@ -82,22 +83,26 @@ attn_simt_kernel(const Geometry gp, const float* __restrict__ q,
   const int q_pos = q_lo + row;
   const bool row_valid = row < q_valid;
 
+  // the visit log of this query tile: [count, 4 ints per visit]
+  const long long log_off = ((long long)bh * n_qt + qid) * log_stride;
+  const long long log_len = (long long)gp.B * gp.H_q * n_qt * log_stride;
   if (q_valid <= 0) {            // a tile of padding only: nothing to compute or write
-    if (vlog && threadIdx.x == 0) vlog[((size_t)bh * n_qt + qid) * log_stride] = 0;
+    if (vlog && threadIdx.x == 0 && in_range(log_off, 1, log_len, status)) vlog[log_off] = 0;
     return;
   }
 
   float4 qv[NV], acc[NV];
-  const float4* qrow = reinterpret_cast<const float4*>(
-      q + ((qrow0 + (row_valid ? q_pos : q_lo)) * g.H_q + h) * D);
+  const long long q_elem = ((long long)(qrow0 + (row_valid ? q_pos : q_lo)) * g.H_q + h) * D;
+  const bool row_ok = row_valid && in_range(q_elem, D, extent_q(gp), status);
+  const float4* qrow = reinterpret_cast<const float4*>(q + q_elem);
 #pragma unroll
   for (int e = 0; e < NV; ++e) {
-    qv[e] = row_valid ? qrow[part + 4 * e] : make_float4(0.f, 0.f, 0.f, 0.f);
+    qv[e] = row_ok ? qrow[part + 4 * e] : make_float4(0.f, 0.f, 0.f, 0.f);
     acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   float m = -INFINITY, l = 0.f;
 
-  int* log_base = vlog ? vlog + ((size_t)bh * n_qt + qid) * log_stride : nullptr;
+  int* log_base = vlog ? vlog + log_off : nullptr;
   int n_vis = 0;
 
   KvIter it;
@@ -105,7 +110,8 @@ attn_simt_kernel(const Geometry gp, const float* __restrict__ q,
   KvTile kv;
   while (it.next(g, kv)) {
     const int work = kv.work;
-    if (log_base && threadIdx.x == 0) log_visit(log_base, n_vis, kv, tile_class(g, q_lo, kv));
+    if (log_base && threadIdx.x == 0 && in_range(log_off + 1 + 4 * n_vis, 4, log_len, status))
+      log_visit(log_base, n_vis, kv, tile_class(g, q_lo, kv));
     ++n_vis;
 
     __syncthreads();    // the previous tile is no longer read
@@ -114,8 +120,8 @@ attn_simt_kernel(const Geometry gp, const float* __restrict__ q,
     for (int idx = threadIdx.x; idx < kRows * V4; idx += kThreads) {
       const int kr = idx / V4, c = idx % V4;
       float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
-      if (kr < kv.valid) {
-        const size_t off = ((krow0 + kv.lo + kr) * g.H_kv + hk) * V4 + c;
+      const size_t off = ((krow0 + kv.lo + kr) * g.H_kv + hk) * V4 + c;
+      if (kr < kv.valid && in_range((long long)off * 4, 4, extent_kv(gp), status)) {
         kk = reinterpret_cast<const float4*>(k)[off];
         vv = reinterpret_cast<const float4*>(v)[off];
       }
@@ -166,7 +172,7 @@ attn_simt_kernel(const Geometry gp, const float* __restrict__ q,
     m = m_new;
   }
 
-  if (row_valid) {
+  if (row_ok) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
     float4* orow = reinterpret_cast<float4*>(
         out + ((qrow0 + q_pos) * g.H_q + h) * D);
@@ -174,17 +180,17 @@ attn_simt_kernel(const Geometry gp, const float* __restrict__ q,
     for (int e = 0; e < NV; ++e)
       orow[part + 4 * e] = make_float4(acc[e].x * inv, acc[e].y * inv,
                                        acc[e].z * inv, acc[e].w * inv);
-    if (part == 0 && lse)
+    if (part == 0 && lse && in_range((long long)(lrow + q_pos), 1, extent_lse(gp), status))
       lse[lrow + q_pos] =
           l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
   }
-  if (log_base && threadIdx.x == 0) log_base[0] = n_vis;
+  if (log_base && threadIdx.x == 0 && in_range(log_off, 1, log_len, status)) log_base[0] = n_vis;
 }
 
 template <int D, bool kVarlen = false>
 ra_status launch_d(const Geometry& g, const float* q, const float* k,
                    const float* v, float* out, float* lse, int* vlog,
-                   int log_stride, cudaStream_t stream) {
+                   int log_stride, int* status, cudaStream_t stream) {
   const int smem = 2 * kRows * D * (int)sizeof(float);
   if (cudaFuncSetAttribute(attn_simt_kernel<D, kVarlen>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -193,32 +199,33 @@ ra_status launch_d(const Geometry& g, const float* q, const float* k,
   const long long grid = (long long)g.n_seg * g.nt * g.B * g.H_q;
   if (grid > 0x7fffffffLL) return RA_ERR_RANGE;
   attn_simt_kernel<D, kVarlen><<<(unsigned)grid, kThreads, smem, stream>>>(
-      g, q, k, v, out, lse, vlog, log_stride);
+      g, q, k, v, out, lse, vlog, log_stride, status);
   return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
 }
 
 }  // namespace
 
 ra_status launch_attn_simt_varlen(const Geometry& g, const float* q, const float* k,
-                                  const float* v, float* out, float* lse, cudaStream_t stream) {
-  if (g.D == 64) return launch_d<64, true>(g, q, k, v, out, lse, nullptr, 0, stream);
-  return launch_d<128, true>(g, q, k, v, out, lse, nullptr, 0, stream);
+                                  const float* v, float* out, float* lse, int* dev_status,
+                                  cudaStream_t stream) {
+  if (g.D == 64) return launch_d<64, true>(g, q, k, v, out, lse, nullptr, 0, dev_status, stream);
+  return launch_d<128, true>(g, q, k, v, out, lse, nullptr, 0, dev_status, stream);
 }
 
 ra_status launch_attn_simt_sharded(const Geometry& g, const float* q, const float* k,
-                                   const float* v, float* out, float* lse, cudaStream_t stream) {
-  if (g.D == 64) return launch_d<64>(g, q, k, v, out, lse, nullptr, 0, stream);
-  return launch_d<128>(g, q, k, v, out, lse, nullptr, 0, stream);
+                                   const float* v, float* out, float* lse, int* dev_status,
+                                   cudaStream_t stream) {
+  if (g.D == 64) return launch_d<64>(g, q, k, v, out, lse, nullptr, 0, dev_status, stream);
+  return launch_d<128>(g, q, k, v, out, lse, nullptr, 0, dev_status, stream);
 }
 
 ra_status launch_attn_simt(const Geometry& g, const float* q, const float* k,
                            const float* v, void* out, float* lse,
                            int* visit_log, int log_stride, int* dev_status,
                            cudaStream_t stream) {
-  (void)dev_status;   // this kernel has no waits that could expire
   float* o = static_cast<float*>(out);
-  if (g.D == 64) return launch_d<64>(g, q, k, v, o, lse, visit_log, log_stride, stream);
-  return launch_d<128>(g, q, k, v, o, lse, visit_log, log_stride, stream);
+  if (g.D == 64) return launch_d<64>(g, q, k, v, o, lse, visit_log, log_stride, dev_status, stream);
+  return launch_d<128>(g, q, k, v, o, lse, visit_log, log_stride, dev_status, stream);
 }
 
 }  // namespace ra

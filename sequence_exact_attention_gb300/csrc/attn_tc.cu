@@ -58,9 +58,10 @@
 #include <cstdint>
 #include <mutex>
 
+#include "checks.cuh"
+#include "fastmath.cuh"
 #include "ra_internal.h"
 #include "ring_iter.cuh"
-#include "fastmath.cuh"
 #include "sm100.cuh"
 
 namespace ra {
@@ -285,8 +286,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   // A tile of padding only (uneven or packed lengths) has nothing to compute
   // or write: the whole CTA leaves before it sets anything up.
+  // the visit log of this query tile: [count, 4 ints per visit]
+  const long long log_off = ((long long)bh * n_qt + qt) * log_stride;
+  const long long log_len = (long long)gp.B * gp.H_q * n_qt * log_stride;
   if (q_valid <= 0) {
-    if (vlog && threadIdx.x == 0) vlog[((size_t)bh * n_qt + qt) * log_stride] = 0;
+    if (vlog && threadIdx.x == 0 && in_range(log_off, 1, log_len, status)) vlog[log_off] = 0;
     return;
   }
 
@@ -467,9 +471,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     // [kSplit][128] partial sums
     float* red = reinterpret_cast<float*>(base_ptr + C::kRedOff);
 
-    int* log_base = (vlog && threadIdx.x == 0)
-                        ? vlog + ((size_t)bh * n_qt + qt) * log_stride
-                        : nullptr;
+    int* log_base = (vlog && threadIdx.x == 0) ? vlog + log_off : nullptr;
 
     float m_run = -INFINITY, l_run = 0.f;    // l_run: this part's partial sum
     int j = 0;               // key tiles done (= P tiles published)
@@ -485,7 +487,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     bool have = it.next(g, kv);
     while (have) {
       const int work = kv.work;
-      if (log_base) log_visit(log_base, j, kv, tile_class(g, q_lo, kv));
+      if (log_base && in_range(log_off + 1 + 4 * j, 4, log_len, status))
+        log_visit(log_base, j, kv, tile_class(g, q_lo, kv));
       const int bb = j % kBuf;
       const uint32_t u = (uint32_t)(j / kBuf);
       const uint32_t tS = tmem + t_lane + s_col(bb) + part * kSCols;
@@ -604,7 +607,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       kv = nxt;
       have = have_next;
     }
-    if (log_base) log_base[0] = j;
+    if (log_base && in_range(log_off, 1, log_len, status)) log_base[0] = j;
 
     // ---- epilogue: out = O / l, lse = ln2 * (m + log2 l), l = sum of the parts
     float* red_l = red + 2 * kSplit * 128;
@@ -621,8 +624,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (ok) {
       const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
       const size_t row_off = ((orow + q_pos) * g.H_q + h) * D + part * kOC;
-      store_out_cols<kOC, kOutF32>(tO, j > 0, row_valid, out, row_off, inv_l);
-      if (row_valid && lse && part == 0)
+      const bool store = row_valid && in_range((long long)row_off, kOC, extent_q(gp), status);
+      store_out_cols<kOC, kOutF32>(tO, j > 0, store, out, row_off, inv_l);
+      if (row_valid && lse && part == 0 &&
+          in_range((long long)(lrow + q_pos), 1, extent_lse(gp), status))
         lse[lrow + q_pos] =
             l_tot > 0.f ? (m_run + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
     }

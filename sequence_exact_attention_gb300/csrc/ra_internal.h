@@ -62,13 +62,15 @@ ra_status launch_attn_tc_varlen(const Geometry& g, const void* q, const void* k,
                                 const void* v, void* out, float* lse, int* dev_status,
                                 cudaStream_t stream);
 ra_status launch_attn_simt_varlen(const Geometry& g, const float* q, const float* k,
-                                  const float* v, float* out, float* lse, cudaStream_t stream);
+                                  const float* v, float* out, float* lse, int* dev_status,
+                                  cudaStream_t stream);
 // Sequence-sharded layout launches (g.shard_rows set, no visit log, all steps).
 ra_status launch_attn_tc_sharded(const Geometry& g, const void* q, const void* k,
                                  const void* v, void* out, float* lse, int* dev_status,
                                  cudaStream_t stream);
 ra_status launch_attn_simt_sharded(const Geometry& g, const float* q, const float* k,
-                                   const float* v, float* out, float* lse, cudaStream_t stream);
+                                   const float* v, float* out, float* lse, int* dev_status,
+                                   cudaStream_t stream);
 ra_status launch_attn_tc(const Geometry& g, const void* q, const void* k,
                          const void* v, void* out, float* lse, int* visit_log,
                          int log_stride, int* dev_status, int sm_count,

@@ -38,6 +38,26 @@ def test_library_exports_every_declared_symbol(lib):
     assert lib.ring_attn_version() >= 103
 
 
+def test_checked_build_exports_the_same_symbols(lib):
+    """The bounds-checked build loads without a GPU and has the same ABI."""
+    path = binding.LIBRARIES["debug"]
+    assert os.path.exists(path), "the build makes both libraries"
+    dbg = ctypes.CDLL(path)
+    for n in _header_functions():
+        assert hasattr(dbg, n), f"{n} not exported by the checked build"
+    dbg.ring_attn_version.restype = ctypes.c_int
+    assert dbg.ring_attn_version() == lib.ring_attn_version()
+
+
+def test_use_library_switches_and_restores():
+    prev = binding.use_library("debug")
+    try:
+        assert binding._lib_path == binding.LIBRARIES["debug"]
+    finally:
+        binding.use_library(prev)
+    assert binding._lib_path == binding.LIBRARIES[prev]
+
+
 def test_strerror_covers_every_status(lib):
     seen = set()
     for st in range(0, 11):
