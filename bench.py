@@ -30,12 +30,39 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "ring-attn fwd TFLOP/s, bf16 S=32K causal, 1 GB300; % of dense BF16 peak"
+
+
+def _fwd_metric(w):
+    """The headline metric for the headline workload; the other forward
+    workloads name themselves."""
+    from sequence_exact_attention_gb300.workloads import HEADLINE
+    if w.name == HEADLINE:
+        return METRIC
+    return f"ring-attn fwd TFLOP/s, {w.name}, 1 GB300"
+
+
 UNIT = "TFLOP/s"
 
-# ncu DRAM bytes (read + write) of one launch of the tensor-core kernel on the
-# headline workload, valid only for the kernel source with this digest.
-TRAFFIC = {"attn_tc_sha256_16": "ced19d8160360adf", "workload": "bf16_s32k_causal_zigzag",
-           "bytes_per_launch": 805783552 + 254530048}
+# ncu DRAM bytes (read + write) of one launch of the timed kernel, per
+# workload; an entry holds only while the kernel's sources have the digest
+# stored with it (see _kernel_digest).
+TRAFFIC = {
+    "attn_tc": {"sha256_16": "ced19d8160360adf", "bytes_per_launch": {
+        "bf16_s32k_causal_zigzag": 805783552 + 254530048,
+        "bf16_s16k_d64": 402806784 + 117399808,
+        "bf16_s128k_gqa_causal": 3068165120 + 1055448064,
+        "bf16_varlen_32k_causal_zigzag": 810178048 + 251862528,
+        "bf16_ulysses_s16k_b2_causal": 805466624 + 250964992,
+    }},
+    "merge": {"sha256_16": "110b882547236ed1", "bytes_per_launch": {
+        "merge_p8_s64k": 8657131264 + 1038706688,
+    }},
+}
+KERNEL_SOURCES = {
+    "attn_tc": ("attn_tc.cu", "checks.cuh", "fastmath.cuh", "ring_iter.cuh", "sm100.cuh",
+                "ra_internal.h"),
+    "merge": ("merge.cu", "ra_internal.h"),
+}
 
 
 def _env_int(name, default):
@@ -55,19 +82,27 @@ def _peaks():
                 "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def _kernel_digest():
-    """sha256 (first 16 hex) of the forward kernel's sources -- attn_tc.cu and
-    the headers it includes -- with // comments and blank lines removed: any
-    code change invalidates the stored traffic, a comment edit does not."""
+def _kernel_digest(kernel="attn_tc"):
+    """sha256 (first 16 hex) of a kernel's sources -- its .cu file and the
+    headers it includes -- with // comments and blank lines removed: any code
+    change invalidates the stored traffic, a comment edit does not."""
     import re
     code = []
-    for name in ("attn_tc.cu", "checks.cuh", "fastmath.cuh", "ring_iter.cuh", "sm100.cuh",
-                 "ra_internal.h"):
+    for name in KERNEL_SOURCES[kernel]:
         path = os.path.join(ROOT, "sequence_exact_attention_gb300", "csrc", name)
         with open(path, encoding="utf-8") as f:
             lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in f]
         code.append("\n".join(ln for ln in lines if ln.strip()))
     return hashlib.sha256("\n".join(code).encode()).hexdigest()[:16]
+
+
+def _traffic(kernel, workload):
+    """Stored DRAM bytes per launch of `kernel` on `workload`, or None when
+    none was captured or the kernel's sources changed since."""
+    entry = TRAFFIC[kernel]
+    if entry["sha256_16"] != _kernel_digest(kernel):
+        return None
+    return entry["bytes_per_launch"].get(workload)
 
 
 class ClockSampler:
@@ -208,7 +243,7 @@ def run_reference(args, w):
     sample = (f"{rows_per_step} random query rows x all {w.H_q} heads per step "
               f"(float64 NumPy oracle, full key range per row)")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "impl": "reference", "metric": _fwd_metric(w), "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -378,10 +413,7 @@ def run_ours(args, w):
         bound, peak = "tensor", float(peaks.get("bf16_tflops"))
         peak_note = f"{peak_src} bf16 dense (burst)"
         kname = f"attn_tc_kernel<{w.D},false,false>"
-        digest = _kernel_digest()
-        traffic = (TRAFFIC["bytes_per_launch"]
-                   if TRAFFIC["attn_tc_sha256_16"] == digest and w.name == TRAFFIC.get("workload")
-                   else None)
+        traffic = _traffic("attn_tc", w.name)
     else:
         # exact fp32 FMA path: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz
         bound, peak = "alu", 152 * 128 * 2 * 2.07e9 / 1e12
@@ -398,7 +430,7 @@ def run_ours(args, w):
                          f"workload, float64 NumPy oracle, {dt:.1f} s"}
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "metric": _fwd_metric(w), "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
@@ -641,7 +673,7 @@ def _layout_line(args, world, metric, w, cfg, flop, total_ms, kernel_ms, clk, cp
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": cfg,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": _traffic("attn_tc", w.name),
                      "peak_source": f"{peak_src} bf16 dense (burst)",
                      "kernel": f"attn_tc_kernel<{w.D},false,...>", "kernel_ms": kernel_ms,
                      "frac_of_sustained_peak": achieved / float(peaks["bf16_tflops_sustained"])},
@@ -789,7 +821,8 @@ def run_merge(args, w):
         "config": {"workload": w.name, "n": w.n, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
                    "l2": "inputs larger than L2 (8 GiB of partials)"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]),
-                     "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]), "traffic": None,
+                     "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]),
+                     "traffic": _traffic("merge", w.name),
                      "peak_source": f"{src} HBM copy", "kernel": "lse_merge_kernel",
                      "kernel_ms": kernel_ms},
         "clocks": clk, "gpu_launches": args.steps,
