@@ -1,0 +1,100 @@
+"""Host-side checks of bench.py's bookkeeping; no GPU work.
+
+* every stored DRAM-traffic entry names a workload the bench can run, and is
+  reported only while the kernel's sources still have the stored digest;
+* the digest ignores comments and blank lines but not code;
+* the FLOP and byte counts behind the reported rates match what they count:
+  allowed (query, key) pairs, and the bytes of the merge's tensors.
+"""
+
+import os
+
+import pytest
+
+import bench
+from sequence_exact_attention_gb300 import workloads as wl
+
+
+def _all_names():
+    return (set(wl.WORKLOADS) | set(wl.MERGE_WORKLOADS) | set(wl.VARLEN_WORKLOADS)
+            | set(wl.ULYSSES_WORKLOADS) | set(wl.BWD_WORKLOADS))
+
+
+def test_traffic_entries_name_real_workloads():
+    names = _all_names()
+    for kernel, entry in bench.TRAFFIC.items():
+        assert kernel in bench.KERNEL_SOURCES
+        for w, nbytes in entry["bytes_per_launch"].items():
+            assert w in names, f"{kernel}: unknown workload {w}"
+            assert nbytes > 0
+
+
+def test_traffic_follows_the_source_digest(monkeypatch):
+    w = wl.HEADLINE
+    digest = bench._kernel_digest("attn_tc")
+    entry = dict(bench.TRAFFIC["attn_tc"])
+    monkeypatch.setitem(bench.TRAFFIC, "attn_tc", dict(entry, sha256_16=digest))
+    assert bench._traffic("attn_tc", w) == entry["bytes_per_launch"][w]
+    assert bench._traffic("attn_tc", "no_such_workload") is None
+    monkeypatch.setitem(bench.TRAFFIC, "attn_tc", dict(entry, sha256_16="0" * 16))
+    assert bench._traffic("attn_tc", w) is None
+
+
+def test_digest_ignores_comments_not_code(tmp_path, monkeypatch):
+    csrc = tmp_path / "sequence_exact_attention_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setitem(bench.KERNEL_SOURCES, "probe", ("k.cu",))
+    src = csrc / "k.cu"
+    src.write_text("int f() {\n  return 1;\n}\n")
+    d0 = bench._kernel_digest("probe")
+    src.write_text("// a comment\nint f() {  // trailing\n\n  return 1;\n}\n")
+    assert bench._kernel_digest("probe") == d0
+    src.write_text("int f() {\n  return 2;\n}\n")
+    assert bench._kernel_digest("probe") != d0
+
+
+def test_recorded_digests_cover_existing_sources():
+    for kernel, files in bench.KERNEL_SOURCES.items():
+        for name in files:
+            path = os.path.join(bench.ROOT, "sequence_exact_attention_gb300", "csrc", name)
+            assert os.path.exists(path), path
+
+
+def _allowed_pairs(S, causal):
+    return sum((i + 1) if causal else S for i in range(S))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_flop_counts_allowed_pairs(causal):
+    """4*D FLOP per allowed (query, key) pair; the causal count is the usual
+    S^2/2 convention, within S/2 pairs of the exact S(S+1)/2."""
+    S, D, B, H = 96, 64, 2, 3
+    w = wl.AttnWorkload("t", "bf16", B, H, H, S, D, 4, causal, "contiguous")
+    exact = 4.0 * D * B * H * _allowed_pairs(S, causal)
+    assert abs(w.flop - exact) <= 4.0 * D * B * H * S / 2
+    if not causal:
+        assert w.flop == exact
+    assert wl.bwd_flop(w) == 2.5 * w.flop
+
+
+def test_varlen_flop_is_the_sum_over_sequences():
+    for w in wl.VARLEN_WORKLOADS.values():
+        per_seq = sum(wl.AttnWorkload("s", w.dtype, 1, w.H_q, w.H_kv, n, w.D, w.P, w.causal,
+                                      w.order).flop for n in w.lengths)
+        assert w.flop == pytest.approx(per_seq)
+
+
+def test_merge_bytes_equal_the_tensors_read_and_written():
+    w = wl.MergeWorkload("t", "f32", 3, 1, 2, 8, 64, seed=1)
+    os_, ls = wl.make_merge_parts(w)
+    read = sum(t.numel() * t.element_size() for t in os_ + ls)
+    written = os_[0].numel() * os_[0].element_size() + ls[0].numel() * ls[0].element_size()
+    assert w.bytes == read + written
+
+
+def test_headline_metric_names_only_the_headline():
+    assert bench._fwd_metric(wl.WORKLOADS[wl.HEADLINE]) == bench.METRIC
+    for name, w in wl.WORKLOADS.items():
+        if name != wl.HEADLINE:
+            assert name in bench._fwd_metric(w)
