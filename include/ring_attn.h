@@ -48,6 +48,11 @@
  *    RA_ERR_LAUNCH. A device-side bounded wait that expired is reported in
  *    `dev_status` (where the call takes one) as RA_ERR_TIMEOUT, after the
  *    stream has run the kernel.
+ *  - Two builds export this same ABI: libringattn.so and the bounds-checked
+ *    libringattn_debug.so. In the checked build every global-memory access
+ *    a kernel computes from indices is tested against its tensor's extent.
+ *    A violation skips the access and sets RA_ERR_RANGE in `dev_status`;
+ *    there is no trap. In the release build the checks compile away.
  *  - `scale <= 0` means 1/sqrt(D).
  *  - Tensors stay in natural token order in every chunk order: the order only
  *    decides which virtual rank owns which tokens and the sequence of steps.
@@ -72,7 +77,9 @@ typedef enum {
   RA_ERR_LAUNCH = 7,   /* CUDA runtime error while preparing or launching          */
   RA_ERR_TIMEOUT = 8,  /* a device-side bounded wait expired (dev_status only)     */
   RA_ERR_BUFFER = 9,   /* a caller buffer is too small                             */
-  RA_ERR_RANGE = 10    /* a size overflows 32-bit indexing, or step out of range   */
+  RA_ERR_RANGE = 10    /* a size overflows 32-bit indexing, or step out of range;
+                          in dev_status (checked build only): a device index out
+                          of its tensor's range                                   */
 } ra_status;
 
 typedef enum { RA_BF16 = 0, RA_F32 = 1 } ra_dtype;
