@@ -53,6 +53,7 @@ TRAFFIC = {
         "bf16_s128k_gqa_causal": 3068165120 + 1055448064,
         "bf16_varlen_32k_causal_zigzag": 810178048 + 251862528,
         "bf16_ulysses_s16k_b2_causal": 805466624 + 250964992,
+        "bf16_s32760_uneven_causal_zigzag": 808057856 + 251618304,
     }},
     "merge": {"sha256_16": "110b882547236ed1", "bytes_per_launch": {
         "merge_p8_s64k": 8657131264 + 1038706688,

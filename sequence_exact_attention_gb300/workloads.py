@@ -88,6 +88,11 @@ WORKLOADS = {
         "contiguous", k_shift_odd=3.0, seed=1004),
     "bf16_s16k_d64": AttnWorkload("bf16_s16k_d64", "bf16", 4, 16, 16, 16384,
                                   64, 4, False, "contiguous", seed=1006),
+    # Uneven chunks: S = 32760 is not a multiple of 2P = 16, so every zig-zag
+    # half spans ceil(S / 2P) = 2048 positions and the last one holds 2040.
+    "bf16_s32760_uneven_causal_zigzag": AttnWorkload(
+        "bf16_s32760_uneven_causal_zigzag", "bf16", 1, 32, 32, 32760, 128, 8, True,
+        "zigzag", std=0.5, seed=1009),
 }
 
 MERGE_WORKLOADS = {

@@ -55,12 +55,13 @@ def test_workload_full(name):
 
 
 @pytest.mark.parametrize("name", ["bf16_s32k_causal_zigzag", "bf16_s128k_gqa_causal",
-                                  "bf16_s16k_d64"])
+                                  "bf16_s16k_d64", "bf16_s32760_uneven_causal_zigzag"])
 def test_workload_sampled(name):
     w = WORKLOADS[name]
-    log = name == "bf16_s32k_causal_zigzag"
+    log = name in ("bf16_s32k_causal_zigzag", "bf16_s32760_uneven_causal_zigzag")
     q, k, v, out, lse, vlog, lay = _run(w, log=log)
-    seg = w.S // (2 * w.P if w.order == "zigzag" else w.P)
+    # segment length: S / parts, rounded up when the parts do not divide S
+    seg = -(-w.S // (2 * w.P if w.order == "zigzag" else w.P))
     rows = sample_rows(w.S, seg, 48, seed=w.seed)
     want_o, want_l = oracle.attention_rows(q, k, v, w.causal, w.scale, rows)
     assert_close(out[:, rows], want_o, w.dtype, "out")
