@@ -279,3 +279,32 @@ def test_valid_call_without_gpu_reports_device_error(lib):
     assert _fwd(lib) == RA_ERR_DEVICE
     assert _bwd(lib) == RA_ERR_DEVICE
     assert _fwd_varlen(lib) == RA_ERR_DEVICE
+
+
+def test_binding_refuses_host_tensors():
+    """No CPU fallback: every compute entry of the binding refuses tensors
+    that are not on a CUDA device before it calls the library."""
+    import torch
+    q = torch.zeros(1, 128, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        binding.ring_attn_fwd(q, q, q, 2, True)
+    with pytest.raises(ValueError):
+        binding.ring_attn_bwd(q, q, q, q, torch.zeros(1, 2, 128), q, 2, True)
+    with pytest.raises(ValueError):
+        binding.attn_lse_merge(q.float(), torch.zeros(1, 2, 128), q.float(),
+                               torch.zeros(1, 2, 128))
+    cu = torch.tensor([0, 128], dtype=torch.int32)
+    with pytest.raises(ValueError):
+        binding.ring_attn_fwd_varlen(q[0], q[0], q[0], cu, 128, 2, True)
+    s = q.view(2, 1, 64, 2, 64)
+    with pytest.raises(ValueError):
+        binding.ring_attn_fwd_ulysses(s, s, s, 128, True)
+
+
+def test_missing_library_raises(monkeypatch, tmp_path):
+    """A missing shared library is an error at the first call, not a
+    fallback."""
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "_lib_path", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        binding.load()
