@@ -1,0 +1,84 @@
+// Host build of the kernels' ring bookkeeping (csrc/ring_iter.cuh) and the
+// host planner (csrc/plan.cpp), for the CPU tests in test_iter_cpu.py. The
+// functions below walk the key tiles of one query tile exactly as every role
+// of the attention kernels does, so the walk can be compared with the
+// oracle's tile_visits on many shapes without a GPU.
+#include <algorithm>
+namespace ra {
+using std::max;
+using std::min;
+}  // namespace ra
+#define __ldg(p) (*(p))
+#include "ring_iter.cuh"
+
+namespace {
+
+// The kernel's walk for query tile (seg, ti) of geometry g: entries
+// (step, src, kv tile id, class), at most `cap`; returns the count (0 for a
+// tile that holds no token, like the kernels' early exit).
+int walk(const ra::Geometry& g, int seg, int ti, int* out, int cap) {
+  const int r = ra::seg_owner(g, seg);
+  const int q_lo = seg * g.seg_len + ti * g.tile;
+  const int q_valid = ra::tile_tokens(g, seg, ti);
+  if (q_valid <= 0) return 0;
+  ra::KvIter it;
+  it.init(g, r, q_lo, q_valid);
+  ra::KvTile kv;
+  int n = 0;
+  while (it.next(g, kv)) {
+    if (n < cap) {
+      out[4 * n + 0] = kv.step;
+      out[4 * n + 1] = kv.src;
+      out[4 * n + 2] = kv.id;
+      out[4 * n + 3] = ra::tile_class(g, q_lo, kv);
+    }
+    ++n;
+  }
+  return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Geometry facts: [seg_len, n_seg, nt]; returns the planner's status.
+int ra_test_geometry(int S, int P, int order, int tile, int* facts) {
+  ra::Geometry g;
+  const int st = ra::make_geometry(1, 1, 1, S, 128, P, 1, 0.f, order, -1, tile, &g);
+  if (st != RA_OK) return st;
+  facts[0] = g.seg_len;
+  facts[1] = g.n_seg;
+  facts[2] = g.nt;
+  return RA_OK;
+}
+
+// Walk of query tile `qid` (= segment * nt + tile) of a fixed-length call.
+int ra_test_walk(int S, int P, int causal, int order, int tile, int step, int qid, int* out,
+                 int cap) {
+  ra::Geometry g;
+  if (ra::make_geometry(1, 1, 1, S, 128, P, causal, 0.f, order, step, tile, &g) != RA_OK)
+    return -1;
+  return walk(g, qid / g.nt, qid % g.nt, out, cap);
+}
+
+// Walk of query tile (seg, ti) of packed sequence b, with the grid's
+// geometry sized by max_seqlen as the launchers size it; row0 receives the
+// sequence's first row and facts its [S, seg_len, nt].
+int ra_test_walk_varlen(const int* cu_seqlens, int n_seq, int total, int max_seqlen, int P,
+                        int causal, int order, int tile, int b, int seg, int ti, int* out,
+                        int cap, int* row0, int* facts) {
+  ra::Geometry gp;
+  if (ra::make_geometry(n_seq, 1, 1, max_seqlen, 128, P, causal, 0.f, order, -1, tile, &gp) !=
+      RA_OK)
+    return -1;
+  gp.cu_seqlens = cu_seqlens;
+  gp.total = total;
+  ra::Geometry g;
+  ra::varlen_geometry(gp, b, g, *row0);
+  facts[0] = g.S;
+  facts[1] = g.seg_len;
+  facts[2] = g.nt;
+  return walk(g, seg, ti, out, cap);
+}
+
+}  // extern "C"

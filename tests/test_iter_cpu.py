@@ -1,0 +1,159 @@
+"""The attention kernels' key-tile walk, compiled for the host, against the
+oracle's tile_visits on many shapes (no GPU).
+
+Every role of the attention kernels walks the ring with the same code
+(csrc/ring_iter.cuh: segment ownership, segment and tile lengths clipped at
+S, the ring order of steps and segments, causal skipping) on a geometry the
+host planner (csrc/plan.cpp) builds. tests/iter_harness.cpp compiles both
+unchanged with g++ and walks one query tile as a kernel does. The GPU visit
+log checks the same walk on a few shapes; here it is compared entry by entry
+-- (step, source rank, key tile id, FULL/PARTIAL) -- with oracle.tile_visits
+for even and uneven lengths, every P up to 8, both orders, causal or not,
+both tile heights, single ring steps, and packed sequences, including
+malformed offset tables (which the kernels clamp).
+"""
+
+import ctypes
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle.schedule import segment_length
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "sequence_exact_attention_gb300", "csrc")
+CUDA = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+ORDERS = {"contiguous": 0, "zigzag": 1}
+ORACLE_ORDER = {"contiguous": oracle.ORDER_CONTIGUOUS, "zigzag": oracle.ORDER_ZIGZAG}
+CAP = 1 << 16
+
+
+@pytest.fixture(scope="module")
+def harness(tmp_path_factory):
+    gxx = shutil.which("g++")
+    if gxx is None or not os.path.exists(os.path.join(CUDA, "include", "cuda_runtime.h")):
+        pytest.skip("g++ or the CUDA headers are not available")
+    out = str(tmp_path_factory.mktemp("iter") / "libiter.so")
+    cmd = [gxx, "-std=c++17", "-O1", "-shared", "-fPIC", "-I", CSRC,
+           "-I", os.path.join(ROOT, "include"), "-I", os.path.join(CUDA, "include"),
+           os.path.join(ROOT, "tests", "iter_harness.cpp"), os.path.join(CSRC, "plan.cpp"),
+           "-L", os.path.join(CUDA, "lib64"), "-Wl,-rpath," + os.path.join(CUDA, "lib64"),
+           "-lcudart", "-o", out]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+    lib = ctypes.CDLL(out)
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.ra_test_geometry.argtypes = [ctypes.c_int] * 4 + [ip]
+    lib.ra_test_walk.argtypes = [ctypes.c_int] * 7 + [ip, ctypes.c_int]
+    lib.ra_test_walk_varlen.argtypes = ([ip] + [ctypes.c_int] * 10 + [ip, ctypes.c_int, ip, ip])
+    return lib
+
+
+def _buf(n):
+    return (ctypes.c_int * n)()
+
+
+def _walk(lib, S, P, causal, order, tile, step, qid):
+    out = _buf(4 * CAP)
+    n = lib.ra_test_walk(S, P, int(causal), ORDERS[order], tile, step, qid, out, CAP)
+    assert 0 <= n <= CAP
+    return [tuple(out[4 * i:4 * i + 4]) for i in range(n)]
+
+
+def _geometry(lib, S, P, order, tile):
+    f = _buf(3)
+    assert lib.ra_test_geometry(S, P, ORDERS[order], tile, f) == 0
+    return f[0], f[1], f[2]
+
+
+def _check_all_tiles(lib, S, P, causal, order, tile, step=-1):
+    want = oracle.tile_visits(S, P, causal, ORACLE_ORDER[order], tile)
+    seg_len, n_seg, nt = _geometry(lib, S, P, order, tile)
+    assert seg_len == segment_length(S, P, ORACLE_ORDER[order])
+    assert len(want) == n_seg * nt
+    for qid, w in enumerate(want):
+        if step >= 0:
+            w = [e for e in w if e[0] == step]
+        got = _walk(lib, S, P, causal, order, tile, step, qid)
+        assert got == [tuple(e) for e in w], (S, P, causal, order, tile, step, qid)
+
+
+SMALL_S = [1, 2, 5, 63, 64, 65, 127, 128, 129, 255, 256, 300, 777, 1000, 1001, 1023]
+
+
+@pytest.mark.parametrize("order", ["contiguous", "zigzag"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 8])
+def test_walk_matches_oracle_small(harness, order, causal, P):
+    for S in SMALL_S:
+        for tile in (64, 128):
+            _check_all_tiles(harness, S, P, causal, order, tile)
+
+
+@pytest.mark.parametrize("S,P,order", [(4096, 8, "contiguous"), (4100, 8, "zigzag"),
+                                       (16384, 4, "contiguous"), (32760, 8, "zigzag"),
+                                       (32768, 8, "zigzag")])
+def test_walk_matches_oracle_workload_sizes(harness, S, P, order):
+    _check_all_tiles(harness, S, P, True, order, 128)
+
+
+@pytest.mark.parametrize("order", ["contiguous", "zigzag"])
+def test_single_step_walk_is_that_step_of_the_ring(harness, order):
+    for S in (300, 1001):
+        for P in (2, 4):
+            for t in range(P):
+                _check_all_tiles(harness, S, P, True, order, 128, step=t)
+                _check_all_tiles(harness, S, P, False, order, 64, step=t)
+
+
+def _clamped_length(cu, b, total, max_seqlen):
+    lo = min(max(int(cu[b]), 0), total)
+    hi = min(max(int(cu[b + 1]), lo), total)
+    return lo, min(hi - lo, max_seqlen)
+
+
+def _check_varlen(lib, cu, total, max_seqlen, P, causal, order, tile):
+    n_seq = len(cu) - 1
+    carr = (ctypes.c_int * len(cu))(*[int(x) for x in cu])
+    # the grid's geometry: sized by max_seqlen
+    _, n_seg, nt_grid = _geometry(lib, max_seqlen, P, order, tile)
+    for b in range(n_seq):
+        row0_want, S_b = _clamped_length(cu, b, total, max_seqlen)
+        want = oracle.tile_visits(S_b, P, causal, ORACLE_ORDER[order], tile) if S_b > 0 else []
+        seg_len_b = -(-S_b // n_seg)             # ceil: the sequence's own chunks
+        nt_b = -(-seg_len_b // tile)
+        for seg in range(n_seg):
+            for ti in range(nt_grid):
+                out, row0, facts = _buf(4 * CAP), ctypes.c_int(), _buf(3)
+                n = lib.ra_test_walk_varlen(carr, n_seq, total, max_seqlen, P, int(causal),
+                                            ORDERS[order], tile, b, seg, ti, out, CAP,
+                                            ctypes.byref(row0), facts)
+                assert row0.value == row0_want and facts[0] == S_b
+                got = [tuple(out[4 * i:4 * i + 4]) for i in range(n)]
+                if ti < nt_b:
+                    assert got == [tuple(e) for e in want[seg * nt_b + ti]], (cu, b, seg, ti)
+                else:
+                    assert got == [], (cu, b, seg, ti)      # a tile past the sequence
+
+
+@pytest.mark.parametrize("order", ["contiguous", "zigzag"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_walk_is_each_sequences_own_ring(harness, order, causal):
+    lengths = [300, 0, 1, 777, 128, 1000]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    _check_varlen(harness, cu, int(cu[-1]), max(lengths), 4, causal, order, 128)
+    _check_varlen(harness, cu, int(cu[-1]), max(lengths), 3, causal, order, 64)
+
+
+@pytest.mark.parametrize("cu,total,max_seqlen", [
+    ([0, 500, 300, 900], 900, 600),     # decreasing offset: an empty sequence
+    ([0, 400, 1200], 1000, 800),        # past the tensors' end: clipped at total
+    ([-50, 200, 260], 260, 300),        # negative offset: clamped to 0
+    ([0, 700, 900], 900, 256),          # longer than max_seqlen: clipped to it
+])
+def test_varlen_walk_clamps_malformed_tables(harness, cu, total, max_seqlen):
+    _check_varlen(harness, np.asarray(cu), total, max_seqlen, 2, True, "zigzag", 128)
