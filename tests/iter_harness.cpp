@@ -1,8 +1,9 @@
-// Host build of the kernels' ring bookkeeping (csrc/ring_iter.cuh) and the
-// host planner (csrc/plan.cpp), for the CPU tests in test_iter_cpu.py. The
-// functions below walk the key tiles of one query tile exactly as every role
-// of the attention kernels does, so the walk can be compared with the
-// oracle's tile_visits on many shapes without a GPU.
+// Host build of the kernels' ring bookkeeping (csrc/ring_iter.cuh), the
+// checked build's range checks (csrc/checks.cuh) and the host planner
+// (csrc/plan.cpp), for the CPU tests in test_iter_cpu.py. The functions
+// below walk the key tiles of one query tile exactly as every role of the
+// attention kernels does, so the walk can be compared with the oracle's
+// tile_visits on many shapes without a GPU.
 #include <algorithm>
 namespace ra {
 using std::max;
@@ -10,6 +11,10 @@ using std::min;
 }  // namespace ra
 #define __ldg(p) (*(p))
 #include "ring_iter.cuh"
+// the checked build's range checks, with the device atomic as a plain store
+#define RA_DEBUG_CHECKS
+#define atomicExch(p, v) (*(p) = (v))
+#include "checks.cuh"
 
 namespace {
 
@@ -79,6 +84,34 @@ int ra_test_walk_varlen(const int* cu_seqlens, int n_seq, int total, int max_seq
   facts[1] = g.seg_len;
   facts[2] = g.nt;
   return walk(g, seg, ti, out, cap);
+}
+
+// The checked build's tensor extents for a geometry: layout 0 fixed-length
+// [B, S, H, D], 1 packed (`total` rows), 2 sequence-sharded (P * B * C rows);
+// ext = [q/out, k/v, lse] in elements.
+int ra_test_extents(int layout, int B, int H_q, int H_kv, int S, int D, int P, int total,
+                    long long* ext) {
+  ra::Geometry g;
+  if (ra::make_geometry(B, H_q, H_kv, S, D, P, 1, 0.f, RA_ORDER_CONTIGUOUS, -1, 128, &g) !=
+      RA_OK)
+    return -1;
+  static const int kDummy[2] = {0, 0};
+  if (layout == 1) {
+    g.cu_seqlens = kDummy;
+    g.total = total;
+  } else if (layout == 2) {
+    g.shard_rows = g.seg_len;
+  }
+  ext[0] = ra::extent_q(g);
+  ext[1] = ra::extent_kv(g);
+  ext[2] = ra::extent_lse(g);
+  return 0;
+}
+
+// One range check as the checked kernels make it: 1 if in range; else 0 and
+// *status = RA_ERR_RANGE.
+int ra_test_in_range(long long first, long long count, long long extent, int* status) {
+  return ra::in_range(first, count, extent, status) ? 1 : 0;
 }
 
 }  // extern "C"

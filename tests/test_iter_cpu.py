@@ -10,7 +10,9 @@ log checks the same walk on a few shapes; here it is compared entry by entry
 -- (step, source rank, key tile id, FULL/PARTIAL) -- with oracle.tile_visits
 for even and uneven lengths, every P up to 8, both orders, causal or not,
 both tile heights, single ring steps, and packed sequences, including
-malformed offset tables (which the kernels clamp).
+malformed offset tables (which the kernels clamp). The checked build's range
+checks (csrc/checks.cuh) are built the same way: the tensor extents of each
+layout and the boundary of a check.
 """
 
 import ctypes
@@ -50,6 +52,8 @@ def harness(tmp_path_factory):
     lib.ra_test_geometry.argtypes = [ctypes.c_int] * 4 + [ip]
     lib.ra_test_walk.argtypes = [ctypes.c_int] * 7 + [ip, ctypes.c_int]
     lib.ra_test_walk_varlen.argtypes = ([ip] + [ctypes.c_int] * 10 + [ip, ctypes.c_int, ip, ip])
+    lib.ra_test_extents.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(ctypes.c_longlong)]
+    lib.ra_test_in_range.argtypes = [ctypes.c_longlong] * 3 + [ip]
     return lib
 
 
@@ -157,3 +161,27 @@ def test_varlen_walk_is_each_sequences_own_ring(harness, order, causal):
 ])
 def test_varlen_walk_clamps_malformed_tables(harness, cu, total, max_seqlen):
     _check_varlen(harness, np.asarray(cu), total, max_seqlen, 2, True, "zigzag", 128)
+
+
+@pytest.mark.parametrize("layout", [0, 1, 2])
+def test_checked_build_extents(harness, layout):
+    B, H_q, H_kv, S, D, P, total = 3, 8, 2, 1001, 128, 4, 2500
+    ext = (ctypes.c_longlong * 3)()
+    assert harness.ra_test_extents(layout, B, H_q, H_kv, S, D, P, total, ext) == 0
+    # rows of the call's layout: B*S, the packed total, or P shards of ceil(S/P) per batch
+    rows = {0: B * S, 1: total, 2: P * B * (-(-S // P))}[layout]
+    assert list(ext) == [rows * H_q * D, rows * H_kv * D, rows * H_q]
+
+
+def test_checked_build_range_boundary(harness):
+    st = ctypes.c_int(0)
+    assert harness.ra_test_in_range(0, 10, 10, ctypes.byref(st)) == 1
+    assert harness.ra_test_in_range(9, 1, 10, ctypes.byref(st)) == 1
+    assert st.value == 0
+    assert harness.ra_test_in_range(9, 2, 10, ctypes.byref(st)) == 0
+    assert st.value == 10                     # RA_ERR_RANGE
+    st.value = 0
+    assert harness.ra_test_in_range(-1, 1, 10, ctypes.byref(st)) == 0
+    assert st.value == 10
+    assert harness.ra_test_in_range(5, 1, 10, None) == 1
+    assert harness.ra_test_in_range(50, 1, 10, None) == 0     # no status word: only skipped
