@@ -2,7 +2,10 @@
 
 Argument marshalling only: tensors become device pointers and sizes, the
 current torch stream becomes the ``stream`` argument, a non-zero status
-becomes ``RingAttnError``. Every step of the computation runs in the CUDA
+becomes ``RingAttnError``. Because the library reads and writes through bare
+pointers, every tensor a call passes must have exactly the shape and dtype
+the call implies, be contiguous and live on the current CUDA device; the
+binding checks that first and raises ``ValueError`` otherwise. Every step of the computation runs in the CUDA
 kernels of ``_lib/libringattn.so``; there is no fallback of any kind, and a
 missing library raises at the first call.
 """
@@ -171,6 +174,41 @@ def _dev(t, name):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _like(t, name, shape, dtype):
+    """A tensor the library reads or writes through a bare pointer must have
+    exactly the shape and dtype the call implies (None: not given)."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _int_buffer(t, name, n):
+    """An int32 buffer of at least n elements (None: not given)."""
+    import torch
+    if t is None:
+        return
+    if t.dtype != torch.int32 or t.numel() < n:
+        raise ValueError(f"{name} must be int32 with at least {n} elements")
+
+
+def _on_device(named):
+    """Every tensor on one CUDA device, contiguous, and that device current
+    (the library launches on the current device)."""
+    import torch
+    devs = set()
+    for t, n in named:
+        if t is not None:
+            _dev(t, n)
+            devs.add(t.device)
+    if len(devs) > 1:
+        raise ValueError(f"the call's tensors are on several devices: {sorted(map(str, devs))}")
+    if devs and next(iter(devs)).index != torch.cuda.current_device():
+        raise ValueError("the call's tensors must be on the current CUDA device")
+
+
 def ring_attn_fwd(q, k, v, P, causal, scale=None, order="contiguous", step=-1,
                   out=None, lse=None, want_lse=True, visit_log=None,
                   dev_status=None, stream=None):
@@ -182,8 +220,6 @@ def ring_attn_fwd(q, k, v, P, causal, scale=None, order="contiguous", step=-1,
     """
     import torch
     lib = load()
-    for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _dev(t, n)
     B, S, H_q, D = q.shape
     H_kv = k.shape[2]
     if k.shape != (B, S, H_kv, D) or v.shape != k.shape:
@@ -192,14 +228,18 @@ def ring_attn_fwd(q, k, v, P, causal, scale=None, order="contiguous", step=-1,
         raise ValueError("q, k, v must share a dtype")
     code = _dtype_code(q.dtype)
     out_dtype = torch.float32 if step >= 0 else q.dtype
+    _like(out, "out", (B, S, H_q, D), out_dtype)
+    _like(lse, "lse", (B, H_q, S), torch.float32)
+    _int_buffer(dev_status, "dev_status", 1)
+    if visit_log is not None:
+        _int_buffer(visit_log, "visit_log",
+                    visit_log_layout(B, H_q, S, D, P, q.dtype, order)["len"])
+    _on_device(((q, "q"), (k, "k"), (v, "v"), (out, "out"), (lse, "lse"),
+                (visit_log, "visit_log"), (dev_status, "dev_status")))
     if out is None:
         out = torch.empty(B, S, H_q, D, device=q.device, dtype=out_dtype)
     if lse is None and (want_lse or step >= 0):
         lse = torch.empty(B, H_q, S, device=q.device, dtype=torch.float32)
-    for t, n in ((out, "out"), (lse, "lse"), (visit_log, "visit_log"),
-                 (dev_status, "dev_status")):
-        if t is not None:
-            _dev(t, n)
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
     st = lib.ring_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                               B, H_q, H_kv, S, D, P, int(bool(causal)), sc,
@@ -211,9 +251,15 @@ def ring_attn_fwd(q, k, v, P, causal, scale=None, order="contiguous", step=-1,
 
 def ring_attn_fwd_plain(q, k, v, out, lse, P, causal, scale=None, stream=None):
     """The plain ``ring_attn_fwd`` entry point (bf16, contiguous order)."""
+    import torch
     lib = load()
     B, S, H_q, D = q.shape
     H_kv = k.shape[2]
+    _like(k, "k", (B, S, H_kv, D), q.dtype)
+    _like(v, "v", (B, S, H_kv, D), q.dtype)
+    _like(out, "out", (B, S, H_q, D), q.dtype)
+    _like(lse, "lse", (B, H_q, S), torch.float32)
+    _on_device(((q, "q"), (k, "k"), (v, "v"), (out, "out"), (lse, "lse")))
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
     st = lib.ring_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                            B, H_q, H_kv, S, D, P, int(bool(causal)), sc,
@@ -248,14 +294,19 @@ def ring_attn_bwd(q, k, v, out, lse, dout, P, causal, scale=None, order="contigu
     """
     import torch
     lib = load()
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (lse, "lse"), (dout, "dout")):
-        _dev(t, n)
     B, S, H_q, D = q.shape
     H_kv = k.shape[2]
-    if k.shape != (B, S, H_kv, D) or v.shape != k.shape:
-        raise ValueError("k and v must be [B, S, H_kv, D] matching q")
-    if out.shape != q.shape or dout.shape != q.shape:
-        raise ValueError("out and dout must be shaped like q")
+    for t, n in ((k, "k"), (v, "v"), (dk, "dk"), (dv, "dv")):
+        _like(t, n, (B, S, H_kv, D), q.dtype)
+    for t, n in ((out, "out"), (dout, "dout"), (dq, "dq")):
+        _like(t, n, q.shape, q.dtype)
+    _like(lse, "lse", (B, H_q, S), torch.float32)
+    _int_buffer(dev_status, "dev_status", 1)
+    if workspace is not None and workspace.dtype != torch.uint8:
+        raise ValueError("workspace must be a uint8 tensor")
+    _on_device(((q, "q"), (k, "k"), (v, "v"), (out, "out"), (lse, "lse"), (dout, "dout"),
+                (dq, "dq"), (dk, "dk"), (dv, "dv"), (workspace, "workspace"),
+                (dev_status, "dev_status")))
     code = _dtype_code(q.dtype)
     if dq is None:
         dq = torch.empty_like(q)
@@ -266,10 +317,6 @@ def ring_attn_bwd(q, k, v, out, lse, dout, P, causal, scale=None, order="contigu
     need = bwd_workspace_bytes(B, H_q, S, D, P, order)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv"), (workspace, "workspace"),
-                 (dev_status, "dev_status")):
-        if t is not None:
-            _dev(t, n)
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
             _ptr(dv), B, H_q, H_kv, S, D, P, int(bool(causal)), sc, code, ORDERS[order],
@@ -282,16 +329,14 @@ def ring_attn_bwd(q, k, v, out, lse, dout, P, causal, scale=None, order="contigu
     return dq, dk, dv
 
 
-def _varlen_args(q, k, cu_seqlens, max_seqlen):
-    for t, n in ((q, "q"), (k, "k"), (cu_seqlens, "cu_seqlens")):
-        _dev(t, n)
+def _varlen_args(q, k, v, cu_seqlens, max_seqlen):
     import torch
     if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1:
         raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
     total, H_q, D = q.shape
     H_kv = k.shape[1]
-    if k.shape != (total, H_kv, D):
-        raise ValueError("k and v must be [total, H_kv, D] matching q")
+    _like(k, "k", (total, H_kv, D), q.dtype)
+    _like(v, "v", (total, H_kv, D), q.dtype)
     return total, H_q, H_kv, D, cu_seqlens.numel() - 1, int(max_seqlen)
 
 
@@ -302,8 +347,12 @@ def ring_attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, P, causal, scale=None,
     cu_seqlens int32 [n+1] (CUDA). Returns (out [total,H_q,D], lse [H_q,total])."""
     import torch
     lib = load()
-    _dev(v, "v")
-    total, H_q, H_kv, D, n, mx = _varlen_args(q, k, cu_seqlens, max_seqlen)
+    total, H_q, H_kv, D, n, mx = _varlen_args(q, k, v, cu_seqlens, max_seqlen)
+    _like(out, "out", q.shape, q.dtype)
+    _like(lse, "lse", (H_q, total), torch.float32)
+    _int_buffer(dev_status, "dev_status", 1)
+    _on_device(((q, "q"), (k, "k"), (v, "v"), (cu_seqlens, "cu_seqlens"), (out, "out"),
+                (lse, "lse"), (dev_status, "dev_status")))
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -323,9 +372,16 @@ def ring_attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens, max_seqlen, P, cau
     """Gradients (dq, dk, dv) of ``ring_attn_fwd_varlen`` for the upstream dout."""
     import torch
     lib = load()
-    for t, nm in ((v, "v"), (out, "out"), (lse, "lse"), (dout, "dout")):
-        _dev(t, nm)
-    total, H_q, H_kv, D, n, mx = _varlen_args(q, k, cu_seqlens, max_seqlen)
+    total, H_q, H_kv, D, n, mx = _varlen_args(q, k, v, cu_seqlens, max_seqlen)
+    _like(out, "out", q.shape, q.dtype)
+    _like(dout, "dout", q.shape, q.dtype)
+    _like(lse, "lse", (H_q, total), torch.float32)
+    _int_buffer(dev_status, "dev_status", 1)
+    if workspace is not None and workspace.dtype != torch.uint8:
+        raise ValueError("workspace must be a uint8 tensor")
+    _on_device(((q, "q"), (k, "k"), (v, "v"), (cu_seqlens, "cu_seqlens"), (out, "out"),
+                (lse, "lse"), (dout, "dout"), (workspace, "workspace"),
+                (dev_status, "dev_status")))
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     need = bwd_workspace_bytes(n, H_q, mx, D, P, order)
     if workspace is None:
@@ -347,14 +403,17 @@ def ring_attn_fwd_ulysses(q, k, v, S, causal, scale=None, out=None, lse=None,
     (C = ceil(S/P)). Returns (out [P,B,C,H_q,D], lse [P,B,H_q,C])."""
     import torch
     lib = load()
-    for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _dev(t, n)
     P, B, C, H_q, D = q.shape
     H_kv = k.shape[3]
-    if k.shape != (P, B, C, H_kv, D) or v.shape != k.shape:
-        raise ValueError("k and v must be [P, B, C, H_kv, D] matching q")
+    _like(k, "k", (P, B, C, H_kv, D), q.dtype)
+    _like(v, "v", (P, B, C, H_kv, D), q.dtype)
     if C != -(-S // P):
         raise ValueError("shard length must be ceil(S / P)")
+    _like(out, "out", q.shape, q.dtype)
+    _like(lse, "lse", (P, B, H_q, C), torch.float32)
+    _int_buffer(dev_status, "dev_status", 1)
+    _on_device(((q, "q"), (k, "k"), (v, "v"), (out, "out"), (lse, "lse"),
+                (dev_status, "dev_status")))
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -373,12 +432,20 @@ def ring_attn_bwd_ulysses(q, k, v, out, lse, dout, S, causal, scale=None, worksp
     sequence-parallel layout [P, B, C, H, D]."""
     import torch
     lib = load()
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (lse, "lse"), (dout, "dout")):
-        _dev(t, n)
     P, B, C, H_q, D = q.shape
     H_kv = k.shape[3]
+    _like(k, "k", (P, B, C, H_kv, D), q.dtype)
+    _like(v, "v", (P, B, C, H_kv, D), q.dtype)
     if C != -(-S // P):
         raise ValueError("shard length must be ceil(S / P)")
+    _like(out, "out", q.shape, q.dtype)
+    _like(dout, "dout", q.shape, q.dtype)
+    _like(lse, "lse", (P, B, H_q, C), torch.float32)
+    _int_buffer(dev_status, "dev_status", 1)
+    if workspace is not None and workspace.dtype != torch.uint8:
+        raise ValueError("workspace must be a uint8 tensor")
+    _on_device(((q, "q"), (k, "k"), (v, "v"), (out, "out"), (lse, "lse"), (dout, "dout"),
+                (workspace, "workspace"), (dev_status, "dev_status")))
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     need = bwd_workspace_bytes(B, H_q, S, D, P, "contiguous")
     if workspace is None:
@@ -397,9 +464,13 @@ def attn_lse_merge(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
     """Pairwise merge; o_* [B,S,H,D], lse_* [B,H,S] float32."""
     import torch
     lib = load()
-    for t, n in ((o_a, "o_a"), (o_b, "o_b"), (lse_a, "lse_a"), (lse_b, "lse_b")):
-        _dev(t, n)
     B, S, H, D = o_a.shape
+    for t, n in ((o_b, "o_b"), (out, "out")):
+        _like(t, n, o_a.shape, o_a.dtype)
+    for t, n in ((lse_a, "lse_a"), (lse_b, "lse_b"), (lse, "lse")):
+        _like(t, n, (B, H, S), torch.float32)
+    _on_device(((o_a, "o_a"), (o_b, "o_b"), (lse_a, "lse_a"), (lse_b, "lse_b"), (out, "out"),
+                (lse, "lse")))
     if out is None:
         out = torch.empty_like(o_a)
     if lse is None:
@@ -416,9 +487,17 @@ def attn_lse_merge_n(os_, lses, out=None, lse=None, stream=None):
     import torch
     lib = load()
     n = len(os_)
-    for t in list(os_) + list(lses):
-        _dev(t, "partial")
+    if n < 1 or len(lses) != n:
+        raise ValueError("need as many lse tensors as partial outputs, at least one")
     B, S, H, D = os_[0].shape
+    for i, t in enumerate(os_):
+        _like(t, f"partial {i}", os_[0].shape, os_[0].dtype)
+    for i, t in enumerate(lses):
+        _like(t, f"lse {i}", (B, H, S), torch.float32)
+    _like(out, "out", os_[0].shape, os_[0].dtype)
+    _like(lse, "lse", (B, H, S), torch.float32)
+    _on_device([(t, "partial") for t in os_] + [(t, "lse") for t in lses] +
+               [(out, "out"), (lse, "lse")])
     if out is None:
         out = torch.empty_like(os_[0])
     if lse is None:
@@ -434,6 +513,9 @@ def attn_lse_merge_n(os_, lses, out=None, lse=None, stream=None):
 def expiry_test(q, k, v, out, lse, dev_status, stream=None):
     """Launch the kernel with one load withheld (see ring_attn_expiry_test)."""
     lib = load()
+    _int_buffer(dev_status, "dev_status", 1)
+    _on_device(((q, "q"), (k, "k"), (v, "v"), (out, "out"), (lse, "lse"),
+                (dev_status, "dev_status")))
     S = q.shape[1]
     st = lib.ring_attn_expiry_test(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), S,
                                    _ptr(dev_status), _stream(stream))

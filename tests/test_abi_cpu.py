@@ -308,3 +308,55 @@ def test_missing_library_raises(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_lib_path", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         binding.load()
+
+
+def test_binding_checks_caller_buffers_before_anything_else():
+    """The library writes through bare pointers, so every caller-supplied
+    buffer must have exactly the shape and dtype the call implies; the
+    binding refuses a wrong one (before it looks at devices)."""
+    import torch
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    B, S, H, Hk, D, P = 1, 256, 4, 2, 64, 2
+    q = torch.zeros(B, S, H, D, dtype=bf)
+    k = torch.zeros(B, S, Hk, D, dtype=bf)
+    lse = torch.zeros(B, H, S, dtype=f32)
+    cases = [
+        (lambda: binding.ring_attn_fwd(q, k, k, P, True, out=torch.zeros(B, S, H, D)), "out"),
+        (lambda: binding.ring_attn_fwd(q, k, k, P, True, out=q[:, :128].contiguous()), "out"),
+        (lambda: binding.ring_attn_fwd(q, k, k, P, True, lse=torch.zeros(B, S, H)), "lse"),
+        (lambda: binding.ring_attn_fwd(q, k, k, P, True, dev_status=torch.zeros(1)),
+         "dev_status"),
+        (lambda: binding.ring_attn_fwd(q, k, k, P, True, step=0, out=q), "out"),
+        (lambda: binding.ring_attn_fwd(q, k, k[:, :, :1].contiguous(), P, True), "k and v"),
+        (lambda: binding.ring_attn_bwd(q, k, k, q, lse, q[:, :128].contiguous(), P, True),
+         "dout"),
+        (lambda: binding.ring_attn_bwd(q, k, k, q, lse, q, P, True, dk=q), "dk"),
+        (lambda: binding.ring_attn_bwd(q, k, k, q, lse, q, P, True,
+                                       workspace=torch.zeros(64, dtype=f32)), "workspace"),
+        (lambda: binding.attn_lse_merge(q.float(), lse, q.float()[:, :, :2].contiguous(), lse),
+         "o_b"),
+        (lambda: binding.attn_lse_merge_n([q.float(), q.float()], [lse]), "as many"),
+        (lambda: binding.attn_lse_merge_n([q.float(), q.float()], [lse, lse[:, :2]]), "lse 1"),
+    ]
+    total = 300
+    qv = torch.zeros(total, H, D, dtype=bf)
+    kv = torch.zeros(total, Hk, D, dtype=bf)
+    cu = torch.tensor([0, 100, 300], dtype=i32)
+    cases += [
+        (lambda: binding.ring_attn_fwd_varlen(qv, kv, kv, cu, 200, P, True,
+                                              lse=torch.zeros(total, H)), "lse"),
+        (lambda: binding.ring_attn_bwd_varlen(qv, kv, kv, qv, torch.zeros(H, total), qv[:10],
+                                              cu, 200, P, True), "dout"),
+    ]
+    C = S // P
+    qs = torch.zeros(P, B, C, H, D, dtype=bf)
+    ks = torch.zeros(P, B, C, Hk, D, dtype=bf)
+    cases += [
+        (lambda: binding.ring_attn_fwd_ulysses(qs, ks, ks, S, True,
+                                               lse=torch.zeros(P, B, C, H)), "lse"),
+        (lambda: binding.ring_attn_bwd_ulysses(qs, ks, qs, qs, torch.zeros(P, B, H, C), qs, S,
+                                               True), "v"),
+    ]
+    for call, name in cases:
+        with pytest.raises(ValueError, match=name):
+            call()
