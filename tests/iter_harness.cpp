@@ -1,6 +1,7 @@
-// Host build of the kernels' ring bookkeeping (csrc/ring_iter.cuh), the
-// checked build's range checks (csrc/checks.cuh) and the host planner
-// (csrc/plan.cpp), for the CPU tests in test_iter_cpu.py. The functions
+// Host build of the kernels' ring bookkeeping (csrc/ring_iter.cuh and the
+// backward's csrc/q_iter.cuh), the checked build's range checks
+// (csrc/checks.cuh) and the host planner (csrc/plan.cpp), for the CPU tests
+// in test_iter_cpu.py. The functions
 // below walk the key tiles of one query tile exactly as every role of the
 // attention kernels does, so the walk can be compared with the oracle's
 // tile_visits on many shapes without a GPU.
@@ -11,6 +12,7 @@ using std::min;
 }  // namespace ra
 #define __ldg(p) (*(p))
 #include "ring_iter.cuh"
+#include "q_iter.cuh"
 // the checked build's range checks, with the device atomic as a plain store
 #define RA_DEBUG_CHECKS
 #define atomicExch(p, v) (*(p) = (v))
@@ -84,6 +86,43 @@ int ra_test_walk_varlen(const int* cu_seqlens, int n_seq, int total, int max_seq
   facts[1] = g.seg_len;
   facts[2] = g.nt;
   return walk(g, seg, ti, out, cap);
+}
+
+// The dK/dV kernel's walk for key tile `kid` (= segment * nt + tile) of a
+// fixed-length call, one query head: entries (ring step, query segment,
+// query tile, mask), at most `cap`; returns the count.
+int ra_test_qwalk(int S, int P, int causal, int order, int tile, int kid, int* out, int cap) {
+  ra::Geometry g;
+  if (ra::make_geometry(1, 1, 1, S, 128, P, causal, 0.f, order, -1, tile, &g) != RA_OK)
+    return -1;
+  const int kseg = kid / g.nt, kti = kid % g.nt;
+  const int src = ra::seg_owner(g, kseg);
+  const int kv_lo = kseg * g.seg_len + kti * g.tile;
+  const int kv_valid = ra::tile_tokens(g, kseg, kti);
+  ra::QTile qt;
+  int n = 0;
+  auto run = [&](auto& it) {
+    it.init(g, src, kv_lo, kv_valid, 0, 1);
+    while (it.next(g, qt)) {
+      if (n < cap) {
+        out[4 * n + 0] = it.t;
+        out[4 * n + 1] = qt.seg;
+        out[4 * n + 2] = qt.ti;
+        out[4 * n + 3] = qt.mask ? 1 : 0;
+      }
+      ++n;
+    }
+  };
+  if (tile == 128) {
+    ra::QIterT<128> it;
+    run(it);
+  } else if (tile == 64) {
+    ra::QIterT<64> it;
+    run(it);
+  } else {
+    return -1;
+  }
+  return n;
 }
 
 // The checked build's tensor extents for a geometry: layout 0 fixed-length

@@ -10,9 +10,12 @@ log checks the same walk on a few shapes; here it is compared entry by entry
 -- (step, source rank, key tile id, FULL/PARTIAL) -- with oracle.tile_visits
 for even and uneven lengths, every P up to 8, both orders, causal or not,
 both tile heights, single ring steps, and packed sequences, including
-malformed offset tables (which the kernels clamp). The checked build's range
-checks (csrc/checks.cuh) are built the same way: the tensor extents of each
-layout and the boundary of a check.
+malformed offset tables (which the kernels clamp). The backward's dK/dV
+kernel walks the other way -- for one key tile, every query tile that sees
+it, in the order the travelling block meets them (csrc/q_iter.cuh) -- and is
+compared with the same oracle table read by key tile. The checked build's
+range checks (csrc/checks.cuh) are built the same way: the tensor extents of
+each layout and the boundary of a check.
 """
 
 import ctypes
@@ -53,6 +56,7 @@ def harness(tmp_path_factory):
     lib.ra_test_walk.argtypes = [ctypes.c_int] * 7 + [ip, ctypes.c_int]
     lib.ra_test_walk_varlen.argtypes = ([ip] + [ctypes.c_int] * 10 + [ip, ctypes.c_int, ip, ip])
     lib.ra_test_extents.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(ctypes.c_longlong)]
+    lib.ra_test_qwalk.argtypes = [ctypes.c_int] * 6 + [ip, ctypes.c_int]
     lib.ra_test_in_range.argtypes = [ctypes.c_longlong] * 3 + [ip]
     return lib
 
@@ -185,3 +189,31 @@ def test_checked_build_range_boundary(harness):
     assert st.value == 10
     assert harness.ra_test_in_range(5, 1, 10, None) == 1
     assert harness.ra_test_in_range(50, 1, 10, None) == 0     # no status word: only skipped
+
+
+def _qwalk_expected(S, P, causal, order, tile):
+    """For every key tile, the (step, query segment, query tile, masked)
+    entries of the query tiles that visit it, from oracle.tile_visits,
+    ordered by ring step and then by query position."""
+    visits = oracle.tile_visits(S, P, causal, ORACLE_ORDER[order], tile)
+    nt = -(-segment_length(S, P, ORACLE_ORDER[order]) // tile)
+    by_key = {}
+    for qid, vs in enumerate(visits):
+        for t, _src, kid, cls in vs:
+            by_key.setdefault(kid, []).append((t, qid // nt, qid % nt,
+                                               int(cls == oracle.PARTIAL)))
+    return {kid: sorted(e) for kid, e in by_key.items()}, len(visits)
+
+
+@pytest.mark.parametrize("order", ["contiguous", "zigzag"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 8])
+def test_backward_walk_matches_oracle(harness, order, causal, P):
+    for S in SMALL_S + [4100]:
+        for tile in (64, 128):
+            want, n_tiles = _qwalk_expected(S, P, causal, order, tile)
+            for kid in range(n_tiles):
+                out = _buf(4 * CAP)
+                n = harness.ra_test_qwalk(S, P, int(causal), ORDERS[order], tile, kid, out, CAP)
+                got = [tuple(out[4 * i:4 * i + 4]) for i in range(n)]
+                assert got == want.get(kid, []), (S, P, causal, order, tile, kid)
