@@ -80,7 +80,6 @@ struct Cfg {
   static constexpr int bDS = 8;       // 256 arrivals: pass 2 done (dS stored)
   static constexpr int bAccV = 9;     // dV MMA of a visit done
   static constexpr int bAccK = 10;    // dK MMA (or dQ MMA) of a visit done
-  static constexpr int bAcc = bAccK;
   static constexpr int bFinal = 11;
   static constexpr int bAccB = 12;    // [2] dQ MMA of a visit done, per dS buffer
   static_assert(kColAcc + D + 128 <= kTmemCols, "dQ kernel: two dS buffers after dQ");
