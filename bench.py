@@ -47,7 +47,7 @@ UNIT = "TFLOP/s"
 # workload; an entry holds only while the kernel's sources have the digest
 # stored with it (see _kernel_digest).
 TRAFFIC = {
-    "attn_tc": {"sha256_16": "ced19d8160360adf", "bytes_per_launch": {
+    "attn_tc": {"sha256_16": "fd362f4e837ab524", "bytes_per_launch": {
         "bf16_s32k_causal_zigzag": 805783552 + 254530048,
         "bf16_s16k_d64": 402806784 + 117399808,
         "bf16_s128k_gqa_causal": 3068165120 + 1055448064,

@@ -140,11 +140,11 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
 }
 
 // P columns of one softmax warp: 32 (two-way split) or 16 (four-way split).
-__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[32]) {
-  tmem_st32(taddr, r);
-}
-__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[16]) {
-  tmem_st16(taddr, r);
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+  static_assert(N == 32 || N == 16, "32 or 16 columns");
+  if constexpr (N == 32) tmem_st32(taddr, r);
+  else tmem_st16(taddr, r);
 }
 
 // Columns [tO, tO + N) of this thread's O row times alpha.
