@@ -98,3 +98,12 @@ def test_headline_metric_names_only_the_headline():
     for name, w in wl.WORKLOADS.items():
         if name != wl.HEADLINE:
             assert name in bench._fwd_metric(w)
+
+
+def test_stored_traffic_is_current():
+    """Every stored DRAM capture belongs to the kernel sources as they are
+    now; after a kernel change the traffic must be captured again (one ncu
+    pass) or the bench reports null."""
+    for kernel, entry in bench.TRAFFIC.items():
+        assert entry["sha256_16"] == bench._kernel_digest(kernel), (
+            f"{kernel}: sources changed since the stored DRAM traffic was captured")
