@@ -42,6 +42,9 @@ def _fwd_metric(w):
 
 
 UNIT = "TFLOP/s"
+VARLEN_METRIC = "ring-attn fwd TFLOP/s, packed variable-length batch, 1 GB300"
+ULYSSES_METRIC = "ring-attn fwd TFLOP/s, Ulysses sequence-parallel layout, 1 GB300"
+MERGE_METRIC = "LSE merge GB/s (algorithmic bytes)"
 
 # ncu DRAM bytes (read + write) of one launch of the timed kernel, per
 # workload; an entry holds only while the kernel's sources have the digest
@@ -722,12 +725,9 @@ def run_varlen(args, w):
                "cores": _blas_threads(), "kind": "oracle",
                "sample": f"256 random query rows of the first sequence ({n} tokens), all "
                          f"heads, float64 NumPy oracle, {dt:.1f} s"}
-    cfg = {"workload": w.name, "lengths": list(w.lengths), "total": w.total, "H_q": w.H_q,
-           "H_kv": w.H_kv, "D": w.D, "P": w.P, "causal": w.causal, "order": w.order,
-           "layout": "packed [total, H, D], cu_seqlens on the device",
-           "l2": "inputs larger than L2", "parallelism": "replicas"}
-    line = _layout_line(args, world, "ring-attn fwd TFLOP/s, packed variable-length batch, "
-                        "1 GB300", w, cfg, w.flop, total_ms, kernel_ms, clk, cpu)
+    cfg = _varlen_config(w)
+    line = _layout_line(args, world, VARLEN_METRIC, w, cfg, w.flop, total_ms, kernel_ms, clk,
+                        cpu)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -759,10 +759,8 @@ def run_ulysses(args, w):
         raise RuntimeError("device-side wait expired")
     if rank != 0:
         return 0
-    cfg = dict(_config(w), layout="sequence-parallel [P, B, C, H, D], C = S/P",
-               parallelism="replicas (P virtual ranks inside one launch)")
-    line = _layout_line(args, world, "ring-attn fwd TFLOP/s, Ulysses sequence-parallel "
-                        "layout, 1 GB300", w, cfg, w.flop, total_ms, kernel_ms, clk, None)
+    line = _layout_line(args, world, ULYSSES_METRIC, w, _ulysses_config(w), w.flop, total_ms,
+                        kernel_ms, clk, None)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -813,14 +811,13 @@ def run_merge(args, w):
     peaks, src = _peaks()
     gbs = w.bytes / (kernel_ms / 1e3) / 1e9
     line = {
-        "metric": "LSE merge GB/s (algorithmic bytes)", "value":
+        "metric": MERGE_METRIC, "value":
             _job_rate(world, w.bytes, args.steps, total_ms) / 1e9,
         "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32" if w.dtype == "f32" else "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "n": w.n, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
-                   "l2": "inputs larger than L2 (8 GiB of partials)"},
+        "config": _merge_config(w),
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]),
                      "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]),
                      "traffic": _traffic("merge", w.name),
@@ -828,6 +825,139 @@ def run_merge(args, w):
                      "kernel_ms": kernel_ms},
         "clocks": clk, "gpu_launches": args.steps,
     }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _varlen_config(w):
+    return {"workload": w.name, "lengths": list(w.lengths), "total": w.total, "H_q": w.H_q,
+            "H_kv": w.H_kv, "D": w.D, "P": w.P, "causal": w.causal, "order": w.order,
+            "layout": "packed [total, H, D], cu_seqlens on the device",
+            "l2": "inputs larger than L2", "parallelism": "replicas"}
+
+
+def _ulysses_config(w):
+    return dict(_config(w), layout="sequence-parallel [P, B, C, H, D], C = S/P",
+                parallelism="replicas (P virtual ranks inside one launch)")
+
+
+def _merge_config(w):
+    return {"workload": w.name, "n": w.n, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
+            "l2": "inputs larger than L2 (8 GiB of partials)"}
+
+
+def _reference_line(args, metric, unit, value, total_t, cfg, sample):
+    """The reference arm's JSON line: the float64 oracle on the host cores."""
+    return {
+        "impl": "reference", "metric": metric, "value": value, "unit": unit,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": cfg,
+        "cpu_baseline": {"value": value, "unit": unit, "cores": _blas_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def _timed_samples(args, sample):
+    """args.warmup untimed and args.steps timed calls of sample(seed) ->
+    (work, seconds); returns (work per second, total seconds)."""
+    for i in range(args.warmup):
+        sample(100 + i)
+    work, total_t = 0.0, 0.0
+    for i in range(args.steps):
+        wk, dt = sample(1000 + i)
+        work += wk
+        total_t += dt
+    return work / total_t, total_t
+
+
+def run_varlen_reference(args, w):
+    """The oracle on sampled rows of the packed batch, each row within its
+    own sequence."""
+    import numpy as np
+    import oracle
+    from sequence_exact_attention_gb300.workloads import make_varlen
+    world, rank, _, _ = _dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    q, k, v, cu = make_varlen(w)
+    cu = np.asarray(cu)
+    n_rows = min(args.ref_rows, w.total)
+
+    def sample(seed):
+        rows = np.sort(np.random.default_rng(seed).choice(w.total, n_rows, replace=False))
+        seq = np.searchsorted(cu, rows, side="right") - 1
+        pairs, dt = 0.0, 0.0
+        for b in np.unique(seq):
+            lo, hi = int(cu[b]), int(cu[b + 1])
+            local = rows[seq == b] - lo
+            t0 = time.perf_counter()
+            oracle.attention_rows(q[None, lo:hi], k[None, lo:hi], v[None, lo:hi], w.causal,
+                                  w.scale, local)
+            dt += time.perf_counter() - t0
+            pairs += float((local + 1).sum()) if w.causal else float(len(local) * (hi - lo))
+        return 4.0 * w.D * w.H_q * pairs, dt
+
+    rate, total_t = _timed_samples(args, sample)
+    line = _reference_line(args, VARLEN_METRIC, UNIT, rate / 1e12, total_t, _varlen_config(w),
+                           f"{n_rows} random rows of the packed batch x all {w.H_q} heads per "
+                           "step, each over its own sequence (float64 NumPy oracle)")
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ulysses_reference(args, w):
+    """The oracle on sampled rows of the same attention: the Ulysses method's
+    result is full attention over the whole sequence."""
+    import numpy as np
+    import oracle
+    from sequence_exact_attention_gb300.workloads import make_sharded_qkv
+    world, rank, _, _ = _dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    qs, ks, vs = make_sharded_qkv(w)
+
+    def unshard(x):      # [P, B, C, H, D] -> [B, S, H, D]
+        P, B, C, H, D = x.shape
+        return x.permute(1, 0, 2, 3, 4).reshape(B, P * C, H, D)[:, :w.S]
+
+    q, k, v = unshard(qs), unshard(ks), unshard(vs)
+    n_rows = min(args.ref_rows, w.S)
+
+    def sample(seed):
+        rate, dt, _ = _oracle_sample_rate(w, q, k, v, n_rows, seed)
+        return rate * dt * 1e12, dt
+
+    rate, total_t = _timed_samples(args, sample)
+    line = _reference_line(args, ULYSSES_METRIC, UNIT, rate / 1e12, total_t, _ulysses_config(w),
+                           f"{n_rows} random query rows x all {w.H_q} heads x {w.B} sequences "
+                           "per step, full key range (float64 NumPy oracle)")
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_merge_reference(args, w):
+    """The oracle's n-way merge on a slice of the workload's rows."""
+    import dataclasses
+    import oracle
+    from sequence_exact_attention_gb300.workloads import make_merge_parts
+    world, rank, _, _ = _dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    ws = dataclasses.replace(w, S=min(w.S, 16 * args.ref_rows))
+    os_, ls = make_merge_parts(ws)
+
+    def sample(seed):
+        t0 = time.perf_counter()
+        oracle.lse_merge_n(os_, ls)
+        return float(ws.bytes), time.perf_counter() - t0
+
+    rate, total_t = _timed_samples(args, sample)
+    line = _reference_line(args, MERGE_METRIC, "GB/s", rate / 1e9, total_t, _merge_config(w),
+                           f"all {ws.n} partials of S={ws.S} positions (same B, H, D, drawn "
+                           "the same way) per step (float64 NumPy oracle)")
     print(json.dumps(line), flush=True)
     return 0
 
@@ -853,12 +983,16 @@ def main():
     ap.add_argument("--seq-len", type=int, default=0,
                     help="override S (smaller profiling cases of the same shape)")
     args = ap.parse_args()
+    ref = args.impl == "reference"
     if args.workload in MERGE_WORKLOADS:
-        return run_merge(args, MERGE_WORKLOADS[args.workload])
+        w = MERGE_WORKLOADS[args.workload]
+        return run_merge_reference(args, w) if ref else run_merge(args, w)
     if args.workload in VARLEN_WORKLOADS:
-        return run_varlen(args, VARLEN_WORKLOADS[args.workload])
+        w = VARLEN_WORKLOADS[args.workload]
+        return run_varlen_reference(args, w) if ref else run_varlen(args, w)
     if args.workload in ULYSSES_WORKLOADS:
-        return run_ulysses(args, ULYSSES_WORKLOADS[args.workload])
+        w = ULYSSES_WORKLOADS[args.workload]
+        return run_ulysses_reference(args, w) if ref else run_ulysses(args, w)
     if args.workload in BWD_WORKLOADS:
         w = BWD_WORKLOADS[args.workload]
         if args.seq_len:

@@ -107,3 +107,37 @@ def test_stored_traffic_is_current():
     for kernel, entry in bench.TRAFFIC.items():
         assert entry["sha256_16"] == bench._kernel_digest(kernel), (
             f"{kernel}: sources changed since the stored DRAM traffic was captured")
+
+
+def _ref_args(**kw):
+    import argparse
+    a = dict(gpus=1, steps=1, warmup=0, ref_rows=8)
+    a.update(kw)
+    return argparse.Namespace(**a)
+
+
+def _last_json(capsys):
+    import json
+    return json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+
+
+@pytest.mark.parametrize("kind", ["varlen", "ulysses", "merge"])
+def test_reference_arms_print_the_contract_line(kind, capsys):
+    """Every workload family's --impl reference arm times the oracle on the
+    host and prints the same metric and unit as the GPU arm."""
+    if kind == "varlen":
+        w = wl.VarlenWorkload("t", "bf16", (40, 0, 7, 100), 2, 1, 64, 2, True, "zigzag", seed=3)
+        assert bench.run_varlen_reference(_ref_args(), w) == 0
+        metric, unit = bench.VARLEN_METRIC, bench.UNIT
+    elif kind == "ulysses":
+        w = wl.AttnWorkload("t", "bf16", 2, 4, 2, 90, 64, 4, True, "contiguous", seed=4)
+        assert bench.run_ulysses_reference(_ref_args(), w) == 0
+        metric, unit = bench.ULYSSES_METRIC, bench.UNIT
+    else:
+        w = wl.MergeWorkload("t", "f32", 3, 1, 2, 512, 64, seed=5)
+        assert bench.run_merge_reference(_ref_args(), w) == 0
+        metric, unit = bench.MERGE_METRIC, "GB/s"
+    line = _last_json(capsys)
+    assert line["impl"] == "reference" and line["metric"] == metric and line["unit"] == unit
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["steps"] == 1
