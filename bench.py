@@ -203,18 +203,50 @@ def _job_rate(world, units_per_step, steps, max_ms):
     return world * units_per_step * steps / (max_ms / 1e3)
 
 
-def _oracle_sample_rate(w, q, k, v, n_rows, seed):
+def _oracle_sample_rate(w, q, k, v, n_rows, seed, want=None):
     """float64 oracle on n_rows sampled query rows (all heads); returns
-    (TFLOP/s by the algorithmic count of those rows, seconds, rows)."""
+    (TFLOP/s by the algorithmic count of those rows, seconds, rows). With a
+    list `want`, the oracle's (out rows, lse rows) are appended to it."""
     import numpy as np
     import oracle
     rows = np.sort(np.random.default_rng(seed).choice(w.S, n_rows, replace=False))
     t0 = time.perf_counter()
-    oracle.attention_rows(q, k, v, w.causal, w.scale, rows)
+    res = oracle.attention_rows(q, k, v, w.causal, w.scale, rows)
     dt = time.perf_counter() - t0
+    if want is not None:
+        want.append(res)
     pairs = float((rows + 1).sum()) if w.causal else float(n_rows * w.S)
     flop = 4.0 * w.D * pairs * w.B * w.H_q
     return flop / dt / 1e12, dt, rows
+
+
+def _parity(w, out, lse, rows, want):
+    """Errors of the timed call's own output on the oracle's sampled rows
+    (the CPU baseline's sample), against the workload's tolerance."""
+    import numpy as np
+    try:
+        want_o, want_l = want
+        eo = np.abs(out[:, rows].float().cpu().numpy() - want_o)
+        el = np.abs(lse[:, :, rows].float().cpu().numpy() - want_l)
+        tol = {"max": 2e-2, "mean": 2e-3} if w.dtype == "bf16" else {"max": 1e-4, "mean": 1e-4}
+        res = {"rows": int(len(rows)), "out_max_abs_err": float(eo.max()),
+               "out_mean_abs_err": float(eo.mean()), "lse_max_abs_err": float(el.max()),
+               "lse_mean_abs_err": float(el.mean()), "tolerance": tol}
+        res["within_tolerance"] = bool(
+            res["out_max_abs_err"] <= tol["max"] and res["out_mean_abs_err"] <= tol["mean"]
+            and res["lse_max_abs_err"] <= tol["max"] and res["lse_mean_abs_err"] <= tol["mean"])
+        return res
+    except Exception as e:       # reporting only: never stop the bench
+        return {"error": repr(e)}
+
+
+def _device_info(dev):
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return {"name": p.name, "sm_count": int(p.multi_processor_count)}
+    except Exception as e:       # reporting only
+        return {"error": repr(e)}
 
 
 def _blas_threads():
@@ -425,13 +457,15 @@ def run_ours(args, w):
         kname = f"attn_simt_kernel<{w.D}>"
         traffic = None
 
-    cpu = None
+    cpu, parity = None, None
     if world == 1 and not args.no_cpu_baseline:
         n_rows = min(args.cpu_rows, w.S)
-        rate, dt, _ = _oracle_sample_rate(w, q, k, v, n_rows, seed=7)
+        want = []
+        rate, dt, rows = _oracle_sample_rate(w, q, k, v, n_rows, seed=7, want=want)
         cpu = {"value": rate, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
                "sample": f"{n_rows} random query rows x all {w.H_q} heads of the same "
                          f"workload, float64 NumPy oracle, {dt:.1f} s"}
+        parity = _parity(w, out, lse, rows, want[0])
 
     line = {
         "metric": _fwd_metric(w), "value": value, "unit": UNIT, "n_gpus": world,
@@ -448,6 +482,8 @@ def run_ours(args, w):
         "e2e": e2e,
         "clocks": clk,
         "gpu_launches": args.steps,
+        "parity": parity,
+        "device": _device_info(dev),
     }
     print(json.dumps(line), flush=True)
     return 0

@@ -141,3 +141,30 @@ def test_reference_arms_print_the_contract_line(kind, capsys):
     assert line["impl"] == "reference" and line["metric"] == metric and line["unit"] == unit
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["steps"] == 1
+
+
+def test_parity_record_of_the_bench_line():
+    """The bench line's parity record compares the timed output with the
+    oracle rows of the CPU-baseline sample, against the tolerance."""
+    import numpy as np
+    import torch
+    import oracle
+    w = wl.AttnWorkload("t", "bf16", 1, 2, 2, 200, 64, 2, True, "zigzag", seed=9)
+    q, k, v = wl.make_qkv(w)
+    o, l = oracle.attention_naive(q, k, v, True, w.scale)
+    out = torch.from_numpy(o).to(torch.bfloat16)
+    lse = torch.from_numpy(l).float()
+    want = []
+    _, _, rows = bench._oracle_sample_rate(w, q, k, v, 16, seed=3, want=want)
+    rec = bench._parity(w, out, lse, rows, want[0])
+    assert rec["rows"] == 16 and rec["within_tolerance"], rec
+    assert rec["out_max_abs_err"] < 1e-2 and rec["lse_max_abs_err"] < 1e-5
+    bad = out.clone()
+    bad[:, rows[0]] += 1.0
+    assert not bench._parity(w, bad, lse, rows, want[0])["within_tolerance"]
+    assert "error" in bench._parity(w, out, lse, rows, None)   # never raises
+
+
+def test_device_info_never_raises():
+    info = bench._device_info(0)
+    assert ("name" in info and "sm_count" in info) or "error" in info
