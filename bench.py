@@ -476,6 +476,10 @@ def run_ours(args, w):
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peak_note, "kernel": kname, "kernel_ms": kernel_ms,
+                     "kernel_ms_median": statistics.median(launch_ms),
+                     "kernel_ms_min": min(launch_ms),
+                     # one exponential per allowed (query, key) pair
+                     "exp2_per_s": flop / (4.0 * w.D) / (kernel_ms / 1e3),
                      "frac_of_sustained_peak": (achieved / float(peaks["bf16_tflops_sustained"])
                                                 if w.dtype == "bf16" else None)},
         "cpu_baseline": cpu,
