@@ -125,6 +125,33 @@ int ra_test_qwalk(int S, int P, int causal, int order, int tile, int kid, int* o
   return n;
 }
 
+// Row addressing of the kernels' loads and stores: for batch b, head h and
+// every position of segment `seg`, the tensor row (in units of H*D
+// elements) and the lse index. layout 0 fixed-length, 1 packed (rows from
+// row0), 2 sequence-sharded; returns the number of positions written.
+int ra_test_rows(int layout, int B, int H_q, int S, int P, int order, int total, int row0,
+                 int b, int h, int seg, long long* rows, long long* lse_idx, int cap) {
+  ra::Geometry g;
+  if (ra::make_geometry(B, H_q, 1, S, 128, P, 1, 0.f, order, -1, 128, &g) != RA_OK) return -1;
+  if (layout == 1) {
+    static const int kDummy[2] = {0, 0};
+    g.cu_seqlens = kDummy;
+    g.total = total;
+  } else if (layout == 2) {
+    g.shard_rows = g.seg_len;
+  }
+  const bool varlen = layout == 1;
+  const ra::SegRows r = ra::seg_rows(g, b, seg, row0, varlen);
+  const size_t l0 = ra::lse_base(g, b, h, seg, row0, varlen);
+  const int n = ra::seg_tokens(g, seg);
+  for (int i = 0; i < n && i < cap; ++i) {
+    const int pos = seg * g.seg_len + i;
+    rows[i] = (long long)(r.grow + pos);
+    lse_idx[i] = (long long)(l0 + pos);
+  }
+  return n;
+}
+
 // The checked build's tensor extents for a geometry: layout 0 fixed-length
 // [B, S, H, D], 1 packed (`total` rows), 2 sequence-sharded (P * B * C rows);
 // ext = [q/out, k/v, lse] in elements.

@@ -13,9 +13,11 @@ both tile heights, single ring steps, and packed sequences, including
 malformed offset tables (which the kernels clamp). The backward's dK/dV
 kernel walks the other way -- for one key tile, every query tile that sees
 it, in the order the travelling block meets them (csrc/q_iter.cuh) -- and is
-compared with the same oracle table read by key tile. The checked build's
-range checks (csrc/checks.cuh) are built the same way: the tensor extents of
-each layout and the boundary of a check.
+compared with the same oracle table read by key tile. The rows every load
+and store addresses (seg_rows, lse_base) are checked against the three
+layouts' definitions. The checked build's range checks (csrc/checks.cuh) are
+built the same way: the tensor extents of each layout and the boundary of a
+check.
 """
 
 import ctypes
@@ -57,6 +59,8 @@ def harness(tmp_path_factory):
     lib.ra_test_walk_varlen.argtypes = ([ip] + [ctypes.c_int] * 10 + [ip, ctypes.c_int, ip, ip])
     lib.ra_test_extents.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(ctypes.c_longlong)]
     lib.ra_test_qwalk.argtypes = [ctypes.c_int] * 6 + [ip, ctypes.c_int]
+    lp = ctypes.POINTER(ctypes.c_longlong)
+    lib.ra_test_rows.argtypes = [ctypes.c_int] * 11 + [lp, lp, ctypes.c_int]
     lib.ra_test_in_range.argtypes = [ctypes.c_longlong] * 3 + [ip]
     return lib
 
@@ -217,3 +221,46 @@ def test_backward_walk_matches_oracle(harness, order, causal, P):
                 n = harness.ra_test_qwalk(S, P, int(causal), ORDERS[order], tile, kid, out, CAP)
                 got = [tuple(out[4 * i:4 * i + 4]) for i in range(n)]
                 assert got == want.get(kid, []), (S, P, causal, order, tile, kid)
+
+
+def _rows(lib, layout, B, H_q, S, P, order, total, row0, b, h, seg):
+    n_max = S + 1
+    rows, lse = (ctypes.c_longlong * n_max)(), (ctypes.c_longlong * n_max)()
+    n = lib.ra_test_rows(layout, B, H_q, S, P, ORDERS[order], total, row0, b, h, seg, rows,
+                         lse, n_max)
+    assert n >= 0
+    return list(rows[:n]), list(lse[:n])
+
+
+@pytest.mark.parametrize("S,P", [(1000, 4), (1001, 4), (256, 2), (5, 4), (4100, 8)])
+def test_row_addressing_of_every_layout(harness, S, P):
+    """The rows the kernels load and store, in each layout, restated from the
+    layouts' definitions: [B, S, H, D] with lse [B, H, S]; packed rows from
+    the sequence's first row with lse [H, total]; the sequence-parallel
+    [P, B, C, H, D] (C = ceil(S/P), shard p = positions pC ..) with lse
+    [P, B, H, C]."""
+    B, H = 3, 2
+    for order in ("contiguous", "zigzag"):
+        parts = 2 * P if order == "zigzag" else P
+        seg_len = -(-S // parts)
+        for seg in range(parts):
+            positions = list(range(seg * seg_len, min(S, (seg + 1) * seg_len)))
+            for b in range(B):
+                for h in range(H):
+                    got = _rows(harness, 0, B, H, S, P, order, 0, 0, b, h, seg)
+                    assert got == ([b * S + p for p in positions],
+                                   [(b * H + h) * S + p for p in positions])
+                    total, row0 = 5000, 17 + 100 * b
+                    got = _rows(harness, 1, B, H, S, P, order, total, row0, b, h, seg)
+                    assert got == ([row0 + p for p in positions],
+                                   [h * total + row0 + p for p in positions])
+        # the sharded layout exists for contiguous chunks only (shard p = chunk p)
+        C = -(-S // P)
+        for p in range(P):
+            positions = list(range(p * C, min(S, (p + 1) * C)))
+            for b in range(B):
+                for h in range(H):
+                    got = _rows(harness, 2, B, H, S, P, "contiguous", 0, 0, b, h, p)
+                    assert got == ([(p * B + b) * C + (x - p * C) for x in positions],
+                                   [((p * B + b) * H + h) * C + (x - p * C)
+                                    for x in positions])
