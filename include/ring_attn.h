@@ -40,7 +40,8 @@
  *    by the caller. Tensor pointers (q, k, v, out, o_*) are 16-byte aligned;
  *    lse, visit logs and status words 4-byte aligned (else RA_ERR_ALIGN).
  *    The library allocates no device memory and keeps no state between calls
- *    except read-only per-device facts.
+ *    except read-only per-device facts and the one scratch array that
+ *    ring_attn_bwd_noalloc uses (module memory, held until exit).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream). Calls enqueue work and return; they never synchronise.
  *  - Arguments are checked on the host before anything is enqueued; on error
@@ -77,9 +78,11 @@ typedef enum {
   RA_ERR_LAUNCH = 7,   /* CUDA runtime error while preparing or launching          */
   RA_ERR_TIMEOUT = 8,  /* a device-side bounded wait expired (dev_status only)     */
   RA_ERR_BUFFER = 9,   /* a caller buffer is too small                             */
-  RA_ERR_RANGE = 10    /* a size overflows 32-bit indexing, or step out of range;
+  RA_ERR_RANGE = 10,   /* a size overflows 32-bit indexing, or step out of range;
                           in dev_status (checked build only): a device index out
                           of its tensor's range                                   */
+  RA_ERR_SCRATCH = 11  /* the problem needs more scratch than the library's
+                          built-in array holds (ring_attn_bwd_noalloc)           */
 } ra_status;
 
 typedef enum { RA_BF16 = 0, RA_F32 = 1 } ra_dtype;
@@ -257,6 +260,43 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v,
                         int causal, float scale, int dtype, int order,
                         void* workspace, size_t workspace_bytes,
                         int* dev_status, void* stream);
+
+/* Size of the scratch array built into the library for ring_attn_bwd_noalloc. */
+#define RA_BWD_NOALLOC_MAX_BYTES (8u << 20)
+
+/*
+ * ring_attn_bwd_noalloc - ring_attn_bwd without a caller workspace; the call
+ * allocates no memory at all. The pages have no counterpart to this entry
+ * point: it exists for callers that cannot call cudaMalloc, such as a plugin
+ * whose host framework owns the device memory through its own pool and hands
+ * it no workspace, or a latency-critical path on which cudaMalloc / cudaFree
+ * may synchronise the device.
+ *
+ * Arguments and results are those of ring_attn_bwd without `workspace` and
+ * `workspace_bytes`: the caller still passes every input and output. The
+ * workspace lives instead in a file-scope device array of
+ * RA_BWD_NOALLOC_MAX_BYTES (8 MiB) that every GPU which loads the library
+ * holds until the process exits. It fits ring_attn_bwd_workspace(...) <=
+ * 8 MiB, i.e. up to 2^20 tile-padded query rows (B * H_q * S rounded up per
+ * 128-row tile of each chunk or half); the S = 32768, H_q = 32 causal
+ * zig-zag problem fits exactly. A larger problem returns RA_ERR_SCRATCH
+ * before anything is launched.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture begins.
+ *  - Every call shares the one array and it keeps the last call's contents.
+ *    Nothing in it has to start at zero: the prep phase overwrites every
+ *    entry a call reads. Calls whose work overlaps on the GPU (two streams,
+ *    or two host threads on one device) race on the array: serialise them.
+ *  - dev_status and every other convention as ring_attn_bwd.
+ * Errors: as ring_attn_bwd, with RA_ERR_SCRATCH in place of RA_ERR_BUFFER.
+ */
+ra_status ring_attn_bwd_noalloc(const void* q, const void* k, const void* v,
+                                const void* out, const float* lse, const void* dout,
+                                void* dq, void* dk, void* dv,
+                                int B, int H_q, int H_kv, int S, int D, int P,
+                                int causal, float scale, int dtype, int order,
+                                int* dev_status, void* stream);
 
 /* Phases of the backward pass (bit flags) for ring_attn_bwd_ex. */
 enum { RA_BWD_PREP = 1, RA_BWD_DKDV = 2, RA_BWD_DQ = 4, RA_BWD_ALL = 7 };

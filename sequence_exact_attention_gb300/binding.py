@@ -31,6 +31,7 @@ EXPORTS = ("ring_attn_fwd", "ring_attn_fwd_ex", "ring_attn_visit_log_len",
            "ring_attn_fwd_varlen", "ring_attn_bwd_varlen", "ring_attn_fwd_ulysses",
            "ring_attn_bwd_ulysses",
            "ring_attn_bwd_workspace", "ring_attn_bwd", "ring_attn_bwd_ex",
+           "ring_attn_bwd_noalloc",
            "attn_lse_merge", "attn_lse_merge_n", "ring_attn_plan",
            "ring_attn_expiry_test", "ring_attn_strerror", "ring_attn_version")
 
@@ -84,6 +85,8 @@ def load():
     lib.ring_attn_bwd_ex.restype = c_int
     lib.ring_attn_bwd_ex.argtypes = ([vp] * 9 + [c_int] * 7 + [c_float, c_int, c_int, vp,
                                                                 ctypes.c_size_t, c_int, vp, vp])
+    lib.ring_attn_bwd_noalloc.restype = c_int
+    lib.ring_attn_bwd_noalloc.argtypes = [vp] * 9 + [c_int] * 7 + [c_float, c_int, c_int, vp, vp]
     lib.ring_attn_fwd_ulysses.restype = c_int
     lib.ring_attn_fwd_ulysses.argtypes = [vp] * 5 + [c_int] * 7 + [c_float, c_int, vp, vp]
     lib.ring_attn_bwd_ulysses.restype = c_int
@@ -326,6 +329,51 @@ def ring_attn_bwd(q, k, v, out, lse, dout, P, causal, scale=None, order="contigu
     else:
         st = lib.ring_attn_bwd_ex(*args, int(phases), _ptr(dev_status), _stream(stream))
     _check(st, "ring_attn_bwd")
+    return dq, dk, dv
+
+
+BWD_NOALLOC_MAX_BYTES = 8 << 20
+RA_ERR_SCRATCH = 11
+
+
+def ring_attn_bwd_noalloc(q, k, v, out, lse, dout, P, causal, scale=None, order="contiguous",
+                          dq=None, dk=None, dv=None, dev_status=None, stream=None):
+    """``ring_attn_bwd`` through the entry point that allocates nothing.
+
+    For callers that cannot allocate device memory (a plugin whose host
+    framework owns the memory pool, a path where cudaMalloc may synchronise):
+    the library keeps the backward's workspace in its own built-in 8 MiB
+    device array. Pass dq, dk, dv to make the whole call allocation-free; when
+    omitted they are allocated here, by torch, as for ``ring_attn_bwd``.
+    Calls that overlap on the GPU share that array and race: serialise them.
+    A problem needing more than ``BWD_NOALLOC_MAX_BYTES`` of workspace raises
+    ``RingAttnError`` with status ``RA_ERR_SCRATCH``.
+    """
+    import torch
+    lib = load()
+    B, S, H_q, D = q.shape
+    H_kv = k.shape[2]
+    for t, n in ((k, "k"), (v, "v"), (dk, "dk"), (dv, "dv")):
+        _like(t, n, (B, S, H_kv, D), q.dtype)
+    for t, n in ((out, "out"), (dout, "dout"), (dq, "dq")):
+        _like(t, n, q.shape, q.dtype)
+    _like(lse, "lse", (B, H_q, S), torch.float32)
+    _int_buffer(dev_status, "dev_status", 1)
+    _on_device(((q, "q"), (k, "k"), (v, "v"), (out, "out"), (lse, "lse"), (dout, "dout"),
+                (dq, "dq"), (dk, "dk"), (dv, "dv"), (dev_status, "dev_status")))
+    code = _dtype_code(q.dtype)
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    st = lib.ring_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), B, H_q, H_kv, S, D, P,
+                                   int(bool(causal)), sc, code, ORDERS[order],
+                                   _ptr(dev_status), _stream(stream))
+    _check(st, "ring_attn_bwd_noalloc")
     return dq, dk, dv
 
 

@@ -28,7 +28,7 @@ VARIANTS = {"release": (LIB, OUT, []),
             "debug": (LIB_DEBUG, os.path.join(OUT, "debug"), ["-DRA_DEBUG_CHECKS"])}
 
 SOURCES = ["plan.cpp", "api.cpp", "tensor_map.cpp", "merge.cu", "attn_simt.cu", "attn_tc.cu",
-           "attn_bwd.cu"]
+           "attn_bwd.cu", "bwd_noalloc.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -180,6 +180,9 @@ const char* ring_attn_strerror(int status) {
     case RA_ERR_TIMEOUT: return "a device-side bounded wait expired";
     case RA_ERR_BUFFER: return "caller buffer too small";
     case RA_ERR_RANGE: return "size out of range (32-bit indexing) or ring step outside [-1, P)";
+    case RA_ERR_SCRATCH:
+      return "problem too large for the library's built-in backward scratch "
+             "(8 MiB: at most 2^20 tile-padded query rows; use ring_attn_bwd with a workspace)";
     default: return "unknown status";
   }
 }
