@@ -50,21 +50,14 @@ MERGE_METRIC = "LSE merge GB/s (algorithmic bytes)"
 # workload; an entry holds only while the kernel's sources have the digest
 # stored with it (see _kernel_digest).
 TRAFFIC = {
-    "attn_tc": {"sha256_16": "fd362f4e837ab524", "bytes_per_launch": {
-        "bf16_s32k_causal_zigzag": 805783552 + 254530048,
-        "bf16_s16k_d64": 402806784 + 117399808,
-        "bf16_s128k_gqa_causal": 3068165120 + 1055448064,
-        "bf16_varlen_32k_causal_zigzag": 810178048 + 251862528,
-        "bf16_ulysses_s16k_b2_causal": 805466624 + 250964992,
-        "bf16_s32760_uneven_causal_zigzag": 808057856 + 251618304,
-    }},
+    "attn_tc": {"sha256_16": "5702fb6fbea06592", "bytes_per_launch": {}},
     "merge": {"sha256_16": "110b882547236ed1", "bytes_per_launch": {
         "merge_p8_s64k": 8657131264 + 1038706688,
     }},
 }
 KERNEL_SOURCES = {
     "attn_tc": ("attn_tc.cu", "checks.cuh", "fastmath.cuh", "ring_iter.cuh", "sm100.cuh",
-                "ra_internal.h"),
+                "ra_internal.h", "tensor_map.cpp"),
     "merge": ("merge.cu", "ra_internal.h"),
 }
 

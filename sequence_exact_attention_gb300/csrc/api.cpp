@@ -69,8 +69,7 @@ ra_status ring_attn_fwd_ex(const void* q, const void* k, const void* v,
                             static_cast<const float*>(k),
                             static_cast<const float*>(v), out, lse, visit_log,
                             log_stride, dev_status, s);
-  return launch_attn_tc(g, q, k, v, out, lse, visit_log, log_stride,
-                        dev_status, sms, s);
+  return launch_attn_tc(g, q, k, v, out, lse, visit_log, log_stride, dev_status, s);
 }
 
 ra_status ring_attn_fwd(const void* q, const void* k, const void* v,
@@ -95,7 +94,7 @@ ra_status ring_attn_expiry_test(const void* q, const void* k, const void* v, voi
   int sms = 0;
   st = check_device(&sms);
   if (st != RA_OK) return st;
-  return launch_attn_tc_withheld(g, q, k, v, out, lse, dev_status, sms,
+  return launch_attn_tc_withheld(g, q, k, v, out, lse, dev_status,
                                  reinterpret_cast<cudaStream_t>(stream));
 }
 

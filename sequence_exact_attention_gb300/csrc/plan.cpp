@@ -38,7 +38,6 @@ ra_status make_geometry(int B, int H_q, int H_kv, int S, int D, int P,
   g->nt = (g->seg_len + tile - 1) / tile;
   g->scale = scale > 0.f ? scale : 1.0f / __builtin_sqrtf((float)D);
   g->scale_log2 = g->scale * 1.4426950408889634f;
-  g->withhold_v0 = 0;
   g->cu_seqlens = nullptr;
   g->total = 0;
   g->shard_rows = 0;

@@ -26,7 +26,6 @@ struct Geometry {
   int nt;          // tiles per segment
   float scale;     // softmax scale
   float scale_log2;  // scale * log2(e)
-  int withhold_v0;   // test only: the producer never loads V of key tile 0
   // Packed variable-length batches (null for fixed-length BSHD tensors):
   // sequence b occupies rows [cu_seqlens[b], cu_seqlens[b+1]) of tensors of
   // `total` rows; B is the number of sequences and S their maximum length,
@@ -56,7 +55,7 @@ ra_status launch_attn_simt(const Geometry& g, const float* q, const float* k,
 // Same kernel with the V load of key tile 0 withheld (expiry-path test).
 ra_status launch_attn_tc_withheld(const Geometry& g, const void* q, const void* k,
                                   const void* v, void* out, float* lse, int* dev_status,
-                                  int sm_count, cudaStream_t stream);
+                                  cudaStream_t stream);
 // Packed variable-length launches (g.cu_seqlens set, no visit log, all steps).
 ra_status launch_attn_tc_varlen(const Geometry& g, const void* q, const void* k,
                                 const void* v, void* out, float* lse, int* dev_status,
@@ -73,8 +72,7 @@ ra_status launch_attn_simt_sharded(const Geometry& g, const float* q, const floa
                                    cudaStream_t stream);
 ra_status launch_attn_tc(const Geometry& g, const void* q, const void* k,
                          const void* v, void* out, float* lse, int* visit_log,
-                         int log_stride, int* dev_status, int sm_count,
-                         cudaStream_t stream);
+                         int log_stride, int* dev_status, cudaStream_t stream);
 
 // TMA map of a [B, S, H, D] bf16 tensor: box = 64 columns x 1 head x
 // `box_rows` rows x 1 batch, 128-byte swizzle (tensor_map.cpp).

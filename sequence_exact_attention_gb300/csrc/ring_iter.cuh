@@ -179,6 +179,29 @@ struct KvIter {
   }
 };
 
+// Number of key tiles KvIter walks for the query rows [q_lo, q_lo + q_valid),
+// in closed form per segment: a segment of len tokens from s0 holds
+// ceil(len / tile) tiles, and under the causal rule the walk stops after the
+// last tile starting at or before the last query row.
+__device__ __forceinline__ int kv_walk_length(const Geometry& g, int r, int q_lo, int q_valid) {
+  if (q_valid <= 0) return 0;
+  const int q_hi = q_lo + q_valid - 1;
+  const int t0 = g.step >= 0 ? g.step : 0;
+  const int t1 = g.step >= 0 ? g.step + 1 : g.P;
+  int n = 0;
+  for (int t = t0; t < t1; ++t) {
+    const int src = r - t < 0 ? r - t + g.P : r - t;
+    for (int w = 0; w < g.segs_per_rank; ++w) {
+      const int seg = rank_seg(g, src, w);
+      const int s0 = seg * g.seg_len;
+      int k = (seg_tokens(g, seg) + g.tile - 1) / g.tile;
+      if (g.causal) k = min(k, q_hi < s0 ? 0 : (q_hi - s0) / g.tile + 1);
+      n += k;
+    }
+  }
+  return n;
+}
+
 // Pair class for the visit log: FULL iff every (valid query, valid key) pair
 // is allowed, PARTIAL otherwise (SKIP tiles are never visited).
 __device__ __forceinline__ int tile_class(const Geometry& g, int q_lo, const KvTile& kv) {

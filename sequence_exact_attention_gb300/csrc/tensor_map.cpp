@@ -1,5 +1,5 @@
-// TMA tensor maps of the [B, S, H, D] bf16 tensors read by the backward
-// kernels. The driver's encoder is looked up once through the runtime, so
+// TMA tensor maps of the [B, S, H, D] bf16 tensors read by the forward and
+// backward kernels. The driver's encoder is looked up once through the runtime, so
 // the library links no driver library directly.
 #include <mutex>
 

@@ -41,6 +41,33 @@ int walk(const ra::Geometry& g, int seg, int ti, int* out, int cap) {
     }
     ++n;
   }
+  // the MMA issuers count the walk in closed form: it must agree
+  if (ra::kv_walk_length(g, r, q_lo, q_valid) != n) return -2;
+  return n;
+}
+
+// The forward kernel's walk for a block of `rows` query rows starting at
+// tile (seg, ti): (step, src, kv tile id, first position) per key tile, plus
+// the closed-form length check; returns the count (-2 on a length mismatch).
+int block_walk(const ra::Geometry& g, int seg, int ti, int rows, int* out, int cap) {
+  const int r = ra::seg_owner(g, seg);
+  const int q_lo = seg * g.seg_len + ti * g.tile;
+  const int q_valid = std::min(rows, ra::seg_tokens(g, seg) - ti * g.tile);
+  if (q_valid <= 0) return 0;
+  ra::KvIter it;
+  it.init(g, r, q_lo, q_valid);
+  ra::KvTile kv;
+  int n = 0;
+  while (it.next(g, kv)) {
+    if (n < cap) {
+      out[4 * n + 0] = kv.step;
+      out[4 * n + 1] = kv.src;
+      out[4 * n + 2] = kv.id;
+      out[4 * n + 3] = kv.lo;
+    }
+    ++n;
+  }
+  if (ra::kv_walk_length(g, r, q_lo, q_valid) != n) return -2;
   return n;
 }
 
@@ -57,6 +84,16 @@ int ra_test_geometry(int S, int P, int order, int tile, int* facts) {
   facts[1] = g.n_seg;
   facts[2] = g.nt;
   return RA_OK;
+}
+
+// Walk of the two-tile block whose first tile is `qid` (= segment * nt +
+// tile) of a fixed-length call.
+int ra_test_block_walk(int S, int P, int causal, int order, int step, int qid, int* out,
+                       int cap) {
+  ra::Geometry g;
+  if (ra::make_geometry(1, 1, 1, S, 128, P, causal, 0.f, order, step, 128, &g) != RA_OK)
+    return -1;
+  return block_walk(g, qid / g.nt, qid % g.nt, 2 * g.tile, out, cap);
 }
 
 // Walk of query tile `qid` (= segment * nt + tile) of a fixed-length call.

@@ -56,6 +56,7 @@ def harness(tmp_path_factory):
     ip = ctypes.POINTER(ctypes.c_int)
     lib.ra_test_geometry.argtypes = [ctypes.c_int] * 4 + [ip]
     lib.ra_test_walk.argtypes = [ctypes.c_int] * 7 + [ip, ctypes.c_int]
+    lib.ra_test_block_walk.argtypes = [ctypes.c_int] * 6 + [ip, ctypes.c_int]
     lib.ra_test_walk_varlen.argtypes = ([ip] + [ctypes.c_int] * 10 + [ip, ctypes.c_int, ip, ip])
     lib.ra_test_extents.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(ctypes.c_longlong)]
     lib.ra_test_qwalk.argtypes = [ctypes.c_int] * 6 + [ip, ctypes.c_int]
@@ -120,6 +121,47 @@ def test_single_step_walk_is_that_step_of_the_ring(harness, order):
             for t in range(P):
                 _check_all_tiles(harness, S, P, True, order, 128, step=t)
                 _check_all_tiles(harness, S, P, False, order, 64, step=t)
+
+
+def _check_blocks(lib, S, P, causal, order, step=-1):
+    """The forward kernel pairs query tiles 2i and 2i+1 of a segment in one
+    block walking the key tiles of the higher tile with tokens. Each tile's
+    own walk (the oracle's tile visits) must be that block walk with the key
+    tiles wholly after the tile left out, in the same order; the closed-form
+    walk length the MMA issuers use must equal the walk's length."""
+    tile = 128
+    want = oracle.tile_visits(S, P, causal, ORACLE_ORDER[order], tile)
+    seg_len, n_seg, nt = _geometry(lib, S, P, order, tile)
+    for seg in range(n_seg):
+        for ti in range(0, nt, 2):
+            qid = seg * nt + ti
+            out = _buf(4 * CAP)
+            n = lib.ra_test_block_walk(S, P, int(causal), ORDERS[order], step, qid, out, CAP)
+            assert 0 <= n <= CAP, (S, P, causal, order, step, qid, n)
+            blk = [tuple(out[4 * i:4 * i + 4]) for i in range(n)]
+            for k in (0, 1):
+                if ti + k >= nt:
+                    continue
+                lo = seg * seg_len + (ti + k) * tile
+                rows = min(tile, min(S, (seg + 1) * seg_len) - lo)
+                w = [tuple(e[:3]) for e in want[qid + k] if step < 0 or e[0] == step]
+                if rows <= 0:
+                    assert w == []
+                    continue
+                hi = lo + rows - 1
+                mine = [e[:3] for e in blk if not (causal and e[3] > hi)]
+                assert mine == w, (S, P, causal, order, step, qid, k)
+
+
+@pytest.mark.parametrize("order", ["contiguous", "zigzag"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_walk_covers_both_tiles(harness, order, causal):
+    for S in (1, 5, 127, 128, 129, 255, 256, 257, 300, 600, 777, 1001, 4096, 4100):
+        for P in (1, 2, 3, 4, 8):
+            _check_blocks(harness, S, P, causal, order)
+    for t in range(4):
+        _check_blocks(harness, 1001, 4, causal, order, step=t)
+    _check_blocks(harness, 32768, 8, causal, order)
 
 
 def _clamped_length(cu, b, total, max_seqlen):
