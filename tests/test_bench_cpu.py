@@ -32,9 +32,9 @@ def test_traffic_entries_name_real_workloads():
 def test_traffic_follows_the_source_digest(monkeypatch):
     w = wl.HEADLINE
     digest = bench._kernel_digest("attn_tc")
-    entry = dict(bench.TRAFFIC["attn_tc"])
-    monkeypatch.setitem(bench.TRAFFIC, "attn_tc", dict(entry, sha256_16=digest))
-    assert bench._traffic("attn_tc", w) == entry["bytes_per_launch"][w]
+    entry = {"sha256_16": digest, "bytes_per_launch": {w: 1234567}}
+    monkeypatch.setitem(bench.TRAFFIC, "attn_tc", entry)
+    assert bench._traffic("attn_tc", w) == 1234567
     assert bench._traffic("attn_tc", "no_such_workload") is None
     monkeypatch.setitem(bench.TRAFFIC, "attn_tc", dict(entry, sha256_16="0" * 16))
     assert bench._traffic("attn_tc", w) is None
