@@ -51,9 +51,7 @@ MERGE_METRIC = "LSE merge GB/s (algorithmic bytes)"
 # stored with it (see _kernel_digest).
 TRAFFIC = {
     "attn_tc": {"sha256_16": "5702fb6fbea06592", "bytes_per_launch": {}},
-    "merge": {"sha256_16": "110b882547236ed1", "bytes_per_launch": {
-        "merge_p8_s64k": 8657131264 + 1038706688,
-    }},
+    "merge": {"sha256_16": "57e019f17a6b1f8b", "bytes_per_launch": {}},
 }
 KERNEL_SOURCES = {
     "attn_tc": ("attn_tc.cu", "checks.cuh", "fastmath.cuh", "ring_iter.cuh", "sm100.cuh",
