@@ -51,7 +51,7 @@ MERGE_METRIC = "LSE merge GB/s (algorithmic bytes)"
 # workload; an entry holds only while the kernel's sources have the digest
 # stored with it (see _kernel_digest).
 TRAFFIC = {
-    "attn_tc": {"sha256_16": "5702fb6fbea06592", "bytes_per_launch": {
+    "attn_tc": {"sha256_16": "5819352996e5e4ab", "bytes_per_launch": {
         "bf16_s32k_causal_zigzag": 835921920 + 254403840,
         "bf16_s16k_d64": 402877952 + 119391232,
         "bf16_s128k_gqa_causal": 2578347264 + 1054976768,

@@ -71,7 +71,7 @@ typedef enum {
   RA_OK = 0,
   RA_ERR_NULL = 1,     /* a required pointer is NULL                              */
   RA_ERR_SHAPE = 2,    /* a size <= 0, H_q % H_kv != 0, merge n out of range       */
-  RA_ERR_HEADDIM = 3,  /* D is not 64 or 128                                       */
+  RA_ERR_HEADDIM = 3,  /* D is not 64 or 128 (attention), not 32-256 (merge)     */
   RA_ERR_ALIGN = 4,    /* a data pointer is not 16-byte aligned                    */
   RA_ERR_DTYPE = 5,    /* unknown dtype or order value                             */
   RA_ERR_DEVICE = 6,   /* current device is not compute capability 10.3            */
@@ -96,7 +96,11 @@ enum { RA_CLASS_SKIP = 0, RA_CLASS_FULL = 1, RA_CLASS_PARTIAL = 2 };
 
 /*
  * ring_attn_fwd - exact attention computed as a ring of P virtual ranks,
- * bfloat16 inputs and output, contiguous chunk order.
+ * bfloat16 inputs and output, contiguous chunk order. Defined by glossary
+ * "sequence parallelism transformers", §Ring Attention ("Block-Wise
+ * Attention", "Ring Communication", "Computation": each rank keeps its query
+ * block, attends to every key/value block as it passes, and accumulates
+ * exactly the full-attention result).
  *
  * All P ring steps run inside one kernel launch: every query tile keeps its
  * running (max, sum, unnormalised output) on chip across steps, which is the
@@ -112,7 +116,9 @@ ra_status ring_attn_fwd(const void* q, const void* k, const void* v,
                         int causal, float scale, void* stream);
 
 /*
- * ring_attn_fwd_ex - ring_attn_fwd with every option.
+ * ring_attn_fwd_ex - ring_attn_fwd with every option. Defined by the same
+ * glossary, §Ring Attention (the per-step partial results of `step`), and
+ * §Implementation Considerations ("Load Balancing": the zig-zag `order`).
  *
  * dtype   RA_BF16 (tensor-core path) or RA_F32 (exact float32 CUDA-core path).
  * order   RA_ORDER_CONTIGUOUS (rank r owns [rS/P, (r+1)S/P)) or
@@ -381,7 +387,10 @@ ra_status attn_lse_merge_n(const void* const* o, const float* const* lse,
                            int B, int H, int S, int D, int dtype, void* stream);
 
 /*
- * ring_attn_plan - the ring schedule as an int32 table, host only.
+ * ring_attn_plan - the ring schedule as an int32 table, host only. Defined
+ * by glossary "sequence parallelism transformers", §Sequence Parallelism
+ * Fundamentals (P chunks of S/P tokens) and §Ring Attention ("Ring
+ * Communication": at step t rank r holds the block of rank (r - t) mod P).
  * One row of RA_PLAN_COLS ints per (rank, step), rank-major then step:
  *   rank, step, src = (rank - step) mod P, class of the whole (query chunk,
  *   key chunk) pair, segment length L (padded, see above), first and second

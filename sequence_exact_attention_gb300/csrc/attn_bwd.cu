@@ -162,7 +162,7 @@ bwd_prep_kernel(const Geometry gp, const __nv_bfloat16* __restrict__ out,
   const int b = bh / gp.H_q, h = bh % gp.H_q;
   Geometry gv;
   int row0 = 0;
-  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0);
+  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0, threadIdx.x == 0 ? status : nullptr);
   const Geometry& g = kVarlen ? gv : gp;
   const size_t srow = seg_rows(gp, b, seg, row0, kVarlen).grow;
   const size_t lrow = lse_base(gp, b, h, seg, row0, kVarlen);
@@ -256,7 +256,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
   // packed variable-length sequences: b is the sequence, `g` its geometry
   Geometry gv;
   int row0 = 0;
-  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0);
+  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0, threadIdx.x == 0 ? status : nullptr);
   const Geometry& g = kVarlen ? gv : gp;
   const SegRows kr = seg_rows(gp, b, kseg, row0, kVarlen);   // the key tile's rows
   const int src = seg_owner(g, kseg);
@@ -542,7 +542,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
   // packed variable-length sequences: b is the sequence, `g` its geometry
   Geometry gv;
   int row0 = 0;
-  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0);
+  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0, threadIdx.x == 0 ? status : nullptr);
   const Geometry& g = kVarlen ? gv : gp;
   const SegRows qr = seg_rows(gp, b, seg, row0, kVarlen);    // the query tile's rows
   const int r = seg_owner(g, seg);

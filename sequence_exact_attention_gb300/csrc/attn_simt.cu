@@ -59,7 +59,7 @@ attn_simt_kernel(const Geometry gp, const float* __restrict__ q,
   const int b = bh / gp.H_q, h = bh % gp.H_q;
   Geometry gv;
   int row0 = 0;
-  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0);
+  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0, threadIdx.x == 0 ? status : nullptr);
   const Geometry& g = kVarlen ? gv : gp;
   const int q_lo = seg * g.seg_len + ti * kRows;
   const int q_valid = tile_tokens(g, seg, ti);     // <= 0: a tile of padding only

@@ -301,7 +301,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int blk = qb - seg * nb;
   Geometry gv;
   int row0 = 0;
-  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0);
+  if constexpr (kVarlen) varlen_geometry(gp, b, gv, row0, threadIdx.x == 0 ? status : nullptr);
   const Geometry& g = kVarlen ? gv : gp;
   const int r = seg_owner(g, seg);
   const int q_lo = seg * g.seg_len + blk * kBlockRows;

@@ -171,7 +171,8 @@ const char* ring_attn_strerror(int status) {
     case RA_OK: return "ok";
     case RA_ERR_NULL: return "a required pointer is NULL";
     case RA_ERR_SHAPE: return "invalid shape (sizes must be positive; H_q divisible by H_kv)";
-    case RA_ERR_HEADDIM: return "unsupported head dimension (D must be 64 or 128)";
+    case RA_ERR_HEADDIM:
+      return "unsupported head dimension (attention: D 64 or 128; merge: D 32, 64, 128 or 256)";
     case RA_ERR_ALIGN: return "misaligned pointer (tensors need 16-byte alignment, lse/log/status 4-byte)";
     case RA_ERR_DTYPE: return "unknown dtype or chunk order";
     case RA_ERR_DEVICE: return "no usable CUDA device of compute capability 10.3 (GB300)";

@@ -44,13 +44,21 @@ __device__ __forceinline__ int tile_tokens(const Geometry& g, int seg, int ti) {
 // ceil(S_b / n_seg) positions, padded like any uneven length. `row0` is the
 // sequence's first row in the packed tensors. Offsets are clamped into
 // [0, total] and lengths to [0, S], so a malformed table cannot move any
-// access outside the tensors.
+// access outside the tensors. The checked build also reports such a table:
+// when clamping changes an offset or a length it sets RA_ERR_RANGE in
+// `status` (if given).
 __device__ __forceinline__ void varlen_geometry(const Geometry& gp, int b, Geometry& gs,
-                                                int& row0) {
-  int lo = __ldg(gp.cu_seqlens + b);
-  int hi = __ldg(gp.cu_seqlens + b + 1);
-  lo = min(max(lo, 0), gp.total);
-  hi = min(max(hi, lo), gp.total);
+                                                int& row0, int* status = nullptr) {
+  const int lo_raw = __ldg(gp.cu_seqlens + b);
+  const int hi_raw = __ldg(gp.cu_seqlens + b + 1);
+  const int lo = min(max(lo_raw, 0), gp.total);
+  const int hi = min(max(hi_raw, lo), gp.total);
+#ifdef RA_DEBUG_CHECKS
+  if (status && (lo != lo_raw || hi != hi_raw || hi - lo > gp.S))
+    atomicExch(status, (int)RA_ERR_RANGE);
+#else
+  (void)status;
+#endif
   gs = gp;
   gs.S = min(hi - lo, gp.S);
   gs.seg_len = (gs.S + gp.n_seg - 1) / gp.n_seg;

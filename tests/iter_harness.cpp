@@ -11,11 +11,11 @@ using std::max;
 using std::min;
 }  // namespace ra
 #define __ldg(p) (*(p))
-#include "ring_iter.cuh"
-#include "q_iter.cuh"
 // the checked build's range checks, with the device atomic as a plain store
 #define RA_DEBUG_CHECKS
 #define atomicExch(p, v) (*(p) = (v))
+#include "ring_iter.cuh"
+#include "q_iter.cuh"
 #include "checks.cuh"
 
 namespace {
@@ -123,6 +123,20 @@ int ra_test_walk_varlen(const int* cu_seqlens, int n_seq, int total, int max_seq
   facts[1] = g.seg_len;
   facts[2] = g.nt;
   return walk(g, seg, ti, out, cap);
+}
+
+// The checked build's report on packed sequence b's offsets: the status word
+// varlen_geometry leaves (0, or RA_ERR_RANGE when it had to clamp).
+int ra_test_varlen_status(const int* cu_seqlens, int n_seq, int total, int max_seqlen, int b) {
+  ra::Geometry gp;
+  if (ra::make_geometry(n_seq, 1, 1, max_seqlen, 128, 1, 1, 0.f, 0, -1, 128, &gp) != RA_OK)
+    return -1;
+  gp.cu_seqlens = cu_seqlens;
+  gp.total = total;
+  ra::Geometry g;
+  int row0 = 0, status = 0;
+  ra::varlen_geometry(gp, b, g, row0, &status);
+  return status;
 }
 
 // The dK/dV kernel's walk for key tile `kid` (= segment * nt + tile) of a

@@ -123,3 +123,34 @@ def test_checked_build_is_in_range_and_identical(library, name):
     assert len(got) == len(want)
     for i, (a, b) in enumerate(zip(got, want)):
         assert torch.equal(a, b), f"{name}: result {i} differs between the builds"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_checked_build_reports_a_sequence_longer_than_max_seqlen(library, dtype):
+    """A packed batch whose offsets describe a sequence longer than the
+    max_seqlen the call passes: the kernels clamp it (every access stays
+    inside the tensors), and the checked build reports the malformed table
+    as RA_ERR_RANGE in the status word instead of leaving it at 0. The
+    backward reports it the same way."""
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    g = torch.Generator().manual_seed(79)
+    total = 400
+    q, k, v, dout = (torch.randn(total, h, 64, generator=g).to(tdt).to(DEV) for h in (2, 1, 1, 2))
+    cu = torch.tensor([0, 100, 400], dtype=torch.int32, device=DEV)   # second sequence: 300 rows
+    binding.use_library("debug")
+    st = _status()
+    out, lse = binding.ring_attn_fwd_varlen(q, k, v, cu, 256, 2, True, order="zigzag",
+                                            dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 10, binding.strerror(int(st.item()))      # RA_ERR_RANGE
+    if dtype == "bf16":
+        st = _status()
+        binding.ring_attn_bwd_varlen(q, k, v, out, lse, dout, cu, 256, 2, True, order="zigzag",
+                                     dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 10
+    # the same table with a max_seqlen that covers it is clean
+    st = _status()
+    binding.ring_attn_fwd_varlen(q, k, v, cu, 300, 2, True, order="zigzag", dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0

@@ -60,6 +60,7 @@ def harness(tmp_path_factory):
     lib.ra_test_walk_varlen.argtypes = ([ip] + [ctypes.c_int] * 10 + [ip, ctypes.c_int, ip, ip])
     lib.ra_test_extents.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(ctypes.c_longlong)]
     lib.ra_test_qwalk.argtypes = [ctypes.c_int] * 6 + [ip, ctypes.c_int]
+    lib.ra_test_varlen_status.argtypes = [ip] + [ctypes.c_int] * 4
     lp = ctypes.POINTER(ctypes.c_longlong)
     lib.ra_test_rows.argtypes = [ctypes.c_int] * 11 + [lp, lp, ctypes.c_int]
     lib.ra_test_in_range.argtypes = [ctypes.c_longlong] * 3 + [ip]
@@ -306,3 +307,20 @@ def test_row_addressing_of_every_layout(harness, S, P):
                     assert got == ([(p * B + b) * C + (x - p * C) for x in positions],
                                    [((p * B + b) * H + h) * C + (x - p * C)
                                     for x in positions])
+
+
+@pytest.mark.parametrize("cu,total,max_seqlen,b,flagged", [
+    ((0, 100, 300), 300, 200, 0, False),       # well formed
+    ((0, 100, 300), 300, 200, 1, False),
+    ((0, 100, 350), 300, 250, 1, True),        # last offset past total
+    ((0, 250, 300), 300, 200, 0, True),        # a sequence longer than max_seqlen
+    ((0, 120, 100, 300), 300, 200, 1, True),   # decreasing offsets
+    ((-5, 100, 300), 300, 200, 0, True),       # negative first offset
+])
+def test_checked_build_reports_clamped_offsets(harness, cu, total, max_seqlen, b, flagged):
+    """The checked build sets RA_ERR_RANGE when the packed offsets need
+    clamping (the release build clamps silently), so a caller can tell a
+    malformed cu_seqlens from a good run."""
+    carr = (ctypes.c_int * len(cu))(*cu)
+    st = harness.ra_test_varlen_status(carr, len(cu) - 1, total, max_seqlen, b)
+    assert st == (10 if flagged else 0)
