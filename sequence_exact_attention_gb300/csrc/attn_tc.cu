@@ -280,20 +280,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work item: one block of two query tiles. Block order: (batch, kv
-  // head) outermost, so the CTAs resident at one time read the keys/values of
-  // one or two kv heads and find them in L2; then blocks by decreasing
-  // position (decreasing causal work, longest first); the query heads sharing
-  // the kv head innermost, so they read the same key tiles at the same time.
+  // ---- work item: one block of two query tiles. The query heads sharing a
+  // kv head are innermost, so they read the same key tiles at the same time.
+  // Blocks come by decreasing position (decreasing causal work, longest
+  // first): within each (batch, kv head), which is outermost, so the CTAs
+  // resident at one time read the keys/values of one or two kv heads and find
+  // them in L2; or, when every head's keys and values fit in L2 (qb_major),
+  // across all heads, so the grid ends with the shortest blocks of all.
   // With packed variable-length sequences, b is the sequence and the grid is
   // sized by the longest one; `g` is then this sequence's own geometry.
   const int grp = gp.H_q / gp.H_kv;
   const int nb = (gp.nt + 1) >> 1;                 // blocks per segment
   const int n_qb = gp.n_seg * nb;
+  const int n_bhk = gp.B * gp.H_kv;
   const int hg = (int)(blockIdx.x % grp);
   const int rest = (int)(blockIdx.x / grp);
-  const int qb = n_qb - 1 - rest % n_qb;
-  const int bhk = rest / n_qb;
+  const int qb = n_qb - 1 - (gp.qb_major ? rest / n_bhk : rest % n_qb);
+  const int bhk = gp.qb_major ? rest % n_bhk : rest / n_qb;
   const int b = bhk / gp.H_kv, hk = bhk % gp.H_kv;
   const int h = hk * grp + hg;
   const int bh = b * gp.H_q + h;
@@ -693,13 +696,20 @@ ra_status launch_typed(const Geometry& g, const CUtensorMap& mq, const CUtensorM
                        int log_stride, int* status, cudaStream_t stream) {
   using C = Cfg<D>;
   auto kern = attn_tc_kernel<D, kOutF32, kVarlen, kWithholdV0>;
+  // keys and values of every head within half of the 126 MB L2: order the
+  // grid longest block first across all heads
+  Geometry gl = g;
+  const long long kv_rows = g.cu_seqlens ? g.total
+                            : (g.shard_rows > 0 ? (long long)g.P * g.B * g.shard_rows
+                                                : (long long)g.B * g.S);
+  gl.qb_major = kv_rows * g.H_kv * g.D * 2 * 2 <= (64ll << 20) ? 1 : 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return RA_ERR_LAUNCH;
   // one block of two query tiles per CTA
   const long long grid = (long long)g.n_seg * ((g.nt + 1) / 2) * g.B * g.H_q;
   if (grid > 0x7fffffffLL) return RA_ERR_RANGE;
-  kern<<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, g, out, lse, vlog,
+  kern<<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, gl, out, lse, vlog,
                                                             log_stride, status);
   return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
 }

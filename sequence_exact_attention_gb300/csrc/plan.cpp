@@ -41,6 +41,7 @@ ra_status make_geometry(int B, int H_q, int H_kv, int S, int D, int P,
   g->cu_seqlens = nullptr;
   g->total = 0;
   g->shard_rows = 0;
+  g->qb_major = 0;
   return RA_OK;
 }
 

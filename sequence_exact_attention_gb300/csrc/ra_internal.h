@@ -36,6 +36,11 @@ struct Geometry {
   // [P, B, shard_rows, H, D] (rank p's rows [p * shard_rows, ...) of every
   // batch contiguous), chunks contiguous with shard_rows = seg_len.
   int shard_rows;
+  // Forward grid order: 0 = (batch, kv head) outermost, so the CTAs resident
+  // at one time share one head's keys and values in L2; 1 = query block
+  // outermost (globally longest first), for problems whose keys and values
+  // fit in L2 anyway.
+  int qb_major;
 };
 
 // Host-side planning helpers (plan.cpp).
