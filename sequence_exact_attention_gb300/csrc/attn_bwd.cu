@@ -78,8 +78,7 @@ struct Cfg {
   static constexpr int bDP = 6;       // dP (or dP^T) in TMEM
   static constexpr int bP = 7;        // 256 arrivals: pass 1 done (P^T stored / S read)
   static constexpr int bDS = 8;       // 256 arrivals: pass 2 done (dS stored)
-  static constexpr int bAccV = 9;     // dV MMA of a visit done
-  static constexpr int bAccK = 10;    // dK MMA (or dQ MMA) of a visit done
+  static constexpr int bAccK = 10;    // dK/dV kernel: the last visit's dV and dK done
   static constexpr int bFinal = 11;
   static constexpr int bAccB = 12;    // [2] dQ MMA of a visit done, per dS buffer
   static_assert(kColAcc + D + 128 <= kTmemCols, "dQ kernel: two dS buffers after dQ");
@@ -126,7 +125,6 @@ __device__ __forceinline__ void init_barriers(BarFn bar, volatile int* abort_fla
     mbar_init(bar(C::bDP), 1);
     mbar_init(bar(C::bP), 256);
     mbar_init(bar(C::bDS), 256);
-    mbar_init(bar(C::bAccV), 1);
     mbar_init(bar(C::bAccK), 1);
     mbar_init(bar(C::bFinal), 1);
     mbar_init(bar(C::bAccB + 0), 1);
@@ -347,15 +345,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
           issue_s(0);
         }
       }
+      // dP^T(j) overwrites the dS^T(j-1) that dK(j-1) reads, and S^T(j+1)
+      // the P^T(j) that dV(j) reads: this thread issues both pairs in that
+      // order and the tensor core executes one thread's MMAs in issue order,
+      // so neither waits for the other to complete (a wait would drain the
+      // tensor core: it holds only the few MMAs queued behind the last issue).
       int j = 0;
       while (ok && have) {
         const int st = j & 1;
-        const uint32_t pj = (uint32_t)(j - 1) & 1;     // parity of visit j-1
         const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
-        // dP^T(j) overwrites the dS^T(j-1) that dK(j-1) reads
-        if (j > 0) ok = mbar_wait(bar(C::bAccK), pj, abort_flag, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + kColDP, v_kmaj + kstep_off(kk), do_kmaj + so + kstep_off(kk), id_s,
@@ -368,13 +366,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int kk = 0; kk < kT / 16; ++kk)
           umma_ts(tmem + kColAcc, tmem + kColS + pcol(kk), do_mn + so + (uint64_t)(kk * 2048 >> 4),
                   id_acc, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(C::bAccV));
-        // S^T(j+1) overwrites the P^T(j) that dV(j) reads
         have = it.next(g, qt);
         if (have) {
           ok = mbar_wait(bar(C::bFull + ((j + 1) & 1)), (uint32_t)((j + 1) >> 1) & 1, abort_flag,
-                         kTimeoutNs) &&
-               mbar_wait(bar(C::bAccV), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+                         kTimeoutNs);
           if (!ok) break;
           tc_fence_after();
           issue_s(j + 1);
@@ -386,7 +381,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int kk = 0; kk < kT / 16; ++kk)
           umma_ts(tmem + kColAcc + D, tmem + kColDP + pcol(kk),
                   q_mn + so + (uint64_t)(kk * 2048 >> 4), id_acc, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(C::bAccK));
+        if (!have) umma_commit(bar(C::bAccK));        // the accumulators are final
         umma_commit(bar(C::bFree + st));
         ++j;
       }
@@ -469,7 +464,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
       ++j;
     }
     // ---- epilogue: this warp's half of the dV and dK columns, as bf16 rows
-    if (ok && j > 0) ok = mbar_wait(bar(C::bAccK), (uint32_t)(j - 1) & 1, abort_flag, kTimeoutNs);
+    // (the issuer commits bAccK once, after the last visit's dK)
+    if (ok && j > 0) ok = mbar_wait(bar(C::bAccK), 0, abort_flag, kTimeoutNs);
     if (ok) {
       tc_fence_after();
       const size_t off = ((kr.grow + kpos) * g.H_kv + hk) * D;
