@@ -51,19 +51,19 @@ MERGE_METRIC = "LSE merge GB/s (algorithmic bytes)"
 # workload; an entry holds only while the kernel's sources have the digest
 # stored with it (see _kernel_digest).
 TRAFFIC = {
-    "attn_tc": {"sha256_16": "5819352996e5e4ab", "bytes_per_launch": {
-        "bf16_s32k_causal_zigzag": 835921920 + 254403840,
-        "bf16_s16k_d64": 402877952 + 119391232,
-        "bf16_s128k_gqa_causal": 2578347264 + 1054976768,
-        "bf16_s4k_causal": 100766208 + 12308224,
-        "bf16_s32760_uneven_causal_zigzag": 836316928 + 254769920,
-        "bf16_varlen_32k_causal_zigzag": 823360768 + 254599936,
-        "bf16_ulysses_s16k_b2_causal": 805491200 + 252054016,
+    "attn_tc": {"sha256_16": "db55ed923a3f9be9", "bytes_per_launch": {
+        "bf16_s32k_causal_zigzag": 837056768 + 254355968,
+        "bf16_s16k_d64": 402817024 + 119393536,
+        "bf16_s128k_gqa_causal": 2580883200 + 1055959552,
+        "bf16_s4k_causal": 104811008 + 8747008,
+        "bf16_s32760_uneven_causal_zigzag": 837335552 + 254595328,
+        "bf16_varlen_32k_causal_zigzag": 824230656 + 254592768,
+        "bf16_ulysses_s16k_b2_causal": 805599488 + 252041472,
     }},
     # the merge was captured on S = 8192 (1.15 GiB on the device) and scaled by
     # 65536 / 8192 = 8: a streaming kernel whose bytes grow with the rows
-    "merge": {"sha256_16": "57e019f17a6b1f8b", "bytes_per_launch": {
-        "merge_p8_s64k": 8 * (1082153728 + 112560640),
+    "merge": {"sha256_16": "6fac89657b942f3c", "bytes_per_launch": {
+        "merge_p8_s64k": 8 * (1082154240 + 112507904),
     }},
 }
 KERNEL_SOURCES = {
