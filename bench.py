@@ -51,14 +51,14 @@ MERGE_METRIC = "LSE merge GB/s (algorithmic bytes)"
 # workload; an entry holds only while the kernel's sources have the digest
 # stored with it (see _kernel_digest).
 TRAFFIC = {
-    "attn_tc": {"sha256_16": "db55ed923a3f9be9", "bytes_per_launch": {
-        "bf16_s32k_causal_zigzag": 837056768 + 254355968,
-        "bf16_s16k_d64": 402817024 + 119393536,
-        "bf16_s128k_gqa_causal": 2580883200 + 1055959552,
-        "bf16_s4k_causal": 104811008 + 8747008,
-        "bf16_s32760_uneven_causal_zigzag": 837335552 + 254595328,
-        "bf16_varlen_32k_causal_zigzag": 824230656 + 254592768,
-        "bf16_ulysses_s16k_b2_causal": 805599488 + 252041472,
+    "attn_tc": {"sha256_16": "f41c04241a8868d4", "bytes_per_launch": {
+        "bf16_s32k_causal_zigzag": 845592832 + 255588864,
+        "bf16_s16k_d64": 402826752 + 119429888,
+        "bf16_s128k_gqa_causal": 2722089728 + 1057852416,
+        "bf16_s4k_causal": 106970368 + 10819584,
+        "bf16_s32760_uneven_causal_zigzag": 846161664 + 255913216,
+        "bf16_varlen_32k_causal_zigzag": 828785920 + 255517440,
+        "bf16_ulysses_s16k_b2_causal": 805435904 + 252942592,
     }},
     # the merge was captured on S = 8192 (1.15 GiB on the device) and scaled by
     # 65536 / 8192 = 8: a streaming kernel whose bytes grow with the rows
@@ -297,11 +297,36 @@ def run_reference(args, w):
     return 0
 
 
-def _config(w):
+L2_MIB = 126
+FLUSH_MIB = 256
+
+
+def _inputs_mib(w):
     esz = 2 if w.dtype == "bf16" else 4
-    in_mib = w.B * w.S * (w.H_q + 2 * w.H_kv) * w.D * esz / 2**20
-    l2 = (f"inputs larger than L2 (q+k+v {in_mib:.0f} MiB vs 126 MiB L2)" if in_mib > 126
-          else f"inputs fit in L2 (q+k+v {in_mib:.1f} MiB); no flush")
+    return w.B * w.S * (w.H_q + 2 * w.H_kv) * w.D * esz / 2**20
+
+
+def _l2_flusher(w, dev, stream):
+    """None when the workload's inputs are larger than L2; else a call that
+    writes a buffer twice the size of L2 on `stream`, run between timed
+    launches so that no launch finds the previous one's data in L2."""
+    if _inputs_mib(w) > L2_MIB:
+        return None
+    import torch
+    buf = torch.empty(FLUSH_MIB << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        with torch.cuda.stream(stream):
+            buf.zero_()
+    return flush
+
+
+def _config(w):
+    in_mib = _inputs_mib(w)
+    l2 = (f"inputs larger than L2 (q+k+v {in_mib:.0f} MiB vs {L2_MIB} MiB L2)" if in_mib > L2_MIB
+          else f"inputs fit in L2 (q+k+v {in_mib:.1f} MiB): L2 flushed before every timed "
+               f"launch ({FLUSH_MIB} MiB write, outside the launch's events); value from "
+               f"the launches' own events")
     return {"workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "S": w.S,
             "D": w.D, "P": w.P, "causal": w.causal, "order": w.order,
             "input_dist": f"N(0,{w.std}^2) {w.dtype}", "l2": l2,
@@ -417,11 +442,14 @@ def run_ours(args, w):
           for _ in range(args.steps)]
     if dist:
         dist.barrier()
+    flush = _l2_flusher(w, dev, stream)
     torch.cuda.synchronize(dev)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
+        if flush is not None:
+            flush()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -432,6 +460,9 @@ def run_ours(args, w):
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if flush is not None:
+        # the flushes between launches are not the workload's time
+        total_ms = sum(launch_ms)
     if int(status.item()) != 0:
         raise RuntimeError("device-side wait expired in the timed region")
     total_ms = _max_over_ranks(total_ms, dist, dev)
@@ -510,8 +541,9 @@ CONFIG_SWEEP = ("fp32_s256", "bf16_s4k_causal", "bf16_s128k_gqa_causal", "merge_
                 "bf16_s16k_d64", "bf16_s32k_causal_zigzag_bwd")
 
 
-def _event_times(fn, warm, timed, stream, dev):
-    """CUDA-event milliseconds of `timed` calls of fn after `warm` calls."""
+def _event_times(fn, warm, timed, stream, dev, between=None):
+    """CUDA-event milliseconds of `timed` calls of fn after `warm` calls; with
+    `between`, that call runs before every timed call, outside its events."""
     import torch
     for _ in range(warm):
         fn()
@@ -519,6 +551,8 @@ def _event_times(fn, warm, timed, stream, dev):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(timed)]
     for a, b in ev:
+        if between is not None:
+            between()
         a.record(stream)
         fn()
         b.record(stream)
@@ -553,7 +587,8 @@ def _sweep_fwd(w, dev, stream, peaks):
 
     clocks = ClockSampler(dev.index)
     clocks.start()
-    ms = _event_times(step, 2, 3 if w.flop > 5e13 else 10, stream, dev)
+    ms = _event_times(step, 2, 3 if w.flop > 5e13 else 10, stream, dev,
+                      between=_l2_flusher(w, dev, stream))
     clk = clocks.stop()
     kernel_ms = statistics.mean(ms)
     achieved = w.flop / (kernel_ms / 1e3) / 1e12
@@ -755,6 +790,7 @@ def run_bwd(args, w):
     clocks.start()
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in phases] for _ in range(args.steps)]
+    flush = _l2_flusher(w, dev, stream)
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -762,6 +798,8 @@ def run_bwd(args, w):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(args.steps):
+        if flush is not None:
+            flush()
         step(evs[i])
     t1.record(stream)
     torch.cuda.synchronize(dev)
@@ -771,6 +809,10 @@ def run_bwd(args, w):
     if int(status.item()) != 0:
         raise RuntimeError("device-side wait expired in the timed region")
     total_ms = t0.elapsed_time(t1)
+    if flush is not None:
+        # each step from its first launch's start to its last launch's end,
+        # without the flushes between steps
+        total_ms = sum(e[0][0].elapsed_time(e[-1][1]) for e in evs)
     total_ms = _max_over_ranks(total_ms, dist, dev)
     flop = bwd_flop(w)
     value = _job_rate(world, flop, args.steps, total_ms) / 1e12

@@ -47,6 +47,10 @@
 //                    earlier by the same thread, so softmax may rescale O_i
 //   pfull[i]         P_i(j) written and O_i rescaled (256 arrivals)
 //   odone[i]         the last PV_i done (epilogue may read O_i)
+//   staged[i]        bf16 output tile i staged in Q_i's buffer (D = 128, full
+//                    tiles): the producer writes it out with TMA stores, one
+//                    16 KB box of whole rows at a time, instead of every
+//                    thread storing 16-byte pieces 8 KB apart
 // Every barrier's next phase depends on its waiter's own progress, so parity
 // waits are unambiguous.
 //
@@ -113,7 +117,8 @@ struct Cfg {
   static constexpr int bSFull = bDone + kKBuf;      // [2]
   static constexpr int bPFull = bSFull + 2;         // [2], 128 arrivals
   static constexpr int bODone = bPFull + 2;         // [2]
-  static constexpr int bFinal = bODone + 2;
+  static constexpr int bStaged = bODone + 2;        // [2] output tile i staged (8 warps)
+  static constexpr int bFinal = bStaged + 2;
   static constexpr int kNumBars = bFinal + 1;
   static constexpr int kHolderOff = kBarBytes - 16;   // TMEM base address
   static constexpr int kNeverOff = kBarBytes - 12;    // stays 0: waits that ignore aborts
@@ -237,6 +242,39 @@ __device__ __forceinline__ void store_out_row(uint32_t tO, bool have_o, bool row
   }
 }
 
+// Epilogue of one softmax thread, staged for a TMA store: its N columns of
+// O at tO (from column col0 of the row), times 1/l, as bf16 into the 128-row
+// tile at smem_tile, laid out as the store's 64-column boxes with the
+// 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r mod 8)).
+template <int N>
+__device__ __forceinline__ void stage_out_row(uint32_t tO, bool have_o, uint32_t smem_tile,
+                                              int row, int col0, float inv_l) {
+#pragma unroll
+  for (int c = 0; c < N / 32; ++c) {
+    uint32_t uo[32];
+    if (have_o) {
+      tmem_ld32(tO + c * 32, uo);
+      tmem_ld_wait(uo);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) uo[i] = 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int chunk = (col0 + c * 32) / 8 + i;          // 16-byte chunk of the row
+      const uint32_t addr = smem_tile + (uint32_t)((chunk / 8) * kBoxBytes + row * 128 +
+                                                   (((chunk % 8) ^ (row & 7)) * 16));
+      const uint32_t w0 = pack_bf16x2(__uint_as_float(uo[8 * i + 0]) * inv_l, __uint_as_float(uo[8 * i + 1]) * inv_l);
+      const uint32_t w1 = pack_bf16x2(__uint_as_float(uo[8 * i + 2]) * inv_l, __uint_as_float(uo[8 * i + 3]) * inv_l);
+      const uint32_t w2 = pack_bf16x2(__uint_as_float(uo[8 * i + 4]) * inv_l, __uint_as_float(uo[8 * i + 5]) * inv_l);
+      const uint32_t w3 = pack_bf16x2(__uint_as_float(uo[8 * i + 6]) * inv_l, __uint_as_float(uo[8 * i + 7]) * inv_l);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1),
+                   "r"(w2), "r"(w3)
+                   : "memory");
+    }
+  }
+}
+
 // S_i = Q_i K^T: M = 128 query rows, N = 128 keys, K = D in steps of 16.
 template <int D>
 __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
@@ -265,10 +303,15 @@ template <int D, bool kOutF32, bool kVarlen, bool kWithholdV0>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const Geometry gp,
+               const __grid_constant__ CUtensorMap tm_v,
+               const __grid_constant__ CUtensorMap tm_o, const Geometry gp,
                void* __restrict__ out, float* __restrict__ lse,
-               int* __restrict__ vlog, int log_stride, int* __restrict__ status) {
+               int* __restrict__ vlog, int log_stride, int* __restrict__ status,
+               int tma_out) {
   using C = Cfg<D>;
+  // Full bf16 output tiles go out through TMA stores at D = 128 (a row part
+  // is 128 bytes); at D = 64 the per-row stores measured faster.
+  constexpr bool kTmaOut = !kOutF32 && D == 128;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -356,6 +399,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_init(bar(C::bSFull + i), 1);
       mbar_init(bar(C::bPFull + i), 32 * kSoftmaxWarps);
       mbar_init(bar(C::bODone + i), 1);
+      if (kTmaOut) mbar_init(bar(C::bStaged + i), kSoftmaxWarps);
     }
     for (int i = 0; i < C::kKBuf; ++i) {
       mbar_init(bar(C::bKFull + i), 1);
@@ -438,6 +482,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           mbar_wait(bar(C::bVFull + jj % C::kVBuf), (uint32_t)(jj / C::kVBuf) & 1, never,
                     kTimeoutNs);
       for (int i = 0; i < (two ? 2 : 1); ++i) mbar_wait(bar(C::bQFull + i), 0, never, kTimeoutNs);
+      // full output tiles, once the softmax warps have staged them in Q_i's
+      // buffer: one TMA store of whole rows each; their shared memory is read
+      // before the CTA leaves
+      if (kTmaOut && tma_out && ok) {
+        for (int i = 0; i < (two ? 2 : 1); ++i) {
+          if (q_valid - i * kTile < kTile) continue;
+          if (!mbar_wait(bar(C::bStaged + i), 0, abort_flag, kTimeoutNs)) break;
+          const uint32_t tile_smem = base + C::kQOff + (uint32_t)(i * C::kTileBytes);
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_store_4d(&tm_o, tile_smem + bx * kBoxBytes, bx * 64, h, trow + q_lo + i * kTile,
+                         tbat);
+          bulk_commit_group();
+        }
+        bulk_wait_read_all();
+      }
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -666,10 +725,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
       if (!ok) break;
       const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-      const size_t row_off = ((orow + q_pos) * g.H_q + h) * D + part * (D / 2);
-      const bool store = row_valid && in_range((long long)row_off, D / 2, extent_q(gp), status);
-      store_out_row<D / 2, kOutF32>(tmem + t_lane + kOCol + (uint32_t)(qi * D + part * (D / 2)),
-                                    j > 0, store, out, row_off, inv_l);
+      const uint32_t tO = tmem + t_lane + kOCol + (uint32_t)(qi * D + part * (D / 2));
+      if (kTmaOut && tma_out && q_valid - qi * kTile >= kTile) {
+        // a full tile: staged in Q_i's buffer (every MMA reading it is done)
+        // and written by one TMA store of whole rows
+        const uint32_t tile_smem = base + C::kQOff + (uint32_t)(qi * C::kTileBytes);
+        stage_out_row<D / 2>(tO, j > 0, tile_smem, row, part * (D / 2), inv_l);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::bStaged + qi));   // the producer stores it
+      } else {
+        const size_t row_off = ((orow + q_pos) * g.H_q + h) * D + part * (D / 2);
+        const bool store = row_valid && in_range((long long)row_off, D / 2, extent_q(gp), status);
+        store_out_row<D / 2, kOutF32>(tO, j > 0, store, out, row_off, inv_l);
+      }
       if (row_valid && lse && part == 0 &&
           in_range((long long)(lrow + q_pos), 1, extent_lse(gp), status))
         lse[lrow + q_pos] =
@@ -692,8 +761,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 // ------------------------------------------------------------------ host
 template <int D, bool kOutF32, bool kVarlen = false, bool kWithholdV0 = false>
 ra_status launch_typed(const Geometry& g, const CUtensorMap& mq, const CUtensorMap& mk,
-                       const CUtensorMap& mv, void* out, float* lse, int* vlog,
-                       int log_stride, int* status, cudaStream_t stream) {
+                       const CUtensorMap& mv, const CUtensorMap& mo, bool tma_out, void* out,
+                       float* lse, int* vlog, int log_stride, int* status, cudaStream_t stream) {
   using C = Cfg<D>;
   auto kern = attn_tc_kernel<D, kOutF32, kVarlen, kWithholdV0>;
   // keys and values of every head within half of the 126 MB L2: order the
@@ -709,8 +778,8 @@ ra_status launch_typed(const Geometry& g, const CUtensorMap& mq, const CUtensorM
   // one block of two query tiles per CTA
   const long long grid = (long long)g.n_seg * ((g.nt + 1) / 2) * g.B * g.H_q;
   if (grid > 0x7fffffffLL) return RA_ERR_RANGE;
-  kern<<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, gl, out, lse, vlog,
-                                                            log_stride, status);
+  kern<<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, gl, out, lse, vlog,
+                                                            log_stride, status, tma_out ? 1 : 0);
   return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
 }
 
@@ -722,15 +791,29 @@ bool make_maps(CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv, const Geometry
          make_bshd_map(mv, v, nb, rows, g.H_kv, g.D, kTile);
 }
 
+// The bf16 output, laid out like q, as a TMA store target. False (the kernel
+// then stores row by row) when the pointer does not suit a tensor map, and
+// always in the checked build, whose per-row stores check every offset.
+bool make_out_map(CUtensorMap* mo, const Geometry& g, const void* out, int nb, int rows) {
+#ifdef RA_DEBUG_CHECKS
+  (void)mo; (void)g; (void)out; (void)nb; (void)rows;
+  return false;
+#else
+  if (reinterpret_cast<uintptr_t>(out) % 16 != 0) return false;
+  return make_bshd_map(mo, out, nb, rows, g.H_q, g.D, kTile);
+#endif
+}
+
 }  // namespace
 
 ra_status launch_attn_tc_withheld(const Geometry& g, const void* q, const void* k,
                                   const void* v, void* out, float* lse, int* dev_status,
                                   cudaStream_t stream) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_maps(&mq, &mk, &mv, g, q, k, v, g.B, g.S)) return RA_ERR_LAUNCH;
   if (g.D != 128) return RA_ERR_HEADDIM;
-  return launch_typed<128, false, false, true>(g, mq, mk, mv, out, lse, nullptr, 0,
+  const bool tma_out = make_out_map(&mo, g, out, g.B, g.S);
+  return launch_typed<128, false, false, true>(g, mq, mk, mv, mo, tma_out, out, lse, nullptr, 0,
                                                dev_status, stream);
 }
 
@@ -738,35 +821,43 @@ ra_status launch_attn_tc_varlen(const Geometry& g, const void* q, const void* k,
                                 const void* v, void* out, float* lse, int* dev_status,
                                 cudaStream_t stream) {
   // the packed tensors are mapped as one batch of `total` rows
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_maps(&mq, &mk, &mv, g, q, k, v, 1, g.total)) return RA_ERR_LAUNCH;
+  const bool tma_out = make_out_map(&mo, g, out, 1, g.total);
   if (g.D == 64)
-    return launch_typed<64, false, true>(g, mq, mk, mv, out, lse, nullptr, 0, dev_status, stream);
-  return launch_typed<128, false, true>(g, mq, mk, mv, out, lse, nullptr, 0, dev_status, stream);
+    return launch_typed<64, false, true>(g, mq, mk, mv, mo, tma_out, out, lse, nullptr, 0,
+                                         dev_status, stream);
+  return launch_typed<128, false, true>(g, mq, mk, mv, mo, tma_out, out, lse, nullptr, 0,
+                                        dev_status, stream);
 }
 
 ra_status launch_attn_tc_sharded(const Geometry& g, const void* q, const void* k,
                                  const void* v, void* out, float* lse, int* dev_status,
                                  cudaStream_t stream) {
   // [P, B, C, H, D] mapped as P*B batches of C rows
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_maps(&mq, &mk, &mv, g, q, k, v, g.P * g.B, g.shard_rows)) return RA_ERR_LAUNCH;
+  const bool tma_out = make_out_map(&mo, g, out, g.P * g.B, g.shard_rows);
   if (g.D == 64)
-    return launch_typed<64, false>(g, mq, mk, mv, out, lse, nullptr, 0, dev_status, stream);
-  return launch_typed<128, false>(g, mq, mk, mv, out, lse, nullptr, 0, dev_status, stream);
+    return launch_typed<64, false>(g, mq, mk, mv, mo, tma_out, out, lse, nullptr, 0, dev_status,
+                                   stream);
+  return launch_typed<128, false>(g, mq, mk, mv, mo, tma_out, out, lse, nullptr, 0, dev_status,
+                                  stream);
 }
 
 ra_status launch_attn_tc(const Geometry& g, const void* q, const void* k, const void* v,
                          void* out, float* lse, int* visit_log, int log_stride,
                          int* dev_status, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_maps(&mq, &mk, &mv, g, q, k, v, g.B, g.S)) return RA_ERR_LAUNCH;
   const bool f32_out = g.step >= 0;
+  // single-step partials are float32: stored row by row
+  const bool tma_out = !f32_out && make_out_map(&mo, g, out, g.B, g.S);
   if (g.D == 64)
-    return f32_out ? launch_typed<64, true>(g, mq, mk, mv, out, lse, visit_log, log_stride, dev_status, stream)
-                   : launch_typed<64, false>(g, mq, mk, mv, out, lse, visit_log, log_stride, dev_status, stream);
-  return f32_out ? launch_typed<128, true>(g, mq, mk, mv, out, lse, visit_log, log_stride, dev_status, stream)
-                 : launch_typed<128, false>(g, mq, mk, mv, out, lse, visit_log, log_stride, dev_status, stream);
+    return f32_out ? launch_typed<64, true>(g, mq, mk, mv, mo, false, out, lse, visit_log, log_stride, dev_status, stream)
+                   : launch_typed<64, false>(g, mq, mk, mv, mo, tma_out, out, lse, visit_log, log_stride, dev_status, stream);
+  return f32_out ? launch_typed<128, true>(g, mq, mk, mv, mo, false, out, lse, visit_log, log_stride, dev_status, stream)
+                 : launch_typed<128, false>(g, mq, mk, mv, mo, tma_out, out, lse, visit_log, log_stride, dev_status, stream);
 }
 
 }  // namespace ra
