@@ -538,7 +538,8 @@ def run_ours(args, w):
 # the roofline fraction, the stored DRAM traffic, clocks and parity against
 # the float64 oracle on sampled rows.
 CONFIG_SWEEP = ("fp32_s256", "bf16_s4k_causal", "bf16_s128k_gqa_causal", "merge_p8_s64k",
-                "bf16_s16k_d64", "bf16_s32k_causal_zigzag_bwd")
+                "bf16_s16k_d64", "bf16_s32k_causal_zigzag_bwd", "bf16_varlen_32k_causal_zigzag",
+                "bf16_ulysses_s16k_b2_causal", "bf16_s32760_uneven_causal_zigzag")
 
 
 def _event_times(fn, warm, timed, stream, dev, between=None):
@@ -615,6 +616,103 @@ def _sweep_fwd(w, dev, stream, peaks):
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "traffic": traffic},
             "clocks": clk, "parity": parity}
+
+
+def _layout_entry(w, cfg, metric, kname, ms, clk, parity, peaks):
+    kernel_ms = statistics.mean(ms)
+    achieved = w.flop / (kernel_ms / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    return {"workload": w.name, "config": cfg, "metric": metric, "value": achieved, "unit": UNIT,
+            "kernel": kname, "kernel_ms": kernel_ms, "kernel_ms_min": min(ms),
+            "launches": len(ms),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                         "frac": achieved / peak, "traffic": _traffic("attn_tc", w.name)},
+            "clocks": clk, "parity": parity}
+
+
+def _sweep_varlen(w, dev, stream, peaks):
+    """Packed batch: CUDA-event time of ring_attn_fwd_varlen, parity on 8
+    sampled rows of every sequence against the oracle on that sequence alone."""
+    import numpy as np
+    import torch
+    import oracle
+    from sequence_exact_attention_gb300 import binding
+    from sequence_exact_attention_gb300.workloads import make_varlen
+    q, k, v, cu = make_varlen(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    cud = torch.tensor(cu, dtype=torch.int32, device=dev)
+    out, lse = torch.empty_like(qd), torch.empty(w.H_q, w.total, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        binding.ring_attn_fwd_varlen(qd, kd, vd, cud, w.max_seqlen, w.P, w.causal, w.scale,
+                                     w.order, out=out, lse=lse, dev_status=status, stream=stream)
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    ms = _event_times(step, 2, 10, stream, dev)
+    clk = clocks.stop()
+    rng = np.random.default_rng(13)
+    eo_max = eo_sum = el_max = el_sum = 0.0
+    n_o = n_l = 0
+    out_h, lse_h = out.double().cpu().numpy(), lse.double().cpu().numpy()
+    for i, n in enumerate(w.lengths):
+        lo = cu[i]
+        rows = np.sort(rng.choice(n, min(8, n), replace=False))
+        want_o, want_l = oracle.attention_rows(q[None, lo:lo + n], k[None, lo:lo + n],
+                                               v[None, lo:lo + n], w.causal, w.scale, rows)
+        eo = np.abs(out_h[lo + rows] - want_o[0])
+        el = np.abs(lse_h[:, lo + rows] - want_l[0])
+        eo_max, el_max = max(eo_max, eo.max()), max(el_max, el.max())
+        eo_sum, el_sum = eo_sum + eo.sum(), el_sum + el.sum()
+        n_o, n_l = n_o + eo.size, n_l + el.size
+    parity = _tol_check({"out": (eo_max, eo_sum / n_o), "lse": (el_max, el_sum / n_l)},
+                        {"max": 2e-2, "mean": 2e-3})
+    parity["rows"] = "8 sampled rows of every sequence"
+    parity["status_word"] = int(status.item())
+    return _layout_entry(w, _varlen_config(w), VARLEN_METRIC, "attn_tc_kernel<128,false,true>",
+                         ms, clk, parity, peaks)
+
+
+def _sweep_ulysses(w, dev, stream, peaks):
+    """Sequence-parallel layout: CUDA-event time of ring_attn_fwd_ulysses,
+    parity on sampled positions against full attention over each sequence."""
+    import numpy as np
+    import torch
+    import oracle
+    from sequence_exact_attention_gb300 import binding
+    from sequence_exact_attention_gb300.workloads import make_sharded_qkv
+    q, k, v = make_sharded_qkv(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    P, B, C = q.shape[0], q.shape[1], q.shape[2]
+    out = torch.empty_like(qd)
+    lse = torch.empty(P, B, w.H_q, C, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        binding.ring_attn_fwd_ulysses(qd, kd, vd, w.S, w.causal, w.scale, out=out, lse=lse,
+                                      dev_status=status, stream=stream)
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    ms = _event_times(step, 2, 10, stream, dev)
+    clk = clocks.stop()
+
+    def seq(x):      # [P, B, C, H, D] -> [B, S, H, D]: shard p holds positions [pC, pC + C)
+        return x.permute(1, 0, 2, 3, 4).reshape(B, P * C, x.shape[3], x.shape[4])[:, :w.S]
+
+    rows = np.sort(np.random.default_rng(14).choice(w.S, 32, replace=False))
+    want_o, want_l = oracle.attention_rows(seq(q), seq(k), seq(v), w.causal, w.scale, rows)
+    p_idx, c_idx = torch.from_numpy(rows // C), torch.from_numpy(rows % C)
+    got_o = out.cpu()[p_idx, :, c_idx].permute(1, 0, 2, 3).double().numpy()
+    got_l = lse.cpu()[p_idx, :, :, c_idx].permute(1, 2, 0).double().numpy()
+    eo, el = np.abs(got_o - want_o), np.abs(got_l - want_l)
+    parity = _tol_check({"out": (eo.max(), eo.mean()), "lse": (el.max(), el.mean())},
+                        {"max": 2e-2, "mean": 2e-3})
+    parity["rows"] = 32
+    parity["status_word"] = int(status.item())
+    return _layout_entry(w, _ulysses_config(w), ULYSSES_METRIC, "attn_tc_kernel<128,false,false>",
+                         ms, clk, parity, peaks)
 
 
 def _sweep_merge(w, dev, stream, peaks):
@@ -709,6 +807,7 @@ def _configs_sweep(dev, stream):
     """One entry per workload of CONFIG_SWEEP; a failing entry reports its error."""
     import torch
     from sequence_exact_attention_gb300.workloads import (BWD_WORKLOADS, MERGE_WORKLOADS,
+                                                          ULYSSES_WORKLOADS, VARLEN_WORKLOADS,
                                                           WORKLOADS)
     peaks, _ = _peaks()
     res = []
@@ -716,6 +815,10 @@ def _configs_sweep(dev, stream):
         try:
             if name in MERGE_WORKLOADS:
                 e = _sweep_merge(MERGE_WORKLOADS[name], dev, stream, peaks)
+            elif name in VARLEN_WORKLOADS:
+                e = _sweep_varlen(VARLEN_WORKLOADS[name], dev, stream, peaks)
+            elif name in ULYSSES_WORKLOADS:
+                e = _sweep_ulysses(ULYSSES_WORKLOADS[name], dev, stream, peaks)
             elif name in BWD_WORKLOADS:
                 e = _sweep_bwd(BWD_WORKLOADS[name], dev, stream, peaks)
             else:
