@@ -9,9 +9,10 @@
 //   dQ_i = scale sum_j ds_ij k_j      dK_j = scale sum_i ds_ij q_i
 //   delta_i = <dO_i, o_i>
 // Three launches on the caller's stream:
-//  1. bwd_prep_kernel: per query row, lse in base 2 and delta, into the
-//     caller's workspace, tile-padded (padding rows get lse = +inf, which
-//     makes their p exactly 0, and delta = 0).
+//  1. bwd_prep_kernel: per query row, -lse in base 2 and -delta (negated, so
+//     that the gradient kernels add them with packed FMAs), into the
+//     caller's workspace, tile-padded (padding rows get -lse = -inf, which
+//     makes their p exactly 0, and -delta = 0).
 //  2. bwd_dkdv_kernel: one CTA per key tile of one kv head. It walks the
 //     query tiles that see the tile in ring order -- the owner rank's own
 //     queries first (step 0), then ranks src+1, src+2, ... (the block's trip
@@ -34,6 +35,7 @@
 #include <cuda_bf16.h>
 
 #include "checks.cuh"
+#include "fastmath.cuh"
 #include "q_iter.cuh"
 #include "ra_internal.h"
 #include "ring_iter.cuh"
@@ -43,6 +45,7 @@ namespace ra {
 namespace {
 
 using namespace sm100;
+using namespace fastmath;
 
 constexpr int kT = 128;                         // tile rows (queries or keys)
 constexpr int kThreads = 320;
@@ -189,8 +192,8 @@ bwd_prep_kernel(const Geometry gp, const __nv_bfloat16* __restrict__ out,
   acc += __shfl_xor_sync(0xffffffffu, acc, 4);
   if (sub == 0) {
     const bool lse_ok = valid && in_range((long long)(lrow + pos), 1, extent_lse(gp), status);
-    lse2[gid] = lse_ok ? lse[lrow + pos] * kLog2e : INFINITY;
-    delta[gid] = valid ? acc : 0.f;
+    lse2[gid] = lse_ok ? -(lse[lrow + pos] * kLog2e) : -INFINITY;
+    delta[gid] = valid ? -acc : 0.f;
   }
 }
 
@@ -396,7 +399,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
     const uint32_t c0 = (uint32_t)(hf * 64);          // this warp's first column
     const int kpos = kv_lo + row;
-    const float sl2 = g.scale_log2;
+    const uint64_t sl2x2 = pack2(g.scale_log2, g.scale_log2);
     QIter it;
     it.init(g, src, kv_lo, kv_valid, h0, h0 + grp);
     QTile qt;
@@ -409,9 +412,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
       tc_fence_after();
       const float* stat =
           reinterpret_cast<const float*>(base_ptr + C::kStage0 + st * C::kStageBytes + 2 * C::kTileBytes);
-      const float2* l2v = reinterpret_cast<const float2*>(stat + c0);
-      const float2* dlv = reinterpret_cast<const float2*>(stat + kT + c0);
-      const int lim = qt.mask ? kpos - qt.lo - (int)c0 : -1;   // column c masked iff c < lim
+      // the visit's per-column -lse2 and -delta, as packed pairs
+      const uint64_t* nl2v = reinterpret_cast<const uint64_t*>(stat + c0);
+      const uint64_t* ndlv = reinterpret_cast<const uint64_t*>(stat + kT + c0);
       // ---- pass 1: P^T = exp2(S^T * scale * log2 e - lse2), bf16 into TMEM
       float p[64];
       {
@@ -421,16 +424,26 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
         tmem_ld_wait();
         reg_fence(u0);
         reg_fence(u1);
-        uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
-          const float2 l2 = l2v[i >> 1];
           const uint32_t s0 = i < 32 ? u0[i] : u1[i - 32];
           const uint32_t s1 = i < 32 ? u0[i + 1] : u1[i - 31];
-          p[i] = i < lim ? 0.f : ex2_approx(fmaf(__uint_as_float(s0), sl2, -l2.x));
-          p[i + 1] = i + 1 < lim ? 0.f : ex2_approx(fmaf(__uint_as_float(s1), sl2, -l2.y));
-          pk[i >> 1] = pack_bf16x2(p[i], p[i + 1]);
+          float x0, x1;
+          unpack2(ffma2(pack2(__uint_as_float(s0), __uint_as_float(s1)), sl2x2, nl2v[i >> 1]),
+                  x0, x1);
+          p[i] = ex2_approx(x0);
+          p[i + 1] = ex2_approx(x1);
         }
+        // visits the causal rule cuts: column c is masked iff c < lim
+        if (qt.mask) {
+          const int lim = kpos - qt.lo - (int)c0;
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i < lim) p[i] = 0.f;
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) pk[i >> 1] = pack_bf16x2(p[i], p[i + 1]);
         tmem_st32(tmem + t_lane + kColS + c0, pk);
         tmem_st_wait();
       }
@@ -450,11 +463,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
-          const float2 dl = dlv[i >> 1];
           const uint32_t d0 = i < 32 ? u0[i] : u1[i - 32];
           const uint32_t d1 = i < 32 ? u0[i + 1] : u1[i - 31];
-          pk[i >> 1] = pack_bf16x2(p[i] * (__uint_as_float(d0) - dl.x),
-                                   p[i + 1] * (__uint_as_float(d1) - dl.y));
+          const uint64_t t2 = fadd2(pack2(__uint_as_float(d0), __uint_as_float(d1)), ndlv[i >> 1]);
+          float r0, r1;
+          unpack2(ffma2(pack2(p[i], p[i + 1]), t2, 0ull), r0, r1);
+          pk[i >> 1] = pack_bf16x2(r0, r1);
         }
         tmem_st32(tmem + t_lane + kColDP + c0, pk);
         tmem_st_wait();
@@ -672,11 +686,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
     const uint32_t c0 = (uint32_t)(hf * 64);
     const int q_pos = q_lo + row;
-    const float sl2 = g.scale_log2;
+    const uint64_t sl2x2 = pack2(g.scale_log2, g.scale_log2);
     const long long wi = ws_tile(gp, bh, seg, ti) + row;
     const bool wi_ok = in_range(wi, 1, ws_tile(gp, gp.B * gp.H_q, 0, 0), status);
-    const float l2_row = wi_ok ? lse2[wi] : INFINITY;     // +inf on padding rows: p = 0
-    const float dl_row = wi_ok ? delta[wi] : 0.f;
+    // the row's -lse2 (-inf on padding rows: p = 0) and -delta, as pairs
+    const float nl2_row = wi_ok ? lse2[wi] : -INFINITY;
+    const float ndl_row = wi_ok ? delta[wi] : 0.f;
+    const uint64_t nl2x2 = pack2(nl2_row, nl2_row), ndlx2 = pack2(ndl_row, ndl_row);
     KvIter it;
     it.init(g, r, q_lo, q_valid);
     KvTile kv;
@@ -686,10 +702,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (ok) ok = mbar_wait(bar(C::bS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
       if (!ok) { ++j; continue; }
       tc_fence_after();
-      // key column c of this warp is allowed iff c < lim
-      const int lim = (kv.work == kMask
-                           ? (g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid)
-                           : kT) - (int)c0;
       // ---- pass 1: P = exp2(S * scale * log2 e - lse2), kept in registers
       float p[64];
       {
@@ -700,9 +712,21 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
         reg_fence(u0);
         reg_fence(u1);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const uint32_t s = i < 32 ? u0[i] : u1[i - 32];
-          p[i] = i < lim ? ex2_approx(fmaf(__uint_as_float(s), sl2, -l2_row)) : 0.f;
+        for (int i = 0; i < 64; i += 2) {
+          const uint32_t s0 = i < 32 ? u0[i] : u1[i - 32];
+          const uint32_t s1 = i < 32 ? u0[i + 1] : u1[i - 31];
+          float x0, x1;
+          unpack2(ffma2(pack2(__uint_as_float(s0), __uint_as_float(s1)), sl2x2, nl2x2), x0, x1);
+          p[i] = ex2_approx(x0);
+          p[i + 1] = ex2_approx(x1);
+        }
+        // key tiles the causal rule cuts, and ragged tails: key column c of
+        // this warp is allowed iff c < lim
+        if (kv.work == kMask) {
+          const int lim = (g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid) - (int)c0;
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i >= lim) p[i] = 0.f;
         }
       }
       tc_fence_before();
@@ -723,8 +747,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int i = 0; i < 64; i += 2) {
           const uint32_t d0 = i < 32 ? u0[i] : u1[i - 32];
           const uint32_t d1 = i < 32 ? u0[i + 1] : u1[i - 31];
-          pk[i >> 1] = pack_bf16x2(p[i] * (__uint_as_float(d0) - dl_row),
-                                   p[i + 1] * (__uint_as_float(d1) - dl_row));
+          const uint64_t t2 = fadd2(pack2(__uint_as_float(d0), __uint_as_float(d1)), ndlx2);
+          float r0, r1;
+          unpack2(ffma2(pack2(p[i], p[i + 1]), t2, 0ull), r0, r1);
+          pk[i >> 1] = pack_bf16x2(r0, r1);
         }
         // dS buffer j mod 2 was last read by dQ(j-2)
         if (j >= 2) {
