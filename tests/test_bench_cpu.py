@@ -168,3 +168,15 @@ def test_parity_record_of_the_bench_line():
 def test_device_info_never_raises():
     info = bench._device_info(0)
     assert ("name" in info and "sm_count" in info) or "error" in info
+
+
+def test_l2_rule_follows_the_input_size():
+    """Inputs larger than L2 are timed back to back; inputs that fit are
+    flushed out of L2 before every timed launch, and the config says which."""
+    big, small = wl.WORKLOADS[wl.HEADLINE], wl.WORKLOADS["bf16_s4k_causal"]
+    assert bench._inputs_mib(big) > bench.L2_MIB
+    assert "larger than L2" in bench._config(big)["l2"]
+    assert bench._l2_flusher(big, None, None) is None
+    assert bench._inputs_mib(small) <= bench.L2_MIB
+    assert "flushed" in bench._config(small)["l2"]
+    assert bench.FLUSH_MIB > bench.L2_MIB
