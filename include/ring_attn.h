@@ -220,8 +220,9 @@ ra_status ring_attn_visit_log_len(int B, int H_q, int S, int D, int P,
  * ring_attn_bwd_workspace - bytes of device workspace ring_attn_bwd needs
  * for this shape (written to *bytes). Host only; never touches the GPU.
  * The workspace holds two float32 statistics per query row of the forward
- * result (its lse in base 2 and delta_i = <dout_i, out_i>), stored per
- * (b, h, query tile) with every tile padded to the kernels' tile height.
+ * result, negated (-lse in base 2 and -delta_i, delta_i = <dout_i, out_i>),
+ * stored per (b, h, query tile) with every tile padded to the kernels' tile
+ * height; its contents are the library's own and only its phases read them.
  * Errors: RA_ERR_NULL (bytes NULL), RA_ERR_SHAPE, RA_ERR_HEADDIM,
  * RA_ERR_DTYPE (order), RA_ERR_RANGE.
  */
@@ -311,7 +312,7 @@ enum { RA_BWD_PREP = 1, RA_BWD_DKDV = 2, RA_BWD_DQ = 4, RA_BWD_ALL = 7 };
  * ring_attn_bwd_ex - ring_attn_bwd restricted to the phases in `phases` (a
  * nonzero OR of RA_BWD_*, else RA_ERR_RANGE), enqueued in the order prep,
  * dK/dV, dQ; one kernel launch per phase. The prep phase writes the
- * workspace (lse in base 2 and delta per query row); the dK/dV phase
+ * workspace (-lse in base 2 and -delta per query row); the dK/dV phase
  * (writes dk, dv) and the dQ phase (writes dq) read it and are independent
  * of each other, so after the prep phase they may run on two streams at
  * once. A phase needs the prep phase of the same arguments to have run

@@ -165,7 +165,7 @@ def _ws_bytes(lib, B=1, Hq=2, S=256, D=64, P=4, order=0):
 
 
 def test_bwd_workspace_size(lib):
-    # per (b, h, query tile): 128 base-2 lse values and 128 deltas, float32;
+    # per (b, h, query tile): 128 negated base-2 lse values and 128 negated deltas, float32;
     # tiles are 128 rows, cut per segment (the last tile of a segment padded)
     st, n = _ws_bytes(lib, B=2, Hq=3, S=1000, D=128, P=4)        # segments of 250: 2 tiles
     assert st == RA_OK and n == 2 * (2 * 3 * 4 * 2 * 128) * 4
