@@ -51,14 +51,14 @@ MERGE_METRIC = "LSE merge GB/s (algorithmic bytes)"
 # workload; an entry holds only while the kernel's sources have the digest
 # stored with it (see _kernel_digest).
 TRAFFIC = {
-    "attn_tc": {"sha256_16": "f41c04241a8868d4", "bytes_per_launch": {
-        "bf16_s32k_causal_zigzag": 845592832 + 255588864,
-        "bf16_s16k_d64": 402826752 + 119429888,
-        "bf16_s128k_gqa_causal": 2722089728 + 1057852416,
-        "bf16_s4k_causal": 106970368 + 10819584,
-        "bf16_s32760_uneven_causal_zigzag": 846161664 + 255913216,
-        "bf16_varlen_32k_causal_zigzag": 828785920 + 255517440,
-        "bf16_ulysses_s16k_b2_causal": 805435904 + 252942592,
+    "attn_tc": {"sha256_16": "db34798df47de19e", "bytes_per_launch": {
+        "bf16_s32k_causal_zigzag": 845280256 + 256100864,
+        "bf16_s16k_d64": 402865920 + 119390464,
+        "bf16_s128k_gqa_causal": 2730051328 + 1058496768,
+        "bf16_s4k_causal": 108359424 + 10706432,
+        "bf16_s32760_uneven_causal_zigzag": 844002048 + 255716864,
+        "bf16_varlen_32k_causal_zigzag": 828577280 + 255613440,
+        "bf16_ulysses_s16k_b2_causal": 805553920 + 253317376,
     }},
     # the merge was captured on S = 8192 (1.15 GiB on the device) and scaled by
     # 65536 / 8192 = 8: a streaming kernel whose bytes grow with the rows
