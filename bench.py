@@ -533,7 +533,7 @@ def run_ours(args, w):
     return 0
 
 
-# The other workloads of the benchmark spec, measured in the same run as the headline
+# Every other workload, measured in the same run as the headline
 # (reported under "configs" of the headline line): kernel time by CUDA events,
 # the roofline fraction, the stored DRAM traffic, clocks and parity against
 # the float64 oracle on sampled rows.
