@@ -46,11 +46,9 @@ BWD = [_draw(8000 + i, 700) for i in range(24)]
 F32 = [_draw(6000 + i, 400) for i in range(12)]
 
 
-@pytest.mark.parametrize("case", FWD, ids=_ids(FWD))
-def test_random_forward_matches_oracle(case):
+def _forward_case(case, seed):
     B, H_q, H_kv, S, D, P, causal, order = case
-    w = AttnWorkload("rand", "bf16", B, H_q, H_kv, S, D, P, causal, order,
-                     seed=7500 + FWD.index(case))
+    w = AttnWorkload("rand", "bf16", B, H_q, H_kv, S, D, P, causal, order, seed=seed)
     q, k, v = make_qkv(w)
     dev = torch.device("cuda")
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -61,6 +59,11 @@ def test_random_forward_matches_oracle(case):
     want_o, want_l = oracle.attention_naive(q, k, v, causal, w.scale)
     assert_close(out, want_o, "bf16", "out")
     assert_close(lse, want_l, "bf16", "lse")
+
+
+@pytest.mark.parametrize("case", FWD, ids=_ids(FWD))
+def test_random_forward_matches_oracle(case):
+    _forward_case(case, 7500 + FWD.index(case))
 
 
 @pytest.mark.parametrize("case", F32, ids=_ids(F32))
@@ -160,3 +163,53 @@ def test_random_packed_backward_matches_oracle(case):
     check_grad("dq", dq, rq)
     check_grad("dk", dk, rk)
     check_grad("dv", dv, rv)
+
+
+MEDIUM = [(b, hq, hk, 2000 + s, d, p, c, o)
+          for b, hq, hk, s, d, p, c, o in (_draw(7700 + i, 2500) for i in range(6))]
+
+
+@pytest.mark.parametrize("case", MEDIUM, ids=_ids(MEDIUM))
+def test_random_medium_forward_matches_oracle(case):
+    """Lengths of 2000-4500: walks of up to 36 key tiles a block, so every
+    K/V slot is refilled many times over."""
+    _forward_case(case, 7800 + MEDIUM.index(case))
+
+
+CHECKED = [_draw(7900 + i, 900) for i in range(16)]
+
+
+@pytest.fixture
+def release_after():
+    prev = binding.use_library("release")
+    yield
+    binding.use_library(prev)
+
+
+@pytest.mark.parametrize("case", CHECKED, ids=_ids(CHECKED))
+def test_random_shapes_in_range_in_the_checked_build(release_after, case):
+    """The bounds-checked build (every index-computed global access tested
+    against its tensor's extent) leaves the status word at 0 on random shapes,
+    forward and backward, and gives the release build's results bit for bit."""
+    B, H_q, H_kv, S, D, P, causal, order = case
+    w = AttnWorkload("rand", "bf16", B, H_q, H_kv, S, D, P, causal, order,
+                     seed=7950 + CHECKED.index(case))
+    q, k, v = (t.cuda() for t in make_qkv(w))
+    dout = make_dout(w).cuda()
+
+    def run():
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out, lse = binding.ring_attn_fwd(q, k, v, P, causal, w.scale, order, dev_status=status)
+        grads = binding.ring_attn_bwd(q, k, v, out, lse, dout, P, causal, w.scale, order,
+                                      dev_status=status)
+        torch.cuda.synchronize()
+        return int(status.item()), [out, lse, *grads]
+
+    binding.use_library("release")
+    st, want = run()
+    assert st == 0
+    binding.use_library("debug")
+    st, got = run()
+    assert st == 0, binding.strerror(st)
+    for a, b in zip(got, want):
+        assert torch.equal(a, b)
