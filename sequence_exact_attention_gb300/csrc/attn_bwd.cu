@@ -407,7 +407,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
     bool ok = true;
     while (it.next(g, qt)) {
       const int st = j & 1;
-      if (ok) ok = mbar_wait(bar(C::bS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+      if (ok) ok = mbar_wait_warp(bar(C::bS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
       if (!ok) { ++j; continue; }
       tc_fence_after();
       const float* stat =
@@ -450,7 +450,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
       tc_fence_before();
       mbar_arrive(bar(C::bP));
       // ---- pass 2: dS^T = P^T * (dP^T - delta), bf16 into TMEM
-      ok = mbar_wait(bar(C::bDP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+      ok = mbar_wait_warp(bar(C::bDP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
       if (!ok) { ++j; continue; }
       tc_fence_after();
       {
@@ -479,7 +479,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     // ---- epilogue: this warp's half of the dV and dK columns, as bf16 rows
     // (the issuer commits bAccK once, after the last visit's dK)
-    if (ok && j > 0) ok = mbar_wait(bar(C::bAccK), 0, abort_flag, kTimeoutNs);
+    if (ok && j > 0) ok = mbar_wait_warp(bar(C::bAccK), 0, abort_flag, kTimeoutNs);
     if (ok) {
       tc_fence_after();
       const size_t off = ((kr.grow + kpos) * g.H_kv + hk) * D;
@@ -699,7 +699,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
     int j = 0;
     bool ok = true;
     while (it.next(g, kv)) {
-      if (ok) ok = mbar_wait(bar(C::bS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+      if (ok) ok = mbar_wait_warp(bar(C::bS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
       if (!ok) { ++j; continue; }
       tc_fence_after();
       // ---- pass 1: P = exp2(S * scale * log2 e - lse2), kept in registers
@@ -732,7 +732,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
       tc_fence_before();
       mbar_arrive(bar(C::bP));          // S may be overwritten
       // ---- pass 2: dS = P * (dP - delta), bf16 into TMEM
-      ok = mbar_wait(bar(C::bDP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+      ok = mbar_wait_warp(bar(C::bDP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
       if (!ok) { ++j; continue; }
       tc_fence_after();
       {
@@ -754,8 +754,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         // dS buffer j mod 2 was last read by dQ(j-2)
         if (j >= 2) {
-          ok = mbar_wait(bar(C::bAccB + (j & 1)), (uint32_t)((j >> 1) - 1) & 1, abort_flag,
-                         kTimeoutNs);
+          ok = mbar_wait_warp(bar(C::bAccB + (j & 1)), (uint32_t)((j >> 1) - 1) & 1,
+                              abort_flag, kTimeoutNs);
           if (!ok) { ++j; continue; }
           tc_fence_after();
         }
@@ -767,8 +767,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
       ++j;
     }
     if (ok && j > 0)
-      ok = mbar_wait(bar(C::bAccB + ((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1, abort_flag,
-                     kTimeoutNs);
+      ok = mbar_wait_warp(bar(C::bAccB + ((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1,
+                          abort_flag, kTimeoutNs);
     if (ok) {
       tc_fence_after();
       const size_t off = ((qr.grow + q_pos) * g.H_q + h) * D;

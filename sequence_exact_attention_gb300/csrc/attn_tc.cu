@@ -144,14 +144,6 @@ __device__ __forceinline__ bool mbar_test3(uint32_t b0, uint32_t p0, uint32_t b1
   return t0 && t1 && t2;
 }
 
-// A bounded wait whose outcome is the same in every lane of the warp (the
-// warp-wide tcgen05 loads and stores that follow need all 32 lanes).
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
-                                               volatile int* abort, uint64_t limit_ns) {
-  const bool ok = mbar_wait(bar, parity, abort, limit_ns);
-  return __all_sync(0xffffffffu, ok);
-}
-
 // The N columns of this thread's O row at tO, times alpha.
 template <int N>
 __device__ __forceinline__ void scale_cols(uint32_t tO, float alpha) {

@@ -82,6 +82,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// A bounded wait whose outcome is the same in every lane of the warp: the
+// warp-wide (.sync.aligned) tcgen05 loads and stores that follow a wait need
+// all 32 lanes, also when the wait gives up in some lanes only.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               volatile int* abort, uint64_t limit_ns) {
+  const bool ok = mbar_wait(bar, parity, abort, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar,
                                             int c0, int c1, int c2, int c3) {
