@@ -59,12 +59,14 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kBoxBytes = kT * 64 * 2;          // one TMA box: 128 rows x 64 bf16
 constexpr float kLog2e = 1.4426950408889634f;
 
+// dK/dV kernel: K and V stay resident; each visit's Q, dO and statistics
+// arrive together in a two-stage ring.
 template <int D>
 struct Cfg {
   static constexpr int kTileBytes = kT * D * 2;
   static constexpr int kBoxes = D / 64;
-  static constexpr int kFixA = 0;                          // K (dk/dv) or Q (dq)
-  static constexpr int kFixB = kTileBytes;                 // V (dk/dv) or dO (dq)
+  static constexpr int kFixA = 0;                          // K
+  static constexpr int kFixB = kTileBytes;                 // V
   static constexpr int kStage0 = 2 * kTileBytes;
   static constexpr int kStatBytes = 2 * kT * 4;            // lse2 and delta of a query tile
   static constexpr int kStageBytes = 2 * kTileBytes + kStatBytes;
@@ -77,18 +79,55 @@ struct Cfg {
   static constexpr int bFix = 0;
   static constexpr int bFull = 1;     // [2] stage loaded
   static constexpr int bFree = 3;     // [2] stage no longer read by the tensor cores
-  static constexpr int bS = 5;        // S (or S^T) in TMEM
-  static constexpr int bDP = 6;       // dP (or dP^T) in TMEM
-  static constexpr int bP = 7;        // 256 arrivals: pass 1 done (P^T stored / S read)
-  static constexpr int bDS = 8;       // 256 arrivals: pass 2 done (dS stored)
-  static constexpr int bAccK = 10;    // dK/dV kernel: the last visit's dV and dK done
+  static constexpr int bS = 5;        // S^T in TMEM
+  static constexpr int bDP = 6;       // dP^T in TMEM
+  static constexpr int bP = 7;        // 256 arrivals: pass 1 done (P^T stored)
+  static constexpr int bDS = 8;       // 256 arrivals: pass 2 done (dS^T stored)
+  static constexpr int bAccK = 10;    // the last visit's dV and dK done
   static constexpr int bFinal = 11;
-  static constexpr int bAccB = 12;    // [2] dQ MMA of a visit done, per dS buffer
-  static_assert(kColAcc + D + 128 <= kTmemCols, "dQ kernel: two dS buffers after dQ");
   static constexpr int kHolderOff = kBarBytes - 16;
   static constexpr int kNeverOff = kBarBytes - 12;
   static constexpr int kAbortOff = kBarBytes - 8;
   static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+// dQ kernel: Q and dO stay resident; keys and values arrive in rings of
+// their own, since K_j is read until dQ(j) (three slots) and V_j only by
+// dP(j) (two slots), so each slot is refilled as soon as its last product
+// is done and the next tile has landed before the issuer needs it.
+template <int D>
+struct CfgQ {
+  static constexpr int kTileBytes = kT * D * 2;
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kKBuf = 3;
+  static constexpr int kVBuf = 2;
+  static constexpr int kFixA = 0;                          // Q
+  static constexpr int kFixB = kTileBytes;                 // dO
+  static constexpr int kK0 = 2 * kTileBytes;
+  static constexpr int kV0 = kK0 + kKBuf * kTileBytes;
+  static constexpr int kBarOff = kV0 + kVBuf * kTileBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kUsed = kBarOff + kBarBytes + 1024;  // + alignment slack
+  // one CTA per SM, as in the other kernels
+  static constexpr int kSmemBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
+  static constexpr int bFix = 0;
+  static constexpr int bKFull = 1;                // [kKBuf]
+  static constexpr int bKFree = bKFull + kKBuf;   // [kKBuf] dQ of the slot's tile done
+  static constexpr int bVFull = bKFree + kKBuf;   // [kVBuf]
+  static constexpr int bVFree = bVFull + kVBuf;   // [kVBuf] dP of the slot's tile done
+  static constexpr int bS = bVFree + kVBuf;       // S in TMEM
+  static constexpr int bDP = bS + 1;              // dP in TMEM
+  static constexpr int bP = bDP + 1;              // 256 arrivals: pass 1 has read S
+  static constexpr int bDS = bP + 1;              // 256 arrivals: pass 2 done (dS stored)
+  static constexpr int bAccB = bDS + 1;           // [2] dQ MMA of a visit done, per dS buffer
+  static constexpr int bFinal = bAccB + 2;
+  static constexpr int kNumBars = bFinal + 1;
+  static constexpr int kHolderOff = kBarBytes - 16;
+  static constexpr int kNeverOff = kBarBytes - 12;
+  static constexpr int kAbortOff = kBarBytes - 8;
+  static_assert(kNumBars * 8 <= kHolderOff, "barrier area overflow");
+  static_assert(kColAcc + D + 128 <= kTmemCols, "two dS buffers after dQ");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -130,8 +169,6 @@ __device__ __forceinline__ void init_barriers(BarFn bar, volatile int* abort_fla
     mbar_init(bar(C::bDS), 256);
     mbar_init(bar(C::bAccK), 1);
     mbar_init(bar(C::bFinal), 1);
-    mbar_init(bar(C::bAccB + 0), 1);
-    mbar_init(bar(C::bAccB + 1), 1);
     *abort_flag = 0;
     *never = 0;
     fence_mbar_init();
@@ -513,10 +550,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
 }
 
 // ------------------------------------------------------------------ dQ
-// Per visit the tensor cores run S, dP, dQ; the compute warps read S (pass 1,
-// P kept in registers) and then dP (pass 2), writing bf16 dS into the first
-// 32 columns of their own dP column range. S of the next key tile is issued
-// as soon as pass 1 has read S, so it runs while dS and dQ are computed.
+// Per visit j the tensor cores run S(j), dP(j), dQ(j); the compute warps read
+// S (pass 1, P kept in registers) and then dP (pass 2), writing bf16 dS into
+// one of two TMEM buffers after the dQ accumulator. The issuer sends S(j+1)
+// as soon as pass 1 has read S(j), and dP(j+1) right after pass 2, ahead of
+// dQ(j), so both passes of the next visit find their product done. K_j stays
+// in its slot until dQ(j), V_j only until dP(j).
 template <int D, bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -525,7 +564,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_do, const Geometry gp,
               const float* __restrict__ lse2, const float* __restrict__ delta,
               __nv_bfloat16* __restrict__ dq, int* __restrict__ status) {
-  using C = Cfg<D>;
+  using C = CfgQ<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -560,7 +599,27 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int q_valid = tile_tokens(g, seg, ti);      // <= 0: padding only
   if (q_valid <= 0) return;      // no query, no gradient row: the CTA leaves at once
 
-  init_barriers<C>(bar, abort_flag, never);
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::bFix), 1);
+    for (int i = 0; i < C::kKBuf; ++i) {
+      mbar_init(bar(C::bKFull + i), 1);
+      mbar_init(bar(C::bKFree + i), 1);
+    }
+    for (int i = 0; i < C::kVBuf; ++i) {
+      mbar_init(bar(C::bVFull + i), 1);
+      mbar_init(bar(C::bVFree + i), 1);
+    }
+    mbar_init(bar(C::bS), 1);
+    mbar_init(bar(C::bDP), 1);
+    mbar_init(bar(C::bP), 256);
+    mbar_init(bar(C::bDS), 256);
+    mbar_init(bar(C::bAccB + 0), 1);
+    mbar_init(bar(C::bAccB + 1), 1);
+    mbar_init(bar(C::bFinal), 1);
+    *abort_flag = 0;
+    *never = 0;
+    fence_mbar_init();
+  }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
@@ -582,25 +641,38 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
       KvIter it;
       it.init(g, r, q_lo, q_valid);
       KvTile kv;
-      int j = 0;
+      int nk = 0, nv = 0;                  // K and V tiles loaded
+      int ks = 0, kn = 0, vs = 0, vn = 0;  // next slot of each ring, and its use count
       while (it.next(g, kv)) {
-        const int st = j & 1;
-        if (j >= 2 &&
-            !mbar_wait(bar(C::bFree + st), (uint32_t)((j >> 1) - 1) & 1, abort_flag, kTimeoutNs))
-          break;
-        const uint32_t sb = base + C::kStage0 + st * C::kStageBytes;
         const SegRows kr = seg_rows(gp, b, kv.seg, row0, kVarlen);
-        mbar_arrive_expect_tx(bar(C::bFull + st), 2 * C::kTileBytes);
-        for (int bx = 0; bx < C::kBoxes; ++bx) {
-          tma_load_4d(sb + bx * kBoxBytes, &tm_k, bar(C::bFull + st), bx * 64, hk,
-                      kr.trow + kv.lo, kr.tbat);
-          tma_load_4d(sb + C::kTileBytes + bx * kBoxBytes, &tm_v, bar(C::bFull + st), bx * 64, hk,
-                      kr.trow + kv.lo, kr.tbat);
-        }
-        ++j;
+        // K_j reuses the slot of K_{j-3}: free once dQ(j-3) is done
+        if (kn > 0 &&
+            !mbar_wait(bar(C::bKFree + ks), (uint32_t)(kn - 1) & 1, abort_flag, kTimeoutNs))
+          break;
+        mbar_arrive_expect_tx(bar(C::bKFull + ks), C::kTileBytes);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_4d(base + C::kK0 + ks * C::kTileBytes + bx * kBoxBytes, &tm_k,
+                      bar(C::bKFull + ks), bx * 64, hk, kr.trow + kv.lo, kr.tbat);
+        ++nk;
+        if (++ks == C::kKBuf) { ks = 0; ++kn; }
+        // V_j reuses the slot of V_{j-2}: free once dP(j-2) is done
+        if (vn > 0 &&
+            !mbar_wait(bar(C::bVFree + vs), (uint32_t)(vn - 1) & 1, abort_flag, kTimeoutNs))
+          break;
+        mbar_arrive_expect_tx(bar(C::bVFull + vs), C::kTileBytes);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_4d(base + C::kV0 + vs * C::kTileBytes + bx * kBoxBytes, &tm_v,
+                      bar(C::bVFull + vs), bx * 64, hk, kr.trow + kv.lo, kr.tbat);
+        ++nv;
+        if (++vs == C::kVBuf) { vs = 0; ++vn; }
       }
-      for (int jj = (j > 2 ? j - 2 : 0); jj < j; ++jj)
-        mbar_wait(bar(C::bFull + (jj & 1)), (uint32_t)(jj >> 1) & 1, never, kTimeoutNs);
+      // every issued copy lands before the CTA leaves (the last use of each slot)
+      for (int jj = (nk > C::kKBuf ? nk - C::kKBuf : 0); jj < nk; ++jj)
+        mbar_wait(bar(C::bKFull + jj % C::kKBuf), (uint32_t)(jj / C::kKBuf) & 1, never,
+                  kTimeoutNs);
+      for (int jj = (nv > C::kVBuf ? nv - C::kVBuf : 0); jj < nv; ++jj)
+        mbar_wait(bar(C::bVFull + jj % C::kVBuf), (uint32_t)(jj / C::kVBuf) & 1, never,
+                  kTimeoutNs);
       mbar_wait(bar(C::bFix), 0, never, kTimeoutNs);
     }
     __syncwarp();
@@ -610,9 +682,25 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
       constexpr uint32_t id_acc = idesc_bf16_f32(128, D, true);
       const uint64_t q_kmaj = sw128_desc(base + C::kFixA, 16, 1024);
       const uint64_t do_kmaj = sw128_desc(base + C::kFixB, 16, 1024);
-      const uint64_t k_kmaj = sw128_desc(base + C::kStage0, 16, 1024);
-      const uint64_t v_kmaj = sw128_desc(base + C::kStage0 + C::kTileBytes, 16, 1024);
-      const uint64_t k_mn = sw128_desc(base + C::kStage0, kBoxBytes, 1024);
+      const uint64_t k_kmaj = sw128_desc(base + C::kK0, 16, 1024);
+      const uint64_t v_kmaj = sw128_desc(base + C::kV0, 16, 1024);
+      const uint64_t k_mn = sw128_desc(base + C::kK0, kBoxBytes, 1024);
+      constexpr uint64_t kSlot = (uint64_t)(C::kTileBytes >> 4);   // one slot, in 16-byte units
+      auto issue_s = [&](int slot) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + kColS, q_kmaj + kstep_off(kk), k_kmaj + slot * kSlot + kstep_off(kk),
+                  id_s, kk > 0 ? 1u : 0u);
+        umma_commit(bar(C::bS));
+      };
+      auto issue_dp = [&](int slot) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + kColDP, do_kmaj + kstep_off(kk), v_kmaj + slot * kSlot + kstep_off(kk),
+                  id_s, kk > 0 ? 1u : 0u);
+        umma_commit(bar(C::bDP));
+        umma_commit(bar(C::bVFree + slot));         // V_j is read by dP(j) only
+      };
       bool ok = mbar_wait(bar(C::bFix), 0, abort_flag, kTimeoutNs);
       KvIter it;
       it.init(g, r, q_lo, q_valid);
@@ -620,59 +708,53 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
       bool have = ok && it.next(g, kv);
       // S(0), dP(0)
       if (have) {
-        ok = mbar_wait(bar(C::bFull + 0), 0, abort_flag, kTimeoutNs);
+        ok = mbar_wait(bar(C::bKFull), 0, abort_flag, kTimeoutNs);
         if (ok) {
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + kColS, q_kmaj + kstep_off(kk), k_kmaj + kstep_off(kk), id_s,
-                    kk > 0 ? 1u : 0u);
-          umma_commit(bar(C::bS));
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + kColDP, do_kmaj + kstep_off(kk), v_kmaj + kstep_off(kk), id_s,
-                    kk > 0 ? 1u : 0u);
-          umma_commit(bar(C::bDP));
+          issue_s(0);
+          ok = mbar_wait(bar(C::bVFull), 0, abort_flag, kTimeoutNs);
+          if (ok) {
+            tc_fence_after();
+            issue_dp(0);
+          }
         }
       }
-      // Per visit: S(j+1) once pass 1 has read S(j); dQ(j) once pass 2 has
-      // written dS(j) (into a buffer of its own, alternating); dP(j+1) once
-      // pass 2 has read dP(j). No product waits for another to finish.
+      // Per visit: S(j+1) once pass 1 has read S(j); then, once pass 2 has
+      // read dP(j) and written dS(j) (into a buffer of its own, alternating),
+      // dP(j+1) -- which pass 2 of the next visit waits for -- and dQ(j).
+      // No product waits for another to finish.
+      int ks = 0, kn = 0, vs = 0, vn = 0;   // slots of K(j) and V(j), and their use counts
       int j = 0;
       while (ok && have) {
-        const int st = j & 1;
-        const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
         have = it.next(g, kv);
-        const int sn = (j + 1) & 1;
-        const uint64_t son = (uint64_t)((sn * C::kStageBytes) >> 4);
+        int ks1 = ks + 1, kn1 = kn, vs1 = vs + 1, vn1 = vn;
+        if (ks1 == C::kKBuf) { ks1 = 0; ++kn1; }
+        if (vs1 == C::kVBuf) { vs1 = 0; ++vn1; }
         if (have) {
-          ok = mbar_wait(bar(C::bFull + sn), (uint32_t)((j + 1) >> 1) & 1, abort_flag, kTimeoutNs) &&
+          ok = mbar_wait(bar(C::bKFull + ks1), (uint32_t)kn1 & 1, abort_flag, kTimeoutNs) &&
                mbar_wait(bar(C::bP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
           if (!ok) break;
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + kColS, q_kmaj + kstep_off(kk), k_kmaj + son + kstep_off(kk), id_s,
-                    kk > 0 ? 1u : 0u);
-          umma_commit(bar(C::bS));
+          issue_s(ks1);
         }
         ok = mbar_wait(bar(C::bDS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
+        if (have) {
+          ok = mbar_wait(bar(C::bVFull + vs1), (uint32_t)vn1 & 1, abort_flag, kTimeoutNs);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(vs1);
+        }
         tc_fence_after();
-        const uint32_t ds_col = kColDSq<D>() + (uint32_t)(st * 64);
+        const uint32_t ds_col = kColDSq<D>() + (uint32_t)((j & 1) * 64);
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
-          umma_ts(tmem + kColAcc, tmem + ds_col + dscol(kk), k_mn + so + (uint64_t)(kk * 2048 >> 4),
-                  id_acc, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(C::bAccB + st));
-        umma_commit(bar(C::bFree + st));
-        if (have) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + kColDP, do_kmaj + kstep_off(kk), v_kmaj + son + kstep_off(kk), id_s,
-                    kk > 0 ? 1u : 0u);
-          umma_commit(bar(C::bDP));
-        }
+          umma_ts(tmem + kColAcc, tmem + ds_col + dscol(kk),
+                  k_mn + ks * kSlot + (uint64_t)(kk * 2048 >> 4), id_acc,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(C::bAccB + (j & 1)));
+        umma_commit(bar(C::bKFree + ks));          // K_j's last reader is dQ(j)
+        ks = ks1; kn = kn1; vs = vs1; vn = vn1;
         ++j;
       }
       umma_commit(bar(C::bFinal));
@@ -827,10 +909,11 @@ ra_status launch_d(const Geometry& g, const CUtensorMap& mq, const CUtensorMap& 
     if (cudaGetLastError() != cudaSuccess) return RA_ERR_LAUNCH;
   }
   if (phases & RA_BWD_DQ) {
+    using CQ = CfgQ<D>;
     if (cudaFuncSetAttribute(bwd_dq_kernel<D, kVarlen>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
+                             CQ::kSmemBytes) != cudaSuccess)
       return RA_ERR_LAUNCH;
-    bwd_dq_kernel<D, kVarlen><<<(unsigned)grid_q, kThreads, C::kSmemBytes, stream>>>(
+    bwd_dq_kernel<D, kVarlen><<<(unsigned)grid_q, kThreads, CQ::kSmemBytes, stream>>>(
         mq, mk, mv, mdo, g, lse2, delta, static_cast<__nv_bfloat16*>(dq), status);
     if (cudaGetLastError() != cudaSuccess) return RA_ERR_LAUNCH;
   }
