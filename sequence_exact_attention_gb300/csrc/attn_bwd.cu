@@ -175,6 +175,16 @@ __device__ __forceinline__ void init_barriers(BarFn bar, volatile int* abort_fla
   }
 }
 
+// True in one lane of a converged warp (the same lane every time the whole
+// warp executes it).
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
@@ -677,7 +687,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    if (lane == 0) {
+    // The whole warp runs the issuer's loop, so its descriptor arithmetic is
+    // warp-uniform; one elected lane issues every MMA and commit (a commit
+    // tracks the MMAs of the thread that issues it).
+    {
+      const bool leader = elect_one_sync();
       constexpr uint32_t id_s = idesc_bf16_f32(128, kT, false);
       constexpr uint32_t id_acc = idesc_bf16_f32(128, D, true);
       const uint64_t q_kmaj = sw128_desc(base + C::kFixA, 16, 1024);
@@ -687,32 +701,40 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
       const uint64_t k_mn = sw128_desc(base + C::kK0, kBoxBytes, 1024);
       constexpr uint64_t kSlot = (uint64_t)(C::kTileBytes >> 4);   // one slot, in 16-byte units
       auto issue_s = [&](int slot) {
+        const uint64_t kb = k_kmaj + slot * kSlot;
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColS, q_kmaj + kstep_off(kk), k_kmaj + slot * kSlot + kstep_off(kk),
-                  id_s, kk > 0 ? 1u : 0u);
-        umma_commit(bar(C::bS));
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + kColS, q_kmaj + kstep_off(kk), kb + kstep_off(kk), id_s,
+                    kk > 0 ? 1u : 0u);
+          umma_commit(bar(C::bS));
+        }
+        __syncwarp();
       };
       auto issue_dp = [&](int slot) {
+        const uint64_t vb = v_kmaj + slot * kSlot;
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColDP, do_kmaj + kstep_off(kk), v_kmaj + slot * kSlot + kstep_off(kk),
-                  id_s, kk > 0 ? 1u : 0u);
-        umma_commit(bar(C::bDP));
-        umma_commit(bar(C::bVFree + slot));         // V_j is read by dP(j) only
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + kColDP, do_kmaj + kstep_off(kk), vb + kstep_off(kk), id_s,
+                    kk > 0 ? 1u : 0u);
+          umma_commit(bar(C::bDP));
+          umma_commit(bar(C::bVFree + slot));       // V_j is read by dP(j) only
+        }
+        __syncwarp();
       };
-      bool ok = mbar_wait(bar(C::bFix), 0, abort_flag, kTimeoutNs);
+      bool ok = mbar_wait_warp(bar(C::bFix), 0, abort_flag, kTimeoutNs);
       KvIter it;
       it.init(g, r, q_lo, q_valid);
       KvTile kv;
       bool have = ok && it.next(g, kv);
       // S(0), dP(0)
       if (have) {
-        ok = mbar_wait(bar(C::bKFull), 0, abort_flag, kTimeoutNs);
+        ok = mbar_wait_warp(bar(C::bKFull), 0, abort_flag, kTimeoutNs);
         if (ok) {
           tc_fence_after();
           issue_s(0);
-          ok = mbar_wait(bar(C::bVFull), 0, abort_flag, kTimeoutNs);
+          ok = mbar_wait_warp(bar(C::bVFull), 0, abort_flag, kTimeoutNs);
           if (ok) {
             tc_fence_after();
             issue_dp(0);
@@ -731,34 +753,39 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (ks1 == C::kKBuf) { ks1 = 0; ++kn1; }
         if (vs1 == C::kVBuf) { vs1 = 0; ++vn1; }
         if (have) {
-          ok = mbar_wait(bar(C::bKFull + ks1), (uint32_t)kn1 & 1, abort_flag, kTimeoutNs) &&
-               mbar_wait(bar(C::bP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+          ok = mbar_wait_warp(bar(C::bKFull + ks1), (uint32_t)kn1 & 1, abort_flag, kTimeoutNs) &&
+               mbar_wait_warp(bar(C::bP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
           if (!ok) break;
           tc_fence_after();
           issue_s(ks1);
         }
-        ok = mbar_wait(bar(C::bDS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+        ok = mbar_wait_warp(bar(C::bDS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         if (have) {
-          ok = mbar_wait(bar(C::bVFull + vs1), (uint32_t)vn1 & 1, abort_flag, kTimeoutNs);
+          ok = mbar_wait_warp(bar(C::bVFull + vs1), (uint32_t)vn1 & 1, abort_flag, kTimeoutNs);
           if (!ok) break;
           tc_fence_after();
           issue_dp(vs1);
         }
         tc_fence_after();
         const uint32_t ds_col = kColDSq<D>() + (uint32_t)((j & 1) * 64);
+        const uint64_t kb = k_mn + ks * kSlot;
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          umma_ts(tmem + kColAcc, tmem + ds_col + dscol(kk),
-                  k_mn + ks * kSlot + (uint64_t)(kk * 2048 >> 4), id_acc,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(C::bAccB + (j & 1)));
-        umma_commit(bar(C::bKFree + ks));          // K_j's last reader is dQ(j)
+          for (int kk = 0; kk < kT / 16; ++kk)
+            umma_ts(tmem + kColAcc, tmem + ds_col + dscol(kk), kb + (uint64_t)(kk * 2048 >> 4),
+                    id_acc, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar(C::bAccB + (j & 1)));
+          umma_commit(bar(C::bKFree + ks));        // K_j's last reader is dQ(j)
+        }
+        __syncwarp();
         ks = ks1; kn = kn1; vs = vs1; vn = vn1;
         ++j;
       }
-      umma_commit(bar(C::bFinal));
-      mbar_wait(bar(C::bFinal), 0, never, kTimeoutNs);
+      if (leader) {
+        umma_commit(bar(C::bFinal));
+        mbar_wait(bar(C::bFinal), 0, never, kTimeoutNs);
+      }
     }
     __syncwarp();
   } else {
