@@ -175,16 +175,6 @@ __device__ __forceinline__ void init_barriers(BarFn bar, volatile int* abort_fla
   }
 }
 
-// True in one lane of a converged warp (the same lane every time the whole
-// warp executes it).
-__device__ __forceinline__ bool elect_one_sync() {
-  uint32_t pred;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(pred));
-  return pred != 0;
-}
-
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
@@ -363,7 +353,11 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    if (lane == 0) {
+    // The whole warp runs the issuer's loop, so its descriptor arithmetic is
+    // warp-uniform; one elected lane issues every MMA and commit (a commit
+    // tracks the MMAs of the thread that issues it).
+    {
+      const bool leader = elect_one_sync();
       constexpr uint32_t id_s = idesc_bf16_f32(128, kT, false);
       constexpr uint32_t id_acc = idesc_bf16_f32(128, D, true);
       const uint64_t k_kmaj = sw128_desc(base + C::kFixA, 16, 1024);
@@ -372,7 +366,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
       const uint64_t do_kmaj = sw128_desc(base + C::kStage0 + C::kTileBytes, 16, 1024);
       const uint64_t q_mn = sw128_desc(base + C::kStage0, kBoxBytes, 1024);
       const uint64_t do_mn = sw128_desc(base + C::kStage0 + C::kTileBytes, kBoxBytes, 1024);
-      bool ok = mbar_wait(bar(C::bFix), 0, abort_flag, kTimeoutNs);
+      bool ok = mbar_wait_warp(bar(C::bFix), 0, abort_flag, kTimeoutNs);
       QIter it;
       it.init(g, src, kv_lo, kv_valid, h0, h0 + grp);
       QTile qt;
@@ -380,23 +374,26 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
       // columns), before dK(j): the next P^T pass then overlaps dK(j) and
       // dP^T(j+1).
       auto issue_s = [&](int jj) {
-        const uint64_t so = (uint64_t)(((jj & 1) * C::kStageBytes) >> 4);
+        const uint64_t qb = q_kmaj + (uint64_t)(((jj & 1) * C::kStageBytes) >> 4);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColS, k_kmaj + kstep_off(kk), q_kmaj + so + kstep_off(kk), id_s,
-                  kk > 0 ? 1u : 0u);
-        umma_commit(bar(C::bS));
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + kColS, k_kmaj + kstep_off(kk), qb + kstep_off(kk), id_s,
+                    kk > 0 ? 1u : 0u);
+          umma_commit(bar(C::bS));
+        }
+        __syncwarp();
       };
       bool have = ok && it.next(g, qt);
       if (have) {
-        ok = mbar_wait(bar(C::bFull + 0), 0, abort_flag, kTimeoutNs);
+        ok = mbar_wait_warp(bar(C::bFull + 0), 0, abort_flag, kTimeoutNs);
         if (ok) {
           tc_fence_after();
           issue_s(0);
         }
       }
       // dP^T(j) overwrites the dS^T(j-1) that dK(j-1) reads, and S^T(j+1)
-      // the P^T(j) that dV(j) reads: this thread issues both pairs in that
+      // the P^T(j) that dV(j) reads: one thread issues both pairs in that
       // order and the tensor core executes one thread's MMAs in issue order,
       // so neither waits for the other to complete (a wait would drain the
       // tensor core: it holds only the few MMAs queued behind the last issue).
@@ -404,39 +401,51 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
       while (ok && have) {
         const int st = j & 1;
         const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
+        const uint64_t dob = do_kmaj + so, domn = do_mn + so, qmn = q_mn + so;
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + kColDP, v_kmaj + kstep_off(kk), do_kmaj + so + kstep_off(kk), id_s,
-                  kk > 0 ? 1u : 0u);
-        umma_commit(bar(C::bDP));
-        ok = mbar_wait(bar(C::bP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + kColDP, v_kmaj + kstep_off(kk), dob + kstep_off(kk), id_s,
+                    kk > 0 ? 1u : 0u);
+          umma_commit(bar(C::bDP));
+        }
+        __syncwarp();
+        ok = mbar_wait_warp(bar(C::bP), (uint32_t)j & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          umma_ts(tmem + kColAcc, tmem + kColS + pcol(kk), do_mn + so + (uint64_t)(kk * 2048 >> 4),
-                  id_acc, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kT / 16; ++kk)
+            umma_ts(tmem + kColAcc, tmem + kColS + pcol(kk), domn + (uint64_t)(kk * 2048 >> 4),
+                    id_acc, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        __syncwarp();
         have = it.next(g, qt);
         if (have) {
-          ok = mbar_wait(bar(C::bFull + ((j + 1) & 1)), (uint32_t)((j + 1) >> 1) & 1, abort_flag,
-                         kTimeoutNs);
+          ok = mbar_wait_warp(bar(C::bFull + ((j + 1) & 1)), (uint32_t)((j + 1) >> 1) & 1,
+                              abort_flag, kTimeoutNs);
           if (!ok) break;
           tc_fence_after();
           issue_s(j + 1);
         }
-        ok = mbar_wait(bar(C::bDS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+        ok = mbar_wait_warp(bar(C::bDS), (uint32_t)j & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          umma_ts(tmem + kColAcc + D, tmem + kColDP + pcol(kk),
-                  q_mn + so + (uint64_t)(kk * 2048 >> 4), id_acc, (j > 0 || kk > 0) ? 1u : 0u);
-        if (!have) umma_commit(bar(C::bAccK));        // the accumulators are final
-        umma_commit(bar(C::bFree + st));
+          for (int kk = 0; kk < kT / 16; ++kk)
+            umma_ts(tmem + kColAcc + D, tmem + kColDP + pcol(kk), qmn + (uint64_t)(kk * 2048 >> 4),
+                    id_acc, (j > 0 || kk > 0) ? 1u : 0u);
+          if (!have) umma_commit(bar(C::bAccK));        // the accumulators are final
+          umma_commit(bar(C::bFree + st));
+        }
+        __syncwarp();
         ++j;
       }
-      umma_commit(bar(C::bFinal));
-      mbar_wait(bar(C::bFinal), 0, never, kTimeoutNs);
+      if (leader) {
+        umma_commit(bar(C::bFinal));
+        mbar_wait(bar(C::bFinal), 0, never, kTimeoutNs);
+      }
     }
     __syncwarp();
   } else {

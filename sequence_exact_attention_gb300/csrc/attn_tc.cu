@@ -496,10 +496,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     // One thread issues every MMA, so each product runs on the tensor core
     // as one uninterrupted group into its accumulator (MMAs of two threads
     // interleaved measured much slower). Per key tile j: PV0(j) S0(j+1)
-    // PV1(j) S1(j+1). Between groups the thread only tests barriers: the
+    // PV1(j) S1(j+1). Between groups the warp only tests barriers: the
     // tensor core runs just the few MMAs queued behind the last issue, so any
-    // longer stop here would leave it idle.
-    if (lane == 0) {
+    // longer stop here would leave it idle. The whole warp runs the loop, so
+    // its descriptor arithmetic is warp-uniform; one elected lane issues the
+    // MMAs and commits (a commit tracks the MMAs of the thread that issues
+    // it).
+    {
+      const bool leader = elect_one_sync();
       // Descriptors differ only in the start-address field (bits 0-13, in
       // 16-byte units, no carry: shared addresses are < 256 KB), so they are
       // built once and offset per K step and slot.
@@ -511,18 +515,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const uint32_t tO0 = tmem + kOCol, tO1 = tmem + kOCol + D;
       // the walk's length, counted while Q lands
       const int n = kv_walk_length(g, r, q_lo, q_valid);
-      bool ok = mbar_wait(bar(C::bQFull), 0, abort_flag, kTimeoutNs) &&
-                (!two || mbar_wait(bar(C::bQFull + 1), 0, abort_flag, kTimeoutNs));
+      bool ok = mbar_wait_warp(bar(C::bQFull), 0, abort_flag, kTimeoutNs) &&
+                (!two || mbar_wait_warp(bar(C::bQFull + 1), 0, abort_flag, kTimeoutNs));
       if (ok && n > 0) {
-        ok = mbar_wait(bar(C::bKFull), 0, abort_flag, kTimeoutNs);
+        ok = mbar_wait_warp(bar(C::bKFull), 0, abort_flag, kTimeoutNs);
         if (ok) {
           tc_fence_after();
-          issue_s<D>(tS0, q_desc, k_desc);
-          umma_commit(bar(C::bSFull));
-          if (two) {
-            issue_s<D>(tS1, q_desc + q1_off, k_desc);
-            umma_commit(bar(C::bSFull + 1));
+          if (leader) {
+            issue_s<D>(tS0, q_desc, k_desc);
+            umma_commit(bar(C::bSFull));
+            if (two) {
+              issue_s<D>(tS1, q_desc + q1_off, k_desc);
+              umma_commit(bar(C::bSFull + 1));
+            }
           }
+          __syncwarp();
         }
       }
       int ks = 0, kn = 0, vs = 0, vn = 0;
@@ -536,41 +543,49 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         // all three at once and wait one by one only when one is missing
         const uint32_t kb = bar(C::bKFull + (last ? ks : nks));
         const uint32_t kp = last ? (uint32_t)kn & 1 : (uint32_t)nkn & 1;
-        if (!mbar_test3(bar(C::bVFull + vs), (uint32_t)vn & 1, kb, kp, bar(C::bPFull),
-                        (uint32_t)j & 1))
-          ok = mbar_wait(bar(C::bVFull + vs), (uint32_t)vn & 1, abort_flag, kTimeoutNs) &&
-               mbar_wait(kb, kp, abort_flag, kTimeoutNs) &&
-               mbar_wait(bar(C::bPFull), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+        if (!__all_sync(0xffffffffu, mbar_test3(bar(C::bVFull + vs), (uint32_t)vn & 1, kb, kp,
+                                                bar(C::bPFull), (uint32_t)j & 1)))
+          ok = mbar_wait_warp(bar(C::bVFull + vs), (uint32_t)vn & 1, abort_flag, kTimeoutNs) &&
+               mbar_wait_warp(kb, kp, abort_flag, kTimeoutNs) &&
+               mbar_wait_warp(bar(C::bPFull), (uint32_t)j & 1, abort_flag, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
         // PV0(j), then S0(j+1) over the same columns
-        issue_pv<D>(tO0, tS0, vd, j > 0);
-        if (last) {
-          umma_commit(bar(C::bODone));
-        } else {
-          issue_s<D>(tS0, q_desc, kd);
-          umma_commit(bar(C::bSFull));
+        if (leader) {
+          issue_pv<D>(tO0, tS0, vd, j > 0);
+          if (last) {
+            umma_commit(bar(C::bODone));
+          } else {
+            issue_s<D>(tS0, q_desc, kd);
+            umma_commit(bar(C::bSFull));
+          }
         }
+        __syncwarp();
         // PV1(j), then S1(j+1)
         if (two) {
-          ok = mbar_wait(bar(C::bPFull + 1), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+          ok = mbar_wait_warp(bar(C::bPFull + 1), (uint32_t)j & 1, abort_flag, kTimeoutNs);
           if (!ok) break;
           tc_fence_after();
-          issue_pv<D>(tO1, tS1, vd, j > 0);
-          if (last) {
-            umma_commit(bar(C::bODone + 1));
-          } else {
-            issue_s<D>(tS1, q_desc + q1_off, kd);
-            umma_commit(bar(C::bSFull + 1));
+          if (leader) {
+            issue_pv<D>(tO1, tS1, vd, j > 0);
+            if (last) {
+              umma_commit(bar(C::bODone + 1));
+            } else {
+              issue_s<D>(tS1, q_desc + q1_off, kd);
+              umma_commit(bar(C::bSFull + 1));
+            }
           }
+          __syncwarp();
         }
         ks = nks;
         kn = nkn;
         if (++vs == C::kVBuf) { vs = 0; ++vn; }
       }
-      // all tensor-core work this thread issued has completed before teardown
-      umma_commit(bar(C::bFinal));
-      mbar_wait(bar(C::bFinal), 0, never, kTimeoutNs);
+      // all tensor-core work this warp issued has completed before teardown
+      if (leader) {
+        umma_commit(bar(C::bFinal));
+        mbar_wait(bar(C::bFinal), 0, never, kTimeoutNs);
+      }
     }
     __syncwarp();
   } else if (warp < kSoftmaxWarps) {
