@@ -18,15 +18,19 @@
 // serves two query tiles; the one key tile of the walk that lies wholly after
 // Q0 (the diagonal tile of Q1) reaches Q0 fully masked and adds nothing to it.
 // "Receiving" a block is a TMA load of its tiles from this GPU's HBM/L2 into
-// shared memory. Warp roles (320 threads):
-//   warps 0-7  softmax, two threads per query row (row = TMEM lane), 64 key
-//              columns each, for Q0 and then Q1 at every key tile (one warp
-//              holding a row's 128 scores loads them from TMEM far more slowly
-//              than two warps holding 64 each)
-//   warp  8    TMA producer: Q0 and Q1 once, then K_j and V_j into slot rings
-//   warp  9    TMEM allocator; one thread issues every MMA
+// shared memory. Warp roles (320 threads at D = 128, 576 at D = 64):
+//   softmax    two threads per query row (row = TMEM lane), 64 key columns
+//              each (one warp holding a row's 128 scores loads them from TMEM
+//              far more slowly than two warps holding 64 each). D = 128:
+//              warps 0-7, for Q0 and then Q1 at every key tile. D = 64:
+//              warps 0-7 for Q0 and 8-15 for Q1, side by side.
+//   producer   (the next warp) TMA: Q0 and Q1 once, then K_j and V_j into
+//              slot rings
+//   issuer     (the last warp) TMEM allocator; one elected lane issues every
+//              MMA
 // Tensor memory (512 columns): S_i (128 f32 columns) at i * 128, softmax writes
-// P_i as bf16 over the first 64 of them; O_i (D columns) at 256 + i * D.
+// P_i as bf16 over the first 64 of them (D = 128) or over the first 32 of
+// each part's 64 (D = 64); O_i (D columns) at 256 + i * D.
 //
 // The two query tiles give the SM two chains
 //     S_i(j) -> softmax_i(j) -> PV_i(j) -> S_i(j+1) -> ...
@@ -82,10 +86,21 @@ using namespace fastmath;
 
 constexpr int kTile = 128;                 // rows of a query tile and of a key tile
 constexpr int kBlockRows = 2 * kTile;      // query rows per CTA
-constexpr int kSoftmaxWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;                // also allocates / frees TMEM
-constexpr int kThreads = 320;
+// Warp roles by head size. D = 128: eight softmax warps run the softmax of
+// Q0 and then of Q1 at every key tile (320 threads). D = 64, whose products
+// take half as long: sixteen softmax warps, eight per query tile, run the two
+// tiles' softmax side by side (576 threads; five warps share two of the
+// sub-partitions, which caps a thread at 96 registers, so a softmax thread
+// holds 32 scores at a time and reads each chunk from TMEM twice).
+template <int D>
+struct Roles {
+  static constexpr bool kSplit = D == 64;
+  static constexpr int kTileWarps = 8;                  // softmax warps on one tile at a time
+  static constexpr int kSoftmaxWarps = kSplit ? 2 * kTileWarps : kTileWarps;
+  static constexpr int kProducerWarp = kSoftmaxWarps;
+  static constexpr int kMmaWarp = kSoftmaxWarps + 1;    // also allocates / frees TMEM
+  static constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;            // O_i at kOCol + i * D
 constexpr float kRescaleLog2 = 8.0f;       // lazy rescale threshold (x256)
@@ -104,7 +119,8 @@ struct Cfg {
   static constexpr int kBarOff = kVOff + kVBuf * kTileBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kRedOff = kBarOff + kBarBytes;        // softmax exchange
-  static constexpr int kRedBytes = (512 + 512) * 4;          // maxima [2][2][128], sums [2][2][128]
+  // maxima [2 parities][2 tiles][2 parts][128 rows], sums [2 tiles][2 parts][128 rows]
+  static constexpr int kRedBytes = (1024 + 512) * 4;
   static constexpr int kUsed = kRedOff + kRedBytes + 1024;   // + alignment slack
   // More than half an SM's shared memory: one CTA per SM, so the 512-column
   // TMEM allocation never waits for another CTA.
@@ -117,7 +133,7 @@ struct Cfg {
   static constexpr int bSFull = bDone + kKBuf;      // [2]
   static constexpr int bPFull = bSFull + 2;         // [2], 128 arrivals
   static constexpr int bODone = bPFull + 2;         // [2]
-  static constexpr int bStaged = bODone + 2;        // [2] output tile i staged (8 warps)
+  static constexpr int bStaged = bODone + 2;        // [2] output tile i staged (8 warps, D = 128)
   static constexpr int bFinal = bStaged + 2;
   static constexpr int kNumBars = bFinal + 1;
   static constexpr int kHolderOff = kBarBytes - 16;   // TMEM base address
@@ -280,19 +296,21 @@ __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t q_desc, uint64
 }
 
 // O_i (+)= P_i V: A = P_i (bf16, TMEM), B = V (MN-major), M = 128, N = D,
-// K = 128 keys in steps of 16 (8 TMEM columns of bf16 pairs each).
-template <int D>
+// K = 128 keys in steps of 16 (8 TMEM columns of bf16 pairs each). P_i lies
+// in the first 64 columns of S_i, or (kOwnCols) in the first 32 of each
+// part's 64.
+template <int D, bool kOwnCols>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, D, true);
 #pragma unroll
   for (int kk = 0; kk < kTile / 16; ++kk)
-    umma_ts(o_tmem, p_tmem + kk * 8, v_desc + (uint64_t)((kk * 2048) >> 4), idesc,
-            (accumulate || kk > 0) ? 1u : 0u);
+    umma_ts(o_tmem, p_tmem + (kOwnCols ? (kk / 4) * 64 + (kk % 4) * 8 : kk * 8),
+            v_desc + (uint64_t)((kk * 2048) >> 4), idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 template <int D, bool kOutF32, bool kVarlen, bool kWithholdV0>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<D>::kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v,
@@ -301,6 +319,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                int* __restrict__ vlog, int log_stride, int* __restrict__ status,
                int tma_out) {
   using C = Cfg<D>;
+  using R = Roles<D>;
   // Full bf16 output tiles go out through TMA stores at D = 128 (a row part
   // is 128 bytes); at D = 64 the per-row stores measured faster.
   constexpr bool kTmaOut = !kOutF32 && D == 128;
@@ -389,9 +408,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(C::bQFull + i), 1);
       mbar_init(bar(C::bSFull + i), 1);
-      mbar_init(bar(C::bPFull + i), 32 * kSoftmaxWarps);
+      mbar_init(bar(C::bPFull + i), 32 * R::kTileWarps);
       mbar_init(bar(C::bODone + i), 1);
-      if (kTmaOut) mbar_init(bar(C::bStaged + i), kSoftmaxWarps);
+      if (kTmaOut) mbar_init(bar(C::bStaged + i), R::kSoftmaxWarps);
     }
     for (int i = 0; i < C::kKBuf; ++i) {
       mbar_init(bar(C::bKFull + i), 1);
@@ -403,7 +422,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     *never = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == R::kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
   }
@@ -411,7 +430,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  if (warp == kProducerWarp) {
+  if (warp == R::kProducerWarp) {
     // ======================= TMA producer =======================
     if (lane == 0) {
       for (int i = 0; i < (two ? 2 : 1); ++i) {
@@ -491,7 +510,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+  } else if (warp == R::kMmaWarp) {
     // ======================= MMA issuer =======================
     // One thread issues every MMA, so each product runs on the tensor core
     // as one uninterrupted group into its accumulator (MMAs of two threads
@@ -552,7 +571,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc_fence_after();
         // PV0(j), then S0(j+1) over the same columns
         if (leader) {
-          issue_pv<D>(tO0, tS0, vd, j > 0);
+          issue_pv<D, R::kSplit>(tO0, tS0, vd, j > 0);
           if (last) {
             umma_commit(bar(C::bODone));
           } else {
@@ -567,7 +586,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           if (!ok) break;
           tc_fence_after();
           if (leader) {
-            issue_pv<D>(tO1, tS1, vd, j > 0);
+            issue_pv<D, R::kSplit>(tO1, tS1, vd, j > 0);
             if (last) {
               umma_commit(bar(C::bODone + 1));
             } else {
@@ -588,175 +607,333 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
     }
     __syncwarp();
-  } else if (warp < kSoftmaxWarps) {
-    // ============ softmax: two threads per query row, Q0 and Q1 in turn ============
-    // Warps w and w+4 share TMEM lane quarter w % 4 (the same 32 rows of each
-    // query tile); part p = w / 4 takes key columns [64p, 64p+64) of S_i and
-    // O columns [pD/2, (p+1)D/2). Per key tile the eight warps run softmax of
-    // Q0, then of Q1. A row's two partial maxima meet in shared memory at one
-    // named barrier of the pair (which also orders both parts' S loads before
-    // either part writes P over the first 64 S columns); each part keeps its
-    // own partial sums, added in the epilogue.
-    const int wq = warp & 3;                   // TMEM lane quarter
-    const int part = warp >> 2;                // column part
-    const int row = wq * 32 + lane;
-    const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
-    const int ntile = two ? 2 : 1;
-    const float sl2 = g.scale_log2;
-    const uint64_t sl2x2 = pack2(sl2, sl2);
-    const uint32_t pair_bar = 1 + wq;          // named barrier of the row's two warps
-    // [2 exchange parities][2 parts][128 rows] partial maxima, then
-    // [2 tiles][2 parts][128 rows] partial sums
-    float* red = reinterpret_cast<float*>(base_ptr + C::kRedOff);
-    int ex = 0;                                // exchanges so far (buffer parity)
-
-    // one visit record per query tile, written by one thread
-    int* log0 = (vlog && warp == 0 && lane == 0) ? vlog + log_off(0) : nullptr;
-    int* log1 = (log0 && two) ? vlog + log_off(1) : nullptr;
-    int n_log0 = 0, n_log1 = 0;
-
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    int j = 0;               // key tiles done
-    bool ok = true;
-    KvIter it;
-    it.init(g, r, q_lo, q_valid);
-    KvTile kv;
-    bool have = it.next(g, kv);
-    // One thread arrives on done(j) once S(j) of the last tile is done: the
-    // producer's signal that K_j's and V_{j-1}'s slots may be refilled.
-    const bool relay = warp == 0 && lane == 0;
-    int rd = 0;
-    while (have) {
-      if (log0) {
-        // a key tile wholly after query tile i is not part of its own walk
-        // (it reaches the tile fully masked)
-        if (!(g.causal && kv.lo > q_lo + min(kTile, q_valid) - 1) &&
-            in_range(log_off(0) + 1 + 4 * n_log0, 4, log_len, status))
-          log_visit(log0, n_log0++, kv, tile_class(g, q_lo, kv));
-        if (log1 && !(g.causal && kv.lo > q_lo + q_valid - 1) &&
-            in_range(log_off(1) + 1 + 4 * n_log1, 4, log_len, status))
-          log_visit(log1, n_log1++, kv, tile_class(g, q_lo + kTile, kv));
-      }
-#pragma unroll
-      for (int qi = 0; qi < 2; ++qi) {
-        if (qi >= ntile) break;
-        const uint32_t tS = tmem + t_lane + (uint32_t)(qi * kTile);
-        const int qt_lo = q_lo + qi * kTile;
-        const int q_pos = qt_lo + row;
-        float* red_e = red + (ex & 1) * 256;
-        ++ex;
-        if (ok) ok = mbar_wait_warp(bar(C::bSFull + qi), (uint32_t)j & 1, abort_flag, kTimeoutNs);
-        if (!ok) {
-          // keep meeting the partner at every exchange so it never waits alone
-          named_bar_sync(pair_bar, 64);
-          continue;
-        }
-        tc_fence_after();
-        uint32_t uu[2][32];
-        tmem_ld32(tS + part * 64, uu[0]);
-        tmem_ld32(tS + part * 64 + 32, uu[1]);
-        if (relay && qi == ntile - 1) {
-          mbar_arrive(bar(C::bDone + rd));
-          if (++rd == C::kKBuf) rd = 0;
-        }
-        tmem_ld_wait();
-        reg_fence(uu[0]);
-        reg_fence(uu[1]);
-        // tiles the causal rule cuts for this query tile, and ragged tails
-        const bool all_allowed = !g.causal || kv.lo + kv.valid - 1 <= qt_lo;
-        if (!(all_allowed && kv.valid == kTile)) {
-          const int lim = (g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid) - part * 64;
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c >= lim) uu[c / 32][c % 32] = __float_as_uint(-INFINITY);
-        }
-        float m8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
-        max_chunk(uu[0], m8);
-        max_chunk(uu[1], m8);
-        red_e[part * 128 + row] = max8(m8);
-        tc_fence_before();
-        named_bar_sync(pair_bar, 64);
-        tc_fence_after();
-        const float mx = fmaxf(red_e[row], red_e[128 + row]);
-        const float m_new = fmaxf(m_run[qi], mx * sl2);
-        const bool resc = m_new > m_run[qi] + kRescaleLog2;
-        float alpha = 1.f;
-        if (resc) {
-          alpha = ex2_approx(m_run[qi] - m_new);     // 0 when m_run = -inf
-          m_run[qi] = m_new;
-          l_run[qi] *= alpha;
-        }
-        const float m_use = (m_run[qi] == -INFINITY) ? 0.f : m_run[qi];
-        const uint64_t neg_m2 = pack2(-m_use, -m_use);
-        uint64_t sum2a = pack2(0.f, 0.f), sum2b = sum2a;
-        // P of this part's 64 keys: TMEM columns 32p..32p+31 of S_i
-        exp_chunk(uu[0], sl2x2, neg_m2, sum2a, sum2b, tS + part * 32);
-        exp_chunk(uu[1], sl2x2, neg_m2, sum2a, sum2b, tS + part * 32 + 16);
-        {
-          float a0, a1;
-          unpack2(fadd2(sum2a, sum2b), a0, a1);
-          l_run[qi] += a0 + a1;
-        }
-        // O_i is scaled by alpha before P_i(j) V_j is added to it; PV_i(j-1)
-        // is done (S_i(j)'s completion covers it). Both parts take the same
-        // decision for a row.
-        if (__any_sync(0xffffffffu, resc) && j > 0)
-          scale_cols<D / 2>(tmem + t_lane + kOCol + (uint32_t)(qi * D + part * (D / 2)), alpha);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(C::bPFull + qi));
-      }
-      ++j;
-      have = it.next(g, kv);
-    }
-    if (log0 && in_range(log_off(0), 1, log_len, status)) log0[0] = n_log0;
-    if (log1 && in_range(log_off(1), 1, log_len, status)) log1[0] = n_log1;
-    // a second query tile of padding only has an empty record
-    if (log0 && !two && tile1_exists && in_range(log_off(1), 1, log_len, status))
-      vlog[log_off(1)] = 0;
-
-    // ---- epilogue: out = O / l, lse = ln2 * (m + log2 l), l = sum of both parts
-    float* red_l = red + 512;
-    for (int qi = 0; qi < ntile; ++qi) red_l[(qi * 2 + part) * 128 + row] = l_run[qi];
-    named_bar_sync(pair_bar, 64);
-    for (int qi = 0; qi < ntile; ++qi) {
-      const float l_tot = red_l[qi * 256 + row] + red_l[qi * 256 + 128 + row];
+  } else if (warp < R::kSoftmaxWarps) {
+    if constexpr (R::kSplit) {
+      // ============ softmax: warps 0-7 serve Q0, warps 8-15 serve Q1 ============
+      // Two threads per query row: warps w and w+4 of a tile share TMEM lane
+      // quarter w % 4 (the same 32 rows); part p takes key columns [64p, 64p+64)
+      // of S_i and O columns [pD/2, (p+1)D/2). The two tiles' softmax warps run
+      // side by side, so one tile's softmax overlaps the other's and the tensor
+      // core's PV and S of the other tile. A row's two partial maxima meet in
+      // shared memory at one named barrier of the pair; each part writes its P
+      // into its own 64 columns and keeps its own partial sums, added in the
+      // epilogue.
+      const int qi = warp / R::kTileWarps;          // query tile served
+      const int wq = warp & 3;                   // TMEM lane quarter
+      const int part = (warp >> 2) & 1;          // column part
+      const int row = wq * 32 + lane;
+      const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
+      const float sl2 = g.scale_log2;
+      const uint64_t sl2x2 = pack2(sl2, sl2);
+      const uint32_t pair_bar = 1 + qi * 4 + wq; // named barrier of the row's two warps
+      const uint32_t tS = tmem + t_lane + (uint32_t)(qi * kTile);
+      const uint32_t tOp = tmem + t_lane + kOCol + (uint32_t)(qi * D + part * (D / 2));
       const int qt_lo = q_lo + qi * kTile;
       const int q_pos = qt_lo + row;
-      const bool row_valid = row < min(kTile, q_valid - qi * kTile);
-      if (ok && j > 0) {
-        ok = mbar_wait_warp(bar(C::bODone + qi), 0, abort_flag, kTimeoutNs);
-        tc_fence_after();
+      // [2 exchange parities][2 tiles][2 parts][128 rows] partial maxima, then
+      // [2 tiles][2 parts][128 rows] partial sums
+      float* red = reinterpret_cast<float*>(base_ptr + C::kRedOff);
+      int ex = 0;                                // exchanges so far (buffer parity)
+      float m_run = -INFINITY, l_run = 0.f;
+      int j = 0;                                 // key tiles done
+      bool ok = true;
+      if (qi == 0 || two) {
+        // one visit record per query tile, written by the tile's first thread
+        int* log = (vlog && warp == qi * R::kTileWarps && lane == 0) ? vlog + log_off(qi) : nullptr;
+        int n_log = 0;
+        const int q_last = q_lo + min(kTile * (qi + 1), q_valid) - 1;
+        KvIter it;
+        it.init(g, r, q_lo, q_valid);
+        KvTile kv;
+        bool have = it.next(g, kv);
+        // One thread arrives on done(j) once S(j) of the last tile is done: the
+        // producer's signal that K_j's and V_{j-1}'s slots may be refilled.
+        const bool relay = lane == 0 && warp == (two ? R::kTileWarps : 0);
+        int rd = 0;
+        while (have) {
+          // a key tile wholly after the query tile is not part of its own walk
+          // (it reaches the tile fully masked)
+          if (log && !(g.causal && kv.lo > q_last) &&
+              in_range(log_off(qi) + 1 + 4 * n_log, 4, log_len, status))
+            log_visit(log, n_log++, kv, tile_class(g, qt_lo, kv));
+          float* red_e = red + (ex & 1) * 512 + qi * 256;
+          ++ex;
+          if (ok) ok = mbar_wait_warp(bar(C::bSFull + qi), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+          if (!ok) {
+            // keep meeting the partner at every exchange so it never waits alone
+            named_bar_sync(pair_bar, 64);
+            ++j;
+            have = it.next(g, kv);
+            continue;
+          }
+          tc_fence_after();
+          // tiles the causal rule cuts for this query tile, and ragged tails:
+          // columns from lim on (of this part's 64) are masked
+          const bool all_allowed = !g.causal || kv.lo + kv.valid - 1 <= qt_lo;
+          const bool cut = !(all_allowed && kv.valid == kTile);
+          const int lim = (g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid) - part * 64;
+          float m8[8];
+  #pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
+  #pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t u[32];
+            tmem_ld32(tS + part * 64 + c * 32, u);
+            if (relay && c == 0) {
+              mbar_arrive(bar(C::bDone + rd));
+              if (++rd == C::kKBuf) rd = 0;
+            }
+            tmem_ld_wait();
+            reg_fence(u);
+            if (cut) {
+  #pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (c * 32 + i >= lim) u[i] = __float_as_uint(-INFINITY);
+            }
+            max_chunk(u, m8);
+          }
+          red_e[part * 128 + row] = max8(m8);
+          named_bar_sync(pair_bar, 64);
+          const float mx = fmaxf(red_e[row], red_e[128 + row]);
+          const float m_new = fmaxf(m_run, mx * sl2);
+          const bool resc = m_new > m_run + kRescaleLog2;
+          float alpha = 1.f;
+          if (resc) {
+            alpha = ex2_approx(m_run - m_new);         // 0 when m_run = -inf
+            m_run = m_new;
+            l_run *= alpha;
+          }
+          const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+          const uint64_t neg_m2 = pack2(-m_use, -m_use);
+          uint64_t sum2a = pack2(0.f, 0.f), sum2b = sum2a;
+          // the scores again, 32 at a time; P of chunk c (bf16 pairs) goes to
+          // this part's own columns 64p + 16c .. 64p + 16c + 15, which hold
+          // scores already read
+  #pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t u[32];
+            tmem_ld32(tS + part * 64 + c * 32, u);
+            tmem_ld_wait();
+            reg_fence(u);
+            if (cut) {
+  #pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (c * 32 + i >= lim) u[i] = __float_as_uint(-INFINITY);
+            }
+            exp_chunk(u, sl2x2, neg_m2, sum2a, sum2b, tS + part * 64 + c * 16);
+          }
+          {
+            float a0, a1;
+            unpack2(fadd2(sum2a, sum2b), a0, a1);
+            l_run += a0 + a1;
+          }
+          // O_i is scaled by alpha before P_i(j) V_j is added to it; PV_i(j-1)
+          // is done (S_i(j)'s completion covers it). Both parts take the same
+          // decision for a row.
+          if (__any_sync(0xffffffffu, resc) && j > 0) scale_cols<D / 2>(tOp, alpha);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(C::bPFull + qi));
+          ++j;
+          have = it.next(g, kv);
+        }
+        if (log && in_range(log_off(qi), 1, log_len, status)) log[0] = n_log;
+
+        // ---- epilogue: out = O / l, lse = ln2 * (m + log2 l), l = sum of both parts
+        float* red_l = red + 1024 + qi * 256;
+        red_l[part * 128 + row] = l_run;
+        named_bar_sync(pair_bar, 64);
+        const float l_tot = red_l[row] + red_l[128 + row];
+        const bool row_valid = row < min(kTile, q_valid - qi * kTile);
+        if (ok && j > 0) {
+          ok = mbar_wait_warp(bar(C::bODone + qi), 0, abort_flag, kTimeoutNs);
+          tc_fence_after();
+        }
+        if (ok) {
+          const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+          const size_t row_off = ((orow + q_pos) * g.H_q + h) * D + part * (D / 2);
+          const bool store = row_valid && in_range((long long)row_off, D / 2, extent_q(gp), status);
+          store_out_row<D / 2, kOutF32>(tOp, j > 0, store, out, row_off, inv_l);
+          if (row_valid && lse && part == 0 &&
+              in_range((long long)(lrow + q_pos), 1, extent_lse(gp), status))
+            lse[lrow + q_pos] =
+                l_tot > 0.f ? (m_run + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
+        }
+      } else if (vlog && warp == R::kTileWarps && lane == 0 && tile1_exists &&
+                 in_range(log_off(1), 1, log_len, status)) {
+        // a second query tile of padding only has an empty record
+        vlog[log_off(1)] = 0;
       }
-      if (!ok) break;
-      const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-      const uint32_t tO = tmem + t_lane + kOCol + (uint32_t)(qi * D + part * (D / 2));
-      if (kTmaOut && tma_out && q_valid - qi * kTile >= kTile) {
-        // a full tile: staged in Q_i's buffer (every MMA reading it is done)
-        // and written by one TMA store of whole rows
-        const uint32_t tile_smem = base + C::kQOff + (uint32_t)(qi * C::kTileBytes);
-        stage_out_row<D / 2>(tO, j > 0, tile_smem, row, part * (D / 2), inv_l);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::bStaged + qi));   // the producer stores it
-      } else {
-        const size_t row_off = ((orow + q_pos) * g.H_q + h) * D + part * (D / 2);
-        const bool store = row_valid && in_range((long long)row_off, D / 2, extent_q(gp), status);
-        store_out_row<D / 2, kOutF32>(tO, j > 0, store, out, row_off, inv_l);
+    } else {
+      // ============ softmax: two threads per query row, Q0 and Q1 in turn ============
+      // Warps w and w+4 share TMEM lane quarter w % 4 (the same 32 rows of each
+      // query tile); part p = w / 4 takes key columns [64p, 64p+64) of S_i and
+      // O columns [pD/2, (p+1)D/2). Per key tile the eight warps run softmax of
+      // Q0, then of Q1. A row's two partial maxima meet in shared memory at one
+      // named barrier of the pair (which also orders both parts' S loads before
+      // either part writes P over the first 64 S columns); each part keeps its
+      // own partial sums, added in the epilogue.
+      const int wq = warp & 3;                   // TMEM lane quarter
+      const int part = warp >> 2;                // column part
+      const int row = wq * 32 + lane;
+      const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
+      const int ntile = two ? 2 : 1;
+      const float sl2 = g.scale_log2;
+      const uint64_t sl2x2 = pack2(sl2, sl2);
+      const uint32_t pair_bar = 1 + wq;          // named barrier of the row's two warps
+      // [2 exchange parities][2 parts][128 rows] partial maxima, then
+      // [2 tiles][2 parts][128 rows] partial sums
+      float* red = reinterpret_cast<float*>(base_ptr + C::kRedOff);
+      int ex = 0;                                // exchanges so far (buffer parity)
+
+      // one visit record per query tile, written by one thread
+      int* log0 = (vlog && warp == 0 && lane == 0) ? vlog + log_off(0) : nullptr;
+      int* log1 = (log0 && two) ? vlog + log_off(1) : nullptr;
+      int n_log0 = 0, n_log1 = 0;
+
+      float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+      int j = 0;               // key tiles done
+      bool ok = true;
+      KvIter it;
+      it.init(g, r, q_lo, q_valid);
+      KvTile kv;
+      bool have = it.next(g, kv);
+      // One thread arrives on done(j) once S(j) of the last tile is done: the
+      // producer's signal that K_j's and V_{j-1}'s slots may be refilled.
+      const bool relay = warp == 0 && lane == 0;
+      int rd = 0;
+      while (have) {
+        if (log0) {
+          // a key tile wholly after query tile i is not part of its own walk
+          // (it reaches the tile fully masked)
+          if (!(g.causal && kv.lo > q_lo + min(kTile, q_valid) - 1) &&
+              in_range(log_off(0) + 1 + 4 * n_log0, 4, log_len, status))
+            log_visit(log0, n_log0++, kv, tile_class(g, q_lo, kv));
+          if (log1 && !(g.causal && kv.lo > q_lo + q_valid - 1) &&
+              in_range(log_off(1) + 1 + 4 * n_log1, 4, log_len, status))
+            log_visit(log1, n_log1++, kv, tile_class(g, q_lo + kTile, kv));
+        }
+  #pragma unroll
+        for (int qi = 0; qi < 2; ++qi) {
+          if (qi >= ntile) break;
+          const uint32_t tS = tmem + t_lane + (uint32_t)(qi * kTile);
+          const int qt_lo = q_lo + qi * kTile;
+          const int q_pos = qt_lo + row;
+          float* red_e = red + (ex & 1) * 256;
+          ++ex;
+          if (ok) ok = mbar_wait_warp(bar(C::bSFull + qi), (uint32_t)j & 1, abort_flag, kTimeoutNs);
+          if (!ok) {
+            // keep meeting the partner at every exchange so it never waits alone
+            named_bar_sync(pair_bar, 64);
+            continue;
+          }
+          tc_fence_after();
+          uint32_t uu[2][32];
+          tmem_ld32(tS + part * 64, uu[0]);
+          tmem_ld32(tS + part * 64 + 32, uu[1]);
+          if (relay && qi == ntile - 1) {
+            mbar_arrive(bar(C::bDone + rd));
+            if (++rd == C::kKBuf) rd = 0;
+          }
+          tmem_ld_wait();
+          reg_fence(uu[0]);
+          reg_fence(uu[1]);
+          // tiles the causal rule cuts for this query tile, and ragged tails
+          const bool all_allowed = !g.causal || kv.lo + kv.valid - 1 <= qt_lo;
+          if (!(all_allowed && kv.valid == kTile)) {
+            const int lim = (g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid) - part * 64;
+  #pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c >= lim) uu[c / 32][c % 32] = __float_as_uint(-INFINITY);
+          }
+          float m8[8];
+  #pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
+          max_chunk(uu[0], m8);
+          max_chunk(uu[1], m8);
+          red_e[part * 128 + row] = max8(m8);
+          tc_fence_before();
+          named_bar_sync(pair_bar, 64);
+          tc_fence_after();
+          const float mx = fmaxf(red_e[row], red_e[128 + row]);
+          const float m_new = fmaxf(m_run[qi], mx * sl2);
+          const bool resc = m_new > m_run[qi] + kRescaleLog2;
+          float alpha = 1.f;
+          if (resc) {
+            alpha = ex2_approx(m_run[qi] - m_new);     // 0 when m_run = -inf
+            m_run[qi] = m_new;
+            l_run[qi] *= alpha;
+          }
+          const float m_use = (m_run[qi] == -INFINITY) ? 0.f : m_run[qi];
+          const uint64_t neg_m2 = pack2(-m_use, -m_use);
+          uint64_t sum2a = pack2(0.f, 0.f), sum2b = sum2a;
+          // P of this part's 64 keys: TMEM columns 32p..32p+31 of S_i
+          exp_chunk(uu[0], sl2x2, neg_m2, sum2a, sum2b, tS + part * 32);
+          exp_chunk(uu[1], sl2x2, neg_m2, sum2a, sum2b, tS + part * 32 + 16);
+          {
+            float a0, a1;
+            unpack2(fadd2(sum2a, sum2b), a0, a1);
+            l_run[qi] += a0 + a1;
+          }
+          // O_i is scaled by alpha before P_i(j) V_j is added to it; PV_i(j-1)
+          // is done (S_i(j)'s completion covers it). Both parts take the same
+          // decision for a row.
+          if (__any_sync(0xffffffffu, resc) && j > 0)
+            scale_cols<D / 2>(tmem + t_lane + kOCol + (uint32_t)(qi * D + part * (D / 2)), alpha);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(C::bPFull + qi));
+        }
+        ++j;
+        have = it.next(g, kv);
       }
-      if (row_valid && lse && part == 0 &&
-          in_range((long long)(lrow + q_pos), 1, extent_lse(gp), status))
-        lse[lrow + q_pos] =
-            l_tot > 0.f ? (m_run[qi] + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
+      if (log0 && in_range(log_off(0), 1, log_len, status)) log0[0] = n_log0;
+      if (log1 && in_range(log_off(1), 1, log_len, status)) log1[0] = n_log1;
+      // a second query tile of padding only has an empty record
+      if (log0 && !two && tile1_exists && in_range(log_off(1), 1, log_len, status))
+        vlog[log_off(1)] = 0;
+
+      // ---- epilogue: out = O / l, lse = ln2 * (m + log2 l), l = sum of both parts
+      float* red_l = red + 512;
+      for (int qi = 0; qi < ntile; ++qi) red_l[(qi * 2 + part) * 128 + row] = l_run[qi];
+      named_bar_sync(pair_bar, 64);
+      for (int qi = 0; qi < ntile; ++qi) {
+        const float l_tot = red_l[qi * 256 + row] + red_l[qi * 256 + 128 + row];
+        const int qt_lo = q_lo + qi * kTile;
+        const int q_pos = qt_lo + row;
+        const bool row_valid = row < min(kTile, q_valid - qi * kTile);
+        if (ok && j > 0) {
+          ok = mbar_wait_warp(bar(C::bODone + qi), 0, abort_flag, kTimeoutNs);
+          tc_fence_after();
+        }
+        if (!ok) break;
+        const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+        const uint32_t tO = tmem + t_lane + kOCol + (uint32_t)(qi * D + part * (D / 2));
+        if (kTmaOut && tma_out && q_valid - qi * kTile >= kTile) {
+          // a full tile: staged in Q_i's buffer (every MMA reading it is done)
+          // and written by one TMA store of whole rows
+          const uint32_t tile_smem = base + C::kQOff + (uint32_t)(qi * C::kTileBytes);
+          stage_out_row<D / 2>(tO, j > 0, tile_smem, row, part * (D / 2), inv_l);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(C::bStaged + qi));   // the producer stores it
+        } else {
+          const size_t row_off = ((orow + q_pos) * g.H_q + h) * D + part * (D / 2);
+          const bool store = row_valid && in_range((long long)row_off, D / 2, extent_q(gp), status);
+          store_out_row<D / 2, kOutF32>(tO, j > 0, store, out, row_off, inv_l);
+        }
+        if (row_valid && lse && part == 0 &&
+            in_range((long long)(lrow + q_pos), 1, extent_lse(gp), status))
+          lse[lrow + q_pos] =
+              l_tot > 0.f ? (m_run[qi] + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
+      }
     }
   }
 
   // ---- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == R::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -785,7 +962,7 @@ ra_status launch_typed(const Geometry& g, const CUtensorMap& mq, const CUtensorM
   // one block of two query tiles per CTA
   const long long grid = (long long)g.n_seg * ((g.nt + 1) / 2) * g.B * g.H_q;
   if (grid > 0x7fffffffLL) return RA_ERR_RANGE;
-  kern<<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, gl, out, lse, vlog,
+  kern<<<(unsigned)grid, Roles<D>::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, gl, out, lse, vlog,
                                                             log_stride, status, tma_out ? 1 : 0);
   return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_LAUNCH;
 }
