@@ -49,19 +49,16 @@ MERGE_METRIC = "LSE merge GB/s (algorithmic bytes)"
 
 # ncu DRAM bytes (read + write) of one launch of the timed kernel, per
 # workload; an entry holds only while the kernel's sources have the digest
-# stored with it (see _kernel_digest). The forward's bytes were captured at
-# digest db34798df47de19e; the sources of the digest below differ from those
-# only in where a shared wait helper is defined, and compile to a
-# byte-identical sm_103a cubin.
+# stored with it (see _kernel_digest).
 TRAFFIC = {
-    "attn_tc": {"sha256_16": "caec5a53bfb663e5", "bytes_per_launch": {
-        "bf16_s32k_causal_zigzag": 845280256 + 256100864,
-        "bf16_s16k_d64": 402865920 + 119390464,
-        "bf16_s128k_gqa_causal": 2730051328 + 1058496768,
-        "bf16_s4k_causal": 108359424 + 10706432,
-        "bf16_s32760_uneven_causal_zigzag": 844002048 + 255716864,
-        "bf16_varlen_32k_causal_zigzag": 828577280 + 255613440,
-        "bf16_ulysses_s16k_b2_causal": 805553920 + 253317376,
+    "attn_tc": {"sha256_16": "419f638ff48490a0", "bytes_per_launch": {
+        "bf16_s32k_causal_zigzag": 846791168 + 255732992,
+        "bf16_s16k_d64": 402796032 + 119514368,
+        "bf16_s128k_gqa_causal": 2724986368 + 1058387712,
+        "bf16_s4k_causal": 105313536 + 10988800,
+        "bf16_s32760_uneven_causal_zigzag": 845622016 + 255803648,
+        "bf16_varlen_32k_causal_zigzag": 828308736 + 255260672,
+        "bf16_ulysses_s16k_b2_causal": 805500160 + 253177088,
     }},
     # the merge was captured on S = 8192 (1.15 GiB on the device) and scaled by
     # 65536 / 8192 = 8: a streaming kernel whose bytes grow with the rows
