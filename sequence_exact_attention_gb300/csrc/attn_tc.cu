@@ -673,9 +673,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           const bool cut = !(all_allowed && kv.valid == kTile);
           const int lim = (g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid) - part * 64;
           float m8[8];
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t u[32];
             tmem_ld32(tS + part * 64 + c * 32, u);
@@ -686,7 +686,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             tmem_ld_wait();
             reg_fence(u);
             if (cut) {
-  #pragma unroll
+#pragma unroll
               for (int i = 0; i < 32; ++i)
                 if (c * 32 + i >= lim) u[i] = __float_as_uint(-INFINITY);
             }
@@ -709,14 +709,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           // the scores again, 32 at a time; P of chunk c (bf16 pairs) goes to
           // this part's own columns 64p + 16c .. 64p + 16c + 15, which hold
           // scores already read
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t u[32];
             tmem_ld32(tS + part * 64 + c * 32, u);
             tmem_ld_wait();
             reg_fence(u);
             if (cut) {
-  #pragma unroll
+#pragma unroll
               for (int i = 0; i < 32; ++i)
                 if (c * 32 + i >= lim) u[i] = __float_as_uint(-INFINITY);
             }
@@ -813,7 +813,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
               in_range(log_off(1) + 1 + 4 * n_log1, 4, log_len, status))
             log_visit(log1, n_log1++, kv, tile_class(g, q_lo + kTile, kv));
         }
-  #pragma unroll
+#pragma unroll
         for (int qi = 0; qi < 2; ++qi) {
           if (qi >= ntile) break;
           const uint32_t tS = tmem + t_lane + (uint32_t)(qi * kTile);
@@ -842,12 +842,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           const bool all_allowed = !g.causal || kv.lo + kv.valid - 1 <= qt_lo;
           if (!(all_allowed && kv.valid == kTile)) {
             const int lim = (g.causal ? min(kv.valid, q_pos - kv.lo + 1) : kv.valid) - part * 64;
-  #pragma unroll
+#pragma unroll
             for (int c = 0; c < 64; ++c)
               if (c >= lim) uu[c / 32][c % 32] = __float_as_uint(-INFINITY);
           }
           float m8[8];
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
           max_chunk(uu[0], m8);
           max_chunk(uu[1], m8);
