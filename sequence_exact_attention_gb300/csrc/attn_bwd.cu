@@ -77,7 +77,7 @@ struct Cfg {
   // TMEM allocation never waits for another CTA.
   static constexpr int kSmemBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
   static constexpr int bFix = 0;
-  static constexpr int bFull = 1;     // [2] stage loaded
+  static constexpr int bFull = 1;     // [2] stage's Q and lse2 loaded
   static constexpr int bFree = 3;     // [2] stage no longer read by the tensor cores
   static constexpr int bS = 5;        // S^T in TMEM
   static constexpr int bDP = 6;       // dP^T in TMEM
@@ -85,6 +85,7 @@ struct Cfg {
   static constexpr int bDS = 8;       // 256 arrivals: pass 2 done (dS^T stored)
   static constexpr int bAccK = 10;    // the last visit's dV and dK done
   static constexpr int bFinal = 11;
+  static constexpr int bFullDO = 12;  // [2] stage's dO and delta loaded
   static constexpr int kHolderOff = kBarBytes - 16;
   static constexpr int kNeverOff = kBarBytes - 12;
   static constexpr int kAbortOff = kBarBytes - 8;
@@ -161,6 +162,7 @@ __device__ __forceinline__ void init_barriers(BarFn bar, volatile int* abort_fla
     mbar_init(bar(C::bFix), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(C::bFull + i), 1);
+      mbar_init(bar(C::bFullDO + i), 1);
       mbar_init(bar(C::bFree + i), 1);
     }
     mbar_init(bar(C::bS), 1);
@@ -333,22 +335,27 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
           break;
         const uint32_t sb = base + C::kStage0 + st * C::kStageBytes;
         const SegRows qr = seg_rows(gp, b, qt.seg, row0, kVarlen);
-        mbar_arrive_expect_tx(bar(C::bFull + st), 2 * C::kTileBytes + C::kStatBytes);
-        for (int bx = 0; bx < C::kBoxes; ++bx) {
-          tma_load_4d(sb + bx * kBoxBytes, &tm_q, bar(C::bFull + st), bx * 64, qt.h,
-                      qr.trow + qt.lo, qr.tbat);
-          tma_load_4d(sb + C::kTileBytes + bx * kBoxBytes, &tm_do, bar(C::bFull + st), bx * 64,
-                      qt.h, qr.trow + qt.lo, qr.tbat);
-        }
         long long wi = ws_tile(gp, b * gp.H_q + qt.h, qt.seg, qt.ti);
         if (!in_range(wi, kT, ws_tile(gp, gp.B * gp.H_q, 0, 0), status)) wi = 0;
+        // Q and lse2 first, on a barrier of their own: S^T needs only them;
+        // dO and delta follow for dP^T and the second pass
+        mbar_arrive_expect_tx(bar(C::bFull + st), C::kTileBytes + kT * 4);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_4d(sb + bx * kBoxBytes, &tm_q, bar(C::bFull + st), bx * 64, qt.h,
+                      qr.trow + qt.lo, qr.tbat);
         bulk_load(sb + 2 * C::kTileBytes, lse2 + wi, kT * 4, bar(C::bFull + st));
-        bulk_load(sb + 2 * C::kTileBytes + kT * 4, delta + wi, kT * 4, bar(C::bFull + st));
+        mbar_arrive_expect_tx(bar(C::bFullDO + st), C::kTileBytes + kT * 4);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_4d(sb + C::kTileBytes + bx * kBoxBytes, &tm_do, bar(C::bFullDO + st), bx * 64,
+                      qt.h, qr.trow + qt.lo, qr.tbat);
+        bulk_load(sb + 2 * C::kTileBytes + kT * 4, delta + wi, kT * 4, bar(C::bFullDO + st));
         ++j;
       }
       // every issued copy lands before the CTA leaves
-      for (int jj = (j > 2 ? j - 2 : 0); jj < j; ++jj)
+      for (int jj = (j > 2 ? j - 2 : 0); jj < j; ++jj) {
         mbar_wait(bar(C::bFull + (jj & 1)), (uint32_t)(jj >> 1) & 1, never, kTimeoutNs);
+        mbar_wait(bar(C::bFullDO + (jj & 1)), (uint32_t)(jj >> 1) & 1, never, kTimeoutNs);
+      }
       mbar_wait(bar(C::bFix), 0, never, kTimeoutNs);
     }
     __syncwarp();
@@ -402,6 +409,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int st = j & 1;
         const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
         const uint64_t dob = do_kmaj + so, domn = do_mn + so, qmn = q_mn + so;
+        ok = mbar_wait_warp(bar(C::bFullDO + st), (uint32_t)(j >> 1) & 1, abort_flag, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
