@@ -37,7 +37,9 @@
 // and the tensor core runs, per key tile j, PV0(j) S0(j+1) PV1(j) S1(j+1), so
 // while the softmax works on one tile the tensor core runs the other tile's
 // PV and S: with a softmax shorter than two products the tensor core never
-// waits. S_i(j+1) overwrites P_i(j) right behind PV_i(j), which reads it:
+// waits (at D = 64 the two tiles' softmax groups also run side by side, as
+// the products there are short). S_i(j+1) overwrites P_i(j) right behind
+// PV_i(j), which reads it:
 // one thread issues both, and the tensor core executes the MMAs of a thread
 // in issue order, so the read of P_i(j) precedes the write of S_i(j+1).
 //
